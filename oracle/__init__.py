@@ -1,0 +1,208 @@
+"""Plain fp64 CPU oracle for the paged-KV chunk attention with a shared
+Transformer-XL relative-position term.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+with the CUDA library (``paged_kv_chunk_gb300``) and imports nothing from it.
+
+The arithmetic lives in ``oasr_oracle.c`` (plain loops in double); this module
+only builds it with the host C compiler and marshals numpy arrays into it.
+
+Sources (OASR documentation pages):
+  * Scheduler page, section 4.3 "Heterogeneous-offset batching": the score is the
+    content score plus the rel-pos bias matrix_bd / sqrt(d_k), masked per stream
+    by its cache_seqlens.
+  * Model Layer page, table "Three optional encoder declarations", row
+    fixed_attention_window: one Transformer-XL table whose distances are
+    cache + i - j, shared by a cohort with uniform cache_seqlens.
+  * Model Layer page, Nemotron ASR section: Transformer-XL relative position
+    with rel_shift (row 0 of the table holds the largest distance).
+  * ASR Engine page, section 4.3 "Batched paged forward": block_table (B,
+    blocks_per_seq) and cache_seqlens (B,) shared by all layers; the caller
+    commits the cache length after the step.
+  * ASR Engine page, section 4.1: packed micro-batches are one gapless
+    varlen-attention row.
+
+Parity pins (what ties this oracle to something other than itself) live in
+``tests/test_oracle_pins.py``; every function here is pinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oasr_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboasr_oracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oasr_oracle.c`` into ``oracle/_build/liboasr_oracle.so``.
+
+    Uses gcc with OpenMP when the compiler accepts it, else a serial build.
+    Returns the path of the shared library.
+    """
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-fPIC", "-shared", "-std=c99", "-o", tmp, _SRC, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        L = ctypes.c_long
+        Dbl = ctypes.c_double
+        lib.oracle_paged_append.restype = L
+        lib.oracle_paged_append.argtypes = [P, P, P, P, I, I, P, I, P, I, I, I, I, I]
+        lib.oracle_chunk_relattn.restype = L
+        lib.oracle_chunk_relattn.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I,
+                                             Dbl, P, L, P]
+        lib.oracle_packed_relattn.restype = L
+        lib.oracle_packed_relattn.argtypes = [P, P, P, P, I, I, P, P, P, I, I, I, Dbl,
+                                              P, L, P]
+        lib.oracle_num_threads.restype = I
+        lib.oracle_num_threads.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _f32(a) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    """Threads the compiled oracle uses (OpenMP max threads, or 1)."""
+    return int(_load().oracle_num_threads())
+
+
+def paged_append(k_new, v_new, k_pool, v_pool, block_table, cache_seqlens) -> int:
+    """Write the chunk rows into the pools in place (byte copy); see the C file.
+
+    k_new, v_new: [B, T, H, D]; k_pool, v_pool: [num_blocks, bs, H, D] of the
+    same dtype (any fixed-size dtype: float32, or uint16 holding bf16 bits);
+    block_table: int32 [B, max_blocks_per_seq]; cache_seqlens: int32 [B].
+    Returns the number of (b, t, h) rows that were not written because their
+    block lies outside the table or the pool.
+    """
+    lib = _load()
+    k_new = np.ascontiguousarray(k_new)
+    v_new = np.ascontiguousarray(v_new, dtype=k_new.dtype)
+    for pool in (k_pool, v_pool):
+        if not (pool.flags.c_contiguous and pool.dtype == k_new.dtype):
+            raise ValueError("pools must be C-contiguous and of the chunk's dtype")
+    B, T, H, D = k_new.shape
+    nb, bs, H2, D2 = k_pool.shape
+    if (H2, D2) != (H, D) or v_pool.shape != k_pool.shape:
+        raise ValueError("pool shape does not match the chunk")
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    cs = np.ascontiguousarray(cache_seqlens, dtype=np.int32)
+    if bt.ndim != 2 or bt.shape[0] != B or cs.shape != (B,):
+        raise ValueError("block_table must be [B, max_blocks_per_seq], cache_seqlens [B]")
+    return int(lib.oracle_paged_append(_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+                                       nb, bs, _ptr(bt), bt.shape[1], _ptr(cs),
+                                       B, T, H, D, k_new.dtype.itemsize))
+
+
+def chunk_relattn(q, cache_k, cache_v, k_new, v_new, pos_bias_u, pos_bias_v, rel,
+                  scale=None, rows=None) -> np.ndarray:
+    """Streaming chunk attention over an un-paged cache, in float64.
+
+    q, k_new, v_new: [B, T, H, D]; cache_k, cache_v: [B, C, H, D] (C may be 0);
+    pos_bias_u, pos_bias_v: [H, D]; rel: [R, H, D] with R >= C + 2T - 1 and
+    z = R - T.  scale defaults to 1/sqrt(D).  rows: optional int array [n, 3]
+    of (b, i, h) to compute; other rows of the result are NaN.
+    Returns out [B, T, H, D] float64.
+    """
+    lib = _load()
+    q = _f32(q)
+    B, T, H, D = q.shape
+    k_new, v_new = _f32(k_new), _f32(v_new)
+    cache_k, cache_v = _f32(cache_k), _f32(cache_v)
+    C = cache_k.shape[1]
+    if cache_k.shape != (B, C, H, D) or cache_v.shape != (B, C, H, D):
+        raise ValueError("cache must be [B, C, H, D]")
+    if k_new.shape != q.shape or v_new.shape != q.shape:
+        raise ValueError("k_new, v_new must be [B, T, H, D]")
+    u, vb, rel = _f32(pos_bias_u), _f32(pos_bias_v), _f32(rel)
+    if u.shape != (H, D) or vb.shape != (H, D) or rel.ndim != 3 or rel.shape[1:] != (H, D):
+        raise ValueError("pos biases must be [H, D] and rel [R, H, D]")
+    R = rel.shape[0]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    out = np.full((B, T, H, D), np.nan, dtype=np.float64)
+    if rows is not None:
+        rows = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 3)
+        rp, nr = _ptr(rows), rows.shape[0]
+    else:
+        rp, nr = None, 0
+    bad = lib.oracle_chunk_relattn(_ptr(q), _ptr(cache_k), _ptr(cache_v), _ptr(k_new),
+                                   _ptr(v_new), _ptr(u), _ptr(vb), _ptr(rel), R, B, T, C,
+                                   H, D, float(scale), rp, nr, _ptr(out))
+    if bad:
+        raise ValueError(f"rel table too short: {bad} rows need rows outside [0, {R})")
+    return out
+
+
+def packed_relattn(q, k, v, cu_seqlens, pos_bias_u, pos_bias_v, rel, scale=None,
+                   rows=None) -> np.ndarray:
+    """Packed varlen bidirectional attention over one gapless row, in float64.
+
+    q, k, v: [total, H, D]; cu_seqlens: int [num_seqs + 1] starting at 0;
+    rel: [R, H, D] with z = (R - 1) // 2 and R >= 2 * max_seqlen - 1.
+    rows: optional int array [n, 2] of (token, h); other rows are NaN.
+    Returns out [total, H, D] float64.
+    """
+    lib = _load()
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    total, H, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share their shape")
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    if cu.ndim != 1 or cu.shape[0] < 1 or cu[0] != 0 or cu[-1] != total or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens must start at 0, end at total and not decrease")
+    u, vb, rel = _f32(pos_bias_u), _f32(pos_bias_v), _f32(rel)
+    if u.shape != (H, D) or vb.shape != (H, D) or rel.ndim != 3 or rel.shape[1:] != (H, D):
+        raise ValueError("pos biases must be [H, D] and rel [R, H, D]")
+    R = rel.shape[0]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    out = np.full((total, H, D), np.nan, dtype=np.float64)
+    if rows is not None:
+        rows = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 2)
+        rp, nr = _ptr(rows), rows.shape[0]
+    else:
+        rp, nr = None, 0
+    bad = lib.oracle_packed_relattn(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), cu.shape[0] - 1,
+                                    total, _ptr(u), _ptr(vb), _ptr(rel), R, H, D,
+                                    float(scale), rp, nr, _ptr(out))
+    if bad:
+        raise ValueError(f"{bad} rows need rel rows outside [0, {R}) or lie in no segment")
+    return out
