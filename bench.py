@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Benchmark of the streaming encoder step's paged-KV chunk attention on GB300.
+
+A step is one streaming encoder step of a lockstep cohort through `layers` attention
+layers: per layer, the new chunk's K/V are appended into that layer's block-paged pool
+and the chunk attends over cache + chunk with the shared Transformer-XL rel-pos term
+(one fused launch per layer, oasr_chunk_step_paged).  Each layer has its own pools and
+inputs, so the step's working set is several times the 129 MB L2 and no layer is
+served from the previous one's cache.
+
+Prints one JSON line (rank 0).  `value` is encoder frames per second per attention layer
+(B*T*layers*steps / time) over all ranks, timed on the device with CUDA events around
+CUDA-graph replays of the step, inputs resident in HBM.  `e2e` is the same metric with the
+step's inputs copied from pinned host memory and its outputs copied back inside the
+timed region.  `roofline` relates the fused kernel's algorithmic bytes to its average
+launch time and the measured HBM peak.  `cpu_baseline` times the fp64 CPU oracle on a
+bounded sample of the same workload.
+
+--impl reference times the oracle itself on the host cores as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_chunk_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = "encoder frames/s per attention layer and achieved HBM GB/s vs GB300 peak"
+UNIT = "frames/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["chunk_attn.cu", "attn_core.cuh", "ptx.cuh"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="conformer_small", choices=sorted(syn.STREAMING_CONFIGS))
+    ap.add_argument("--layers", type=int, default=0,
+                    help="distinct layer pools per step (0: enough for 4x L2)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work of the cpu_baseline sample (0 disables it)")
+    ap.add_argument("--soak-seconds", type=float, default=1.5,
+                    help="untimed replays before the timed region, for the clock record")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- helpers
+
+
+def workload_bytes(cfg, fused=True):
+    """Algorithmic HBM bytes of one layer step (one launch of the fused kernel)."""
+    es = 2 if cfg.dtype == "bf16" else 4
+    row = cfg.H * cfg.D * es
+    chunk = cfg.B * cfg.T * row
+    b = 2 * chunk                       # read k_new, v_new
+    b += 2 * chunk                      # write them into the pools
+    b += 2 * cfg.B * cfg.C * row        # read the cached K/V
+    if not fused:
+        b += 2 * chunk                  # re-read the appended chunk
+    b += chunk                          # read q
+    b += cfg.R * row                    # read the shared rel table once
+    b += chunk                          # write out
+    return b
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_chunk_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(cfg_name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"chunk_step_{cfg_name}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not (m_sha and m_tr) or m_sha.group(1) != source_digest():
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = list(csv.reader(io.StringIO(self.tmp.read())))
+        self.tmp.close()
+        os.unlink(self.tmp.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+
+
+def oracle_layer_inputs(cfg, seed):
+    x = syn.streaming_inputs(cfg, seed)
+    kp = syn.canary_pool(x["num_blocks"], cfg.block_size, cfg.H, cfg.D, cfg.dtype)
+    vp = kp.copy()
+    return x, kp, vp
+
+
+def oracle_layer_step(oracle, cfg, x, kp, vp):
+    """One layer step on the CPU oracle: append the chunk, then chunk attention."""
+    oracle.paged_append(syn.to_bits(x["k_new"], cfg.dtype), syn.to_bits(x["v_new"], cfg.dtype),
+                        kp, vp, x["block_table"], x["cache_seqlens"])
+    oracle.chunk_relattn(x["q"], x["cache_k"], x["cache_v"], x["k_new"], x["v_new"],
+                         x["pos_bias_u"], x["pos_bias_v"], x["rel"])
+
+
+def cpu_baseline(cfg, seconds):
+    import oracle
+    oracle.build()
+    x, kp, vp = oracle_layer_inputs(cfg, cfg.seed)
+    oracle_layer_step(oracle, cfg, x, kp, vp)   # untimed first call
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_layer_step(oracle, cfg, x, kp, vp)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": cfg.B * cfg.T * n / el, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n} layer steps (append + chunk attention of all {cfg.B} streams x "
+                      f"{cfg.H} heads, one layer) of the {cfg.name} cohort, {el:.1f} s, "
+                      "fp64 C oracle with OpenMP"}
+
+
+def run_reference(args, cfg, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    x, kp, vp = oracle_layer_inputs(cfg, cfg.seed)
+    for _ in range(args.warmup):
+        oracle_layer_step(oracle, cfg, x, kp, vp)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_layer_step(oracle, cfg, x, kp, vp)
+    el = time.perf_counter() - t0
+    value = cfg.B * cfg.T * args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{cfg.name}_streaming", "B": cfg.B, "H": cfg.H, "D": cfg.D,
+                   "T": cfg.T, "cache": cfg.C, "block_size": cfg.block_size, "layers": 1},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: one layer (append + chunk attention) of the "
+                                   f"{cfg.name} cohort on the fp64 C oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+
+def run_ours(args, cfg, rank, world, local):
+    from paged_kv_chunk_gb300 import build as pkg_build
+    from paged_kv_chunk_gb300 import capi
+    pkg_build.build()
+    capi.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    tdtype = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    es = 2 if cfg.dtype == "bf16" else 4
+    touched = workload_bytes(cfg)
+    layers = args.layers or max(1, math.ceil(4 * L2_BYTES / touched))
+    rng = np.random.default_rng(cfg.seed + 1000 * rank)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(cfg.seed + 7919 * rank)
+    B, T, H, D = cfg.B, cfg.T, cfg.H, cfg.D
+    nb, bs = cfg.pool_blocks, cfg.block_size
+
+    def dev_normal(shape):
+        return (torch.randn(shape, generator=gen, device=dev) * syn.SIGMA).to(tdtype)
+
+    pools = [(dev_normal((nb, bs, H, D)), dev_normal((nb, bs, H, D))) for _ in range(layers)]
+    params = [(dev_normal((H, D)), dev_normal((H, D)), dev_normal((cfg.R, H, D)))
+              for _ in range(layers)]
+    bt_h = syn.block_table(rng, B, cfg.mbps, nb)
+    cs_h = np.full((B,), cfg.C, np.int32)
+    bt = torch.from_numpy(bt_h).to(dev)
+    cs = torch.from_numpy(cs_h).to(dev)
+    # per-step inputs of every layer (q, k_new, v_new) and outputs, device-resident
+    x_h = torch.from_numpy(syn.normal(rng, (layers, 3, B, T, H, D), cfg.dtype)).to(tdtype)
+    x_d = x_h.to(dev)
+    out_d = torch.empty((layers, B, T, H, D), dtype=tdtype, device=dev)
+
+    def step_calls(x, out):
+        for l in range(layers):
+            kp, vp = pools[l]
+            u, vb, rel = params[l]
+            capi.oasr_chunk_step_paged(x[l, 0], x[l, 1], x[l, 2], kp, vp, bt, cs, u, vb, rel,
+                                       out=out[l])
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        step_calls(x_d, out_d)              # eager once: kernel attributes, lazy loading
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step_calls(x_d, out_d)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        t_end = time.perf_counter() + args.soak_seconds
+        while time.perf_counter() < t_end:
+            for _ in range(20):
+                graph.replay()
+            stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    clocks = sampler.stop() if sampler else None
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, world)
+    frames = B * T * layers * args.steps * world
+    value = frames / (ms_max / 1e3)
+    launch_us = 1e3 * ms / (args.steps * layers)
+
+    # ---- end to end: pinned host inputs -> device, the step, outputs -> pinned host
+    e2e = None
+    if not args.no_e2e:
+        x_pin = x_h.pin_memory()
+        out_pin = torch.empty(out_d.shape, dtype=tdtype).pin_memory()
+        bt_pin = torch.from_numpy(bt_h).pin_memory()
+        cs_pin = torch.from_numpy(cs_h).pin_memory()
+
+        def e2e_step():
+            x_d.copy_(x_pin, non_blocking=True)
+            bt.copy_(bt_pin, non_blocking=True)
+            cs.copy_(cs_pin, non_blocking=True)
+            graph.replay()
+            out_pin.copy_(out_d, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup)):
+                e2e_step()
+            torch.cuda.synchronize()
+            barrier(world)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            w0 = time.perf_counter()
+            e0.record(stream)
+            for _ in range(args.steps):
+                e2e_step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            wall = time.perf_counter() - w0
+            barrier(world)
+        e_ms = max(e0.elapsed_time(e1), 1e3 * wall)
+        e_ms = max_over_ranks(e_ms, world)
+        h2d = x_pin.numel() * es + bt_pin.numel() * 4 + cs_pin.numel() * 4
+        e2e = {"value": frames / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(out_pin.numel() * es),
+               "path": "pinned host inputs -> H2D copy -> CUDA-graph replay of the per-layer "
+                       "oasr_chunk_step_paged calls -> D2H copy of the outputs, one stream"}
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_hbm_peak()
+    achieved = touched / (launch_us * 1e-6) / 1e9
+    traffic = profiled_traffic(cfg.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+        "config": {"workload": f"{cfg.name}_streaming", "B": B, "H": H, "D": D, "T": T,
+                   "cache": cfg.C, "block_size": bs, "pool_blocks": nb, "rel_rows": cfg.R,
+                   "layers": layers, "global_batch": B * world, "seq_len": cfg.K,
+                   "parallelism": f"dp{world}",
+                   "l2": f"inputs larger than L2: {layers} distinct layer pools, "
+                         f"{layers * touched / 1e6:.0f} MB touched per step",
+                   "timing": "CUDA events around graph replays of the step on the launching stream",
+                   "soak_s": args.soak_seconds},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "chunk_attn_bf16_kernel (fused append + attention)",
+                     "algorithmic_bytes_per_launch": touched,
+                     "avg_launch_us": launch_us, "peak_kind": peak_kind},
+        "gpu_launches": args.steps * layers,
+        "clocks": clocks,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if world == 1 and args.cpu_seconds > 0:
+        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    cfg = syn.STREAMING_CONFIGS[args.config]
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, cfg, rank, int(os.environ.get("WORLD_SIZE", "1")))
+        return
+    rank, world, local = dist_setup()
+    run_ours(args, cfg, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,214 @@
+"""Python binding of the C ABI in ``include/oasr_attn.h`` (``liboasr_attn.so``).
+
+Argument marshalling only: each function checks that the torch tensors it is given
+live on the current CUDA device with the layout the C ABI documents, derives the
+sizes from their shapes and passes raw device pointers plus the current CUDA stream.
+Every step of the computation runs in the library's CUDA kernels; there is no other
+path, and a missing library raises instead of falling back.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liboasr_attn.so")
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "oasr_attn.h")
+
+OASR_OK, OASR_ERR_INVALID_ARG, OASR_ERR_UNSUPPORTED, OASR_ERR_CUDA = 0, 1, 2, 3
+OASR_ERR_BOUNDS, OASR_ERR_TIMEOUT = 4, 5
+OASR_F32, OASR_BF16 = 0, 1
+STATUS_BOUNDS_BIT, STATUS_TIMEOUT_BIT = 1, 2
+
+_lock = threading.Lock()
+_lib = None
+
+
+class OasrError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {msg} (status {status})")
+        self.status = status
+
+
+def load() -> ctypes.CDLL:
+    """Load liboasr_attn.so (built by ``paged_kv_chunk_gb300.build``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built: run `python -m paged_kv_chunk_gb300.build`"
+                               " (or __graft_entry__.build()) first")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+        L.oasr_paged_append.argtypes = [P, P, P, P, I, I, P, I, P, I, I, I, I, I, S]
+        L.oasr_chunk_relattn_paged.argtypes = [P, P, P, I, I, P, I, P, P, P, P, I, P, I, I, I, I,
+                                               F, I, S]
+        L.oasr_chunk_step_paged.argtypes = [P, P, P, P, P, I, I, P, I, P, P, P, P, I, P, I, I, I,
+                                            I, F, I, S]
+        L.oasr_packed_relattn_varlen.argtypes = [P, P, P, P, I, I, I, P, P, P, I, P, I, I, F, I, S]
+        for fn in ("oasr_paged_append", "oasr_chunk_relattn_paged", "oasr_chunk_step_paged",
+                   "oasr_packed_relattn_varlen"):
+            getattr(L, fn).restype = I
+        L.oasr_status_string.argtypes = [I]
+        L.oasr_status_string.restype = ctypes.c_char_p
+        L.oasr_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
+        L.oasr_device_status.restype = I
+        L.oasr_version.argtypes = []
+        L.oasr_version.restype = I
+        _lib = L
+        return L
+
+
+def header_symbols() -> list[str]:
+    """Names of the functions ``include/oasr_attn.h`` declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(oasr_[a-z0-9_]+)\s*\(", text)))
+
+
+def _check(fn: str, status: int):
+    if status != OASR_OK:
+        msg = load().oasr_status_string(status).decode()
+        raise OasrError(fn, status, msg)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return OASR_BF16
+    if t.dtype == torch.float32:
+        return OASR_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: bf16 or float32")
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, ndim=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def oasr_paged_append(k_new, v_new, k_pool, v_pool, block_table, cache_seqlens, stream=None):
+    """Write the chunk (k_new, v_new [B,T,H,D]) into the pools [nb,bs,H,D] in place."""
+    L = load()
+    dt = _dtype_code(k_new)
+    B, T, H, D = k_new.shape
+    nb, bs = k_pool.shape[:2]
+    if tuple(v_new.shape) != (B, T, H, D) or tuple(k_pool.shape[2:]) != (H, D) \
+            or v_pool.shape != k_pool.shape:
+        raise ValueError("shape mismatch between chunk and pools")
+    if tuple(block_table.shape[:1]) != (B,) or tuple(cache_seqlens.shape) != (B,):
+        raise ValueError("block_table must be [B, mbps] and cache_seqlens [B]")
+    _check("oasr_paged_append", L.oasr_paged_append(
+        _dev(k_new, "k_new", k_new.dtype, 4), _dev(v_new, "v_new", k_new.dtype, 4),
+        _dev(k_pool, "k_pool", k_new.dtype, 4), _dev(v_pool, "v_pool", k_new.dtype, 4), nb, bs,
+        _dev(block_table, "block_table", torch.int32, 2), block_table.shape[1],
+        _dev(cache_seqlens, "cache_seqlens", torch.int32, 1), B, T, H, D, dt, _stream(stream)))
+
+
+def _chunk_common(q, k_pool, block_table, cache_seqlens, pos_bias_u, pos_bias_v, rel, out):
+    B, T, H, D = q.shape
+    if k_pool.dim() != 4 or tuple(k_pool.shape[2:]) != (H, D):
+        raise ValueError("k_pool must be [num_blocks, block_size, H, D]")
+    if tuple(pos_bias_u.shape) != (H, D) or tuple(pos_bias_v.shape) != (H, D):
+        raise ValueError("pos biases must be [H, D]")
+    if rel.dim() != 3 or tuple(rel.shape[1:]) != (H, D):
+        raise ValueError("rel must be [R, H, D]")
+    if tuple(out.shape) != (B, T, H, D) or out.dtype != q.dtype:
+        raise ValueError("out must be [B, T, H, D] of q's dtype")
+    if block_table.dim() != 2 or block_table.shape[0] != B or tuple(cache_seqlens.shape) != (B,):
+        raise ValueError("block_table must be [B, mbps] and cache_seqlens [B]")
+    return B, T, H, D
+
+
+def oasr_chunk_relattn_paged(q, k_pool, v_pool, block_table, cache_seqlens, pos_bias_u,
+                             pos_bias_v, rel, out=None, scale=None, stream=None):
+    """Streaming chunk attention over the paged pool; returns out [B,T,H,D]."""
+    L = load()
+    dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty_like(q)
+    B, T, H, D = _chunk_common(q, k_pool, block_table, cache_seqlens, pos_bias_u, pos_bias_v,
+                               rel, out)
+    scale = D ** -0.5 if scale is None else float(scale)
+    _check("oasr_chunk_relattn_paged", L.oasr_chunk_relattn_paged(
+        _dev(q, "q", q.dtype), _dev(k_pool, "k_pool", q.dtype), _dev(v_pool, "v_pool", q.dtype),
+        k_pool.shape[0], k_pool.shape[1], _dev(block_table, "block_table", torch.int32),
+        block_table.shape[1], _dev(cache_seqlens, "cache_seqlens", torch.int32),
+        _dev(pos_bias_u, "pos_bias_u", q.dtype), _dev(pos_bias_v, "pos_bias_v", q.dtype),
+        _dev(rel, "rel", q.dtype), rel.shape[0], _dev(out, "out", q.dtype), B, T, H, D, scale, dt,
+        _stream(stream)))
+    return out
+
+
+def oasr_chunk_step_paged(q, k_new, v_new, k_pool, v_pool, block_table, cache_seqlens,
+                          pos_bias_u, pos_bias_v, rel, out=None, scale=None, stream=None):
+    """Fused append + streaming chunk attention; returns out [B,T,H,D]."""
+    L = load()
+    dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty_like(q)
+    B, T, H, D = _chunk_common(q, k_pool, block_table, cache_seqlens, pos_bias_u, pos_bias_v,
+                               rel, out)
+    if tuple(k_new.shape) != (B, T, H, D) or tuple(v_new.shape) != (B, T, H, D):
+        raise ValueError("k_new, v_new must be [B, T, H, D]")
+    scale = D ** -0.5 if scale is None else float(scale)
+    _check("oasr_chunk_step_paged", L.oasr_chunk_step_paged(
+        _dev(q, "q", q.dtype), _dev(k_new, "k_new", q.dtype), _dev(v_new, "v_new", q.dtype),
+        _dev(k_pool, "k_pool", q.dtype), _dev(v_pool, "v_pool", q.dtype), k_pool.shape[0],
+        k_pool.shape[1], _dev(block_table, "block_table", torch.int32), block_table.shape[1],
+        _dev(cache_seqlens, "cache_seqlens", torch.int32), _dev(pos_bias_u, "pos_bias_u", q.dtype),
+        _dev(pos_bias_v, "pos_bias_v", q.dtype), _dev(rel, "rel", q.dtype), rel.shape[0],
+        _dev(out, "out", q.dtype), B, T, H, D, scale, dt, _stream(stream)))
+    return out
+
+
+def oasr_packed_relattn_varlen(q, k, v, cu_seqlens, max_seqlen, pos_bias_u, pos_bias_v, rel,
+                               out=None, scale=None, stream=None):
+    """Packed varlen bidirectional rel-pos attention; returns out [total,H,D]."""
+    L = load()
+    dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty_like(q)
+    total, H, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape or out.shape != q.shape:
+        raise ValueError("q, k, v, out must share their shape [total, H, D]")
+    if tuple(pos_bias_u.shape) != (H, D) or tuple(pos_bias_v.shape) != (H, D):
+        raise ValueError("pos biases must be [H, D]")
+    if rel.dim() != 3 or tuple(rel.shape[1:]) != (H, D):
+        raise ValueError("rel must be [R, H, D]")
+    scale = D ** -0.5 if scale is None else float(scale)
+    _check("oasr_packed_relattn_varlen", L.oasr_packed_relattn_varlen(
+        _dev(q, "q", q.dtype), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype),
+        _dev(cu_seqlens, "cu_seqlens", torch.int32, 1), cu_seqlens.shape[0] - 1, int(max_seqlen),
+        total, _dev(pos_bias_u, "pos_bias_u", q.dtype), _dev(pos_bias_v, "pos_bias_v", q.dtype),
+        _dev(rel, "rel", q.dtype), rel.shape[0], _dev(out, "out", q.dtype), H, D, scale, dt,
+        _stream(stream)))
+    return out
+
+
+def oasr_device_status(clear: bool = True) -> int:
+    """Raw device status bits (1 = an index was out of range, 2 = a wait timed out)."""
+    L = load()
+    flags = ctypes.c_uint(0)
+    _check("oasr_device_status", L.oasr_device_status(ctypes.byref(flags), int(clear)))
+    return int(flags.value)
+
+
+def oasr_version() -> int:
+    return int(load().oasr_version())

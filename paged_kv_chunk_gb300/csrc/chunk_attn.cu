@@ -1,0 +1,443 @@
+// Streaming chunk attention over the block-paged pool, with the shared Transformer-XL
+// relative-position term (oasr_chunk_relattn_paged), and the fused append + attention
+// step (oasr_chunk_step_paged).
+//
+// Scheduler page, section 4.3 "Heterogeneous-offset batching": each stream's keys are
+// masked by its cache_seqlens and the rel-pos bias matrix_bd / sqrt(d_k) is added to the
+// content score.  Model Layer page, fixed_attention_window row: with uniform cache length
+// one table serves the cohort, distances cache + i - j; Nemotron ASR section: rel_shift
+// order, so the row for query i and key j is rho = (R - T - C) + j - i.
+//
+// bf16 path (the hot path): one CTA per (stream, head), 4 warps.  Keys are streamed in
+// stages of 64 through a TMA pipeline: each stage is one box per block-table page for K
+// and for V (the page's rows of this head, 128 B each, 128-byte swizzled) plus one box of
+// the rel band; all arrive on one mbarrier.  The per-stage math is in attn_core.cuh.
+// The fused variant first writes this head's slice of the chunk into the pool with
+// 16-byte stores, fences them against the async proxy, and only then issues the stages
+// that cover the chunk; stages that hold only cached keys are issued before the writes.
+//
+// f32 path: a SIMT kernel (one warp per query row, lanes over keys, fp32 FMA and expf).
+#include "attn_core.cuh"
+#include "host_common.h"
+
+namespace oasr {
+namespace {
+
+struct ChunkArgs {
+    const uint16_t* k_new;   // fused only
+    const uint16_t* v_new;   // fused only
+    uint16_t* k_pool;        // fused only
+    uint16_t* v_pool;        // fused only
+    const int32_t* block_table;
+    const int32_t* cache_seqlens;
+    const uint16_t* pos_bias_u;
+    const uint16_t* pos_bias_v;
+    uint16_t* out;
+    unsigned* status;
+    int num_blocks, block_size, mbps, T, H, R;
+    int box_rows;            // rows of one K/V TMA box = min(block_size, 64)
+    float scale_log2;        // scale * log2(e)
+};
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t x)
+{
+    return __uint_as_float(static_cast<uint32_t>(x) << 16);
+}
+
+template <int MT, int NS, bool FUSED>
+__global__ void __launch_bounds__(kThreads) chunk_attn_bf16_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
+    const ChunkArgs a)
+{
+    using TL = Tile<MT>;
+    using SP = SmemPlan<MT, NS>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sb = smem_addr(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.x / a.H, h = blockIdx.x - (blockIdx.x / a.H) * a.H;
+    const int T = a.T;
+    unsigned err = 0;
+
+    int C = __ldg(a.cache_seqlens + b);
+    if (C < 0) { C = 0; err |= kErrBounds; }
+    int K = C + T;
+    const int cap = a.mbps * a.block_size;
+    if (K > cap) { K = cap; err |= kErrBounds; }
+    const int n_stages = (K + kStageKeys - 1) / kStageKeys;
+    const int off = a.R - T - C;   // rho = off + j - i
+    const uint32_t bar_full = sb + SP::off_bar;
+    const uint32_t bar_q = bar_full + NS * 8;
+    float* s_u = reinterpret_cast<float*>(sm + SP::off_u);
+    float* s_vb = reinterpret_cast<float*>(sm + SP::off_vb);
+
+    if (tid == 0) {
+        for (int i = 0; i < NS; ++i) mbar_init(bar_full + 8 * i, 1);
+        mbar_init(bar_q, 1);
+        fence_mbar_init();
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_r);
+    }
+    __syncthreads();
+
+    // Issue stage s into buffer s % NS (thread 0 only).
+    auto issue = [&](int s) {
+        const int buf = s % NS;
+        const uint32_t bar = bar_full + 8 * buf;
+        const int j0 = s * kStageKeys;
+        const int box = a.box_rows;
+        int rows[kStageKeys / 8];
+        int nbox = 0;
+        for (int q = 0; q < kStageKeys / box; ++q) {
+            const int j = j0 + q * box;
+            if (j >= K) break;
+            const int lb = j / a.block_size;
+            const int slot = j - lb * a.block_size;
+            const int blk = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + lb);
+            if (blk < 0 || blk >= a.num_blocks) {
+                err |= kErrBounds;
+                rows[nbox++] = -2 * box;          // outside the pool: the box reads zeros
+            } else {
+                rows[nbox++] = blk * a.block_size + slot;
+            }
+        }
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>((2 * nbox * box + TL::RB) * kRowBytes));
+        const uint64_t pol = policy_evict_first();
+        for (int q = 0; q < nbox; ++q) {
+            tma_load_3d_hint(sb + SP::off_k + buf * SP::kKV + q * box * kRowBytes, &tm_k, bar, 0,
+                             h, rows[q], pol);
+            tma_load_3d_hint(sb + SP::off_v + buf * SP::kKV + q * box * kRowBytes, &tm_v, bar, 0,
+                             h, rows[q], pol);
+        }
+        tma_load_3d(sb + SP::off_r + buf * SP::kR, &tm_r, bar, 0, h, off + j0 - (TL::Tp - 1));
+    };
+
+    const int pre = n_stages < NS ? n_stages : NS;
+    const int first_chunk_stage = FUSED ? C / kStageKeys : n_stages;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar_q, TL::Tp * kRowBytes);
+        tma_load_3d(sb + SP::off_q, &tm_q, bar_q, 0, h, b * T);
+        for (int s = 0; s < pre && s < first_chunk_stage; ++s) issue(s);
+    }
+    if (tid < kHeadDim)
+        s_u[tid] = bf16_bits_to_f32(__ldg(a.pos_bias_u + h * kHeadDim + tid));
+    else
+        s_vb[tid - kHeadDim] = bf16_bits_to_f32(__ldg(a.pos_bias_v + h * kHeadDim + tid - kHeadDim));
+    if constexpr (FUSED) {
+        // This head's slice of the chunk: T rows x 8 vectors of 16 B, for K and for V.
+        for (int idx = tid; idx < 2 * T * 8; idx += kThreads) {
+            const int kv = idx >= T * 8;
+            const int rem = idx - kv * T * 8;
+            const int t = rem >> 3, c = rem & 7;
+            const int p = C + t;
+            const int lb = p / a.block_size;
+            if (lb >= a.mbps) { err |= kErrBounds; continue; }
+            const int slot = p - lb * a.block_size;
+            const int blk = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + lb);
+            if (blk < 0 || blk >= a.num_blocks) { err |= kErrBounds; continue; }
+            const uint16_t* src = (kv ? a.v_new : a.k_new) +
+                                  ((static_cast<long long>(b) * T + t) * a.H + h) * kHeadDim + c * 8;
+            uint16_t* dst = (kv ? a.v_pool : a.k_pool) +
+                            ((static_cast<long long>(blk) * a.block_size + slot) * a.H + h) * kHeadDim +
+                            c * 8;
+            *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
+        }
+        fence_proxy_async_global();
+        __syncthreads();
+        if (tid == 0)
+            for (int s = first_chunk_stage; s < pre; ++s) issue(s);
+    } else {
+        __syncthreads();
+    }
+
+    const int mt = warp % MT, kg = warp / MT;
+    float* gw = reinterpret_cast<float*>(sm + SP::off_g) + warp * 16 * TL::GW;
+    uint32_t qa[4][4];
+    WarpAcc acc;
+    acc_init(acc);
+    bool failed = __syncthreads_or(!mbar_wait(bar_q, 0));
+    int s = 0;
+    if (!failed) {
+        load_q_frags(sb + SP::off_q, mt, lane, qa);
+        for (; s < n_stages; ++s) {
+            const int buf = s % NS;
+            const bool ok = mbar_wait(bar_full + 8 * buf, (s / NS) & 1);
+            const int kvalid = min(kStageKeys, K - s * kStageKeys);
+            float* uk = reinterpret_cast<float*>(sm + SP::off_uk) + buf * kStageKeys;
+            float* vr = reinterpret_cast<float*>(sm + SP::off_vr) + buf * TL::RB;
+            if (ok)
+                stage_prologue<MT>(sm + SP::off_k + buf * SP::kKV, sm + SP::off_v + buf * SP::kKV,
+                                   sm + SP::off_r + buf * SP::kR, s_u, s_vb, uk, vr, kvalid, tid);
+            if (__syncthreads_or(!ok)) { failed = true; break; }
+            stage_compute<MT>(acc, qa, sb + SP::off_k + buf * SP::kKV,
+                              sb + SP::off_v + buf * SP::kKV, sb + SP::off_r + buf * SP::kR, uk,
+                              vr, gw, kvalid, a.scale_log2, mt, kg, lane);
+            __syncthreads();
+            if (tid == 0 && s + NS < n_stages) {
+                fence_proxy_async_smem();
+                issue(s + NS);
+            }
+        }
+    }
+    if (failed) {
+        // Let the copies still in flight land before the CTA's shared memory is released.
+        if (tid == 0) {
+            const int issued = min(n_stages, s + NS);
+            for (int s2 = s; s2 < issued; ++s2)
+                mbar_wait(bar_full + 8 * (s2 % NS), (s2 / NS) & 1, 100000000ull);
+            err |= kErrTimeout;
+        }
+        if (err) atomicOr(a.status, err);
+        return;
+    }
+
+    float* comb_o = reinterpret_cast<float*>(sm + SP::off_comb_o);
+    float* comb_m = reinterpret_cast<float*>(sm + SP::off_comb_ml);
+    float* comb_l = comb_m + TL::KG * TL::Tp;
+    write_partial<MT>(acc, comb_o, comb_m, comb_l, mt, kg, lane);
+    __syncthreads();
+    for (int idx = tid; idx < T * 8; idx += kThreads) {
+        const int row = idx >> 3, d0 = (idx & 7) * 8;
+        const uint4 v = combine_row8<MT>(comb_o, comb_m, comb_l, row, d0);
+        *reinterpret_cast<uint4*>(a.out + ((static_cast<long long>(b) * T + row) * a.H + h) *
+                                              kHeadDim + d0) = v;
+    }
+    if (err) atomicOr(a.status, err);
+}
+
+// ----------------------------------------------------------------------------- fp32
+
+template <bool FUSED>
+__global__ void __launch_bounds__(128) chunk_attn_f32_kernel(
+    const float* __restrict__ q, const float* __restrict__ k_new, const float* __restrict__ v_new,
+    float* k_pool, float* v_pool, int num_blocks, int block_size,
+    const int32_t* __restrict__ block_table, int mbps, const int32_t* __restrict__ cache_seqlens,
+    const float* __restrict__ u, const float* __restrict__ vb, const float* __restrict__ rel,
+    int R, float* __restrict__ out, int T, int H, float scale, unsigned* status)
+{
+    __shared__ float s_qu[64][kHeadDim];
+    __shared__ float s_qv[64][kHeadDim];
+    const int b = blockIdx.x / H, h = blockIdx.x % H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    unsigned err = 0;
+    int C = cache_seqlens[b];
+    if (C < 0) { C = 0; err |= kErrBounds; }
+    int K = C + T;
+    const int cap = mbps * block_size;
+    if (K > cap) { K = cap; err |= kErrBounds; }
+    const int off = R - T - C;
+
+    if (FUSED) {
+        for (int idx = tid; idx < 2 * T * kHeadDim; idx += blockDim.x) {
+            const int kv = idx >= T * kHeadDim;
+            const int rem = idx - kv * T * kHeadDim;
+            const int t = rem / kHeadDim, d = rem % kHeadDim;
+            const int p = C + t;
+            const int lb = p / block_size;
+            if (lb >= mbps) { err |= kErrBounds; continue; }
+            const int blk = block_table[static_cast<long long>(b) * mbps + lb];
+            if (blk < 0 || blk >= num_blocks) { err |= kErrBounds; continue; }
+            const long long dst =
+                ((static_cast<long long>(blk) * block_size + (p - lb * block_size)) * H + h) * kHeadDim + d;
+            const long long src = ((static_cast<long long>(b) * T + t) * H + h) * kHeadDim + d;
+            (kv ? v_pool : k_pool)[dst] = (kv ? v_new : k_new)[src];
+        }
+    }
+    for (int idx = tid; idx < T * kHeadDim; idx += blockDim.x) {
+        const int t = idx / kHeadDim, d = idx % kHeadDim;
+        const float qq = q[((static_cast<long long>(b) * T + t) * H + h) * kHeadDim + d];
+        s_qu[t][d] = qq + u[h * kHeadDim + d];
+        s_qv[t][d] = qq + vb[h * kHeadDim + d];
+    }
+    __syncthreads();
+
+    for (int i = warp; i < T; i += 4) {
+        float m = -INFINITY, l = 0.f, o0 = 0.f, o1 = 0.f;
+        for (int j0 = 0; j0 < K; j0 += 32) {
+            const int j = j0 + lane;
+            float sc = -INFINITY;
+            long long row_off = -1;   // element offset of key j's row in the pools
+            if (j < K) {
+                const int lb = j / block_size;
+                const int blk = block_table[static_cast<long long>(b) * mbps + lb];
+                float acc = 0.f;
+                if (blk >= 0 && blk < num_blocks) {
+                    row_off = ((static_cast<long long>(blk) * block_size + (j - lb * block_size)) * H + h) *
+                              kHeadDim;
+                    const float4* kr = reinterpret_cast<const float4*>(k_pool + row_off);
+#pragma unroll 4
+                    for (int d4 = 0; d4 < kHeadDim / 4; ++d4) {
+                        const float4 kk = kr[d4];
+                        acc = fmaf(s_qu[i][4 * d4], kk.x, acc);
+                        acc = fmaf(s_qu[i][4 * d4 + 1], kk.y, acc);
+                        acc = fmaf(s_qu[i][4 * d4 + 2], kk.z, acc);
+                        acc = fmaf(s_qu[i][4 * d4 + 3], kk.w, acc);
+                    }
+                } else {
+                    err |= kErrBounds;
+                }
+                const int rho = off + j - i;
+                if (rho >= 0 && rho < R) {
+                    const float4* rr =
+                        reinterpret_cast<const float4*>(rel + (static_cast<long long>(rho) * H + h) * kHeadDim);
+#pragma unroll 4
+                    for (int d4 = 0; d4 < kHeadDim / 4; ++d4) {
+                        const float4 r4 = rr[d4];
+                        acc = fmaf(s_qv[i][4 * d4], r4.x, acc);
+                        acc = fmaf(s_qv[i][4 * d4 + 1], r4.y, acc);
+                        acc = fmaf(s_qv[i][4 * d4 + 2], r4.z, acc);
+                        acc = fmaf(s_qv[i][4 * d4 + 3], r4.w, acc);
+                    }
+                }
+                sc = acc * scale;
+            }
+            float mx = sc;
+#pragma unroll
+            for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const float m_new = fmaxf(m, mx);
+            const float alpha = (m == -INFINITY) ? 0.f : expf(m - m_new);
+            const float p = (j < K) ? expf(sc - m_new) : 0.f;
+            float psum = p;
+#pragma unroll
+            for (int o = 16; o; o >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
+            l = l * alpha + psum;
+            o0 *= alpha;
+            o1 *= alpha;
+            const int nj = min(32, K - j0);
+            for (int jj = 0; jj < nj; ++jj) {
+                const float pj = __shfl_sync(0xffffffffu, p, jj);
+                const long long ro = __shfl_sync(0xffffffffu, row_off, jj);
+                if (ro >= 0) {
+                    o0 = fmaf(pj, v_pool[ro + lane], o0);
+                    o1 = fmaf(pj, v_pool[ro + 32 + lane], o1);
+                }
+            }
+            m = m_new;
+        }
+        float* dst = out + ((static_cast<long long>(b) * T + i) * H + h) * kHeadDim;
+        dst[lane] = o0 / l;
+        dst[lane + 32] = o1 / l;
+    }
+    if (err) atomicOr(status, err);
+}
+
+// --------------------------------------------------------------------------- host
+
+int g_smem_done[16][64];
+
+template <int MT, int NS, bool FUSED>
+oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, void* k_pool,
+                        void* v_pool, int num_blocks, int block_size, const int32_t* bt,
+                        int mbps, const int32_t* cs, const void* u, const void* vb,
+                        const void* rel, int R, void* out, int B, int T, int H, float scale,
+                        cudaStream_t stream, int slot)
+{
+    CUtensorMap tm_q, tm_k, tm_v, tm_r;
+    const int box = block_size < kStageKeys ? block_size : kStageKeys;
+    if (!encode_rows_bf16(&tm_q, q, static_cast<long long>(B) * T, H, Tile<MT>::Tp) ||
+        !encode_rows_bf16(&tm_k, k_pool, static_cast<long long>(num_blocks) * block_size, H, box) ||
+        !encode_rows_bf16(&tm_v, v_pool, static_cast<long long>(num_blocks) * block_size, H, box) ||
+        !encode_rows_bf16(&tm_r, rel, R, H, Tile<MT>::RB))
+        return OASR_ERR_INVALID_ARG;
+    unsigned* status = status_word();
+    if (!status) return OASR_ERR_CUDA;
+    auto kern = chunk_attn_bf16_kernel<MT, NS, FUSED>;
+    constexpr int smem = SmemPlan<MT, NS>::bytes;
+    if (!ensure_smem(kern, smem, g_smem_done[slot])) return OASR_ERR_CUDA;
+    ChunkArgs a;
+    a.k_new = static_cast<const uint16_t*>(k_new);
+    a.v_new = static_cast<const uint16_t*>(v_new);
+    a.k_pool = static_cast<uint16_t*>(k_pool);
+    a.v_pool = static_cast<uint16_t*>(v_pool);
+    a.block_table = bt;
+    a.cache_seqlens = cs;
+    a.pos_bias_u = static_cast<const uint16_t*>(u);
+    a.pos_bias_v = static_cast<const uint16_t*>(vb);
+    a.out = static_cast<uint16_t*>(out);
+    a.status = status;
+    a.num_blocks = num_blocks;
+    a.block_size = block_size;
+    a.mbps = mbps;
+    a.T = T;
+    a.H = H;
+    a.R = R;
+    a.box_rows = box;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    kern<<<static_cast<unsigned>(B) * H, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, tm_r, a);
+    return launch_status();
+}
+
+template <bool FUSED>
+oasr_status dispatch(const void* q, const void* k_new, const void* v_new, void* k_pool,
+                     void* v_pool, int num_blocks, int block_size, const int32_t* bt, int mbps,
+                     const int32_t* cs, const void* u, const void* vb, const void* rel, int R,
+                     void* out, int B, int T, int H, int D, float scale, oasr_dtype dt,
+                     cudaStream_t stream)
+{
+    if (!q || !k_pool || !v_pool || !bt || !cs || !u || !vb || !rel || !out)
+        return OASR_ERR_INVALID_ARG;
+    if (FUSED && (!k_new || !v_new)) return OASR_ERR_INVALID_ARG;
+    if (num_blocks <= 0 || block_size <= 0 || mbps <= 0 || R <= 0 || B <= 0 || T <= 0 ||
+        H <= 0 || D <= 0)
+        return OASR_ERR_INVALID_ARG;
+    if (dt != OASR_F32 && dt != OASR_BF16) return OASR_ERR_UNSUPPORTED;
+    if (D != kHeadDim || T > 64) return OASR_ERR_UNSUPPORTED;
+    if (block_size < 8 || block_size > 256 || (block_size & (block_size - 1)))
+        return OASR_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * H > 0x7fffffffLL) return OASR_ERR_UNSUPPORTED;
+    const void* ptrs[] = {q, k_pool, v_pool, u, vb, rel, out, FUSED ? k_new : q,
+                          FUSED ? v_new : q};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return OASR_ERR_INVALID_ARG;
+    if (dt == OASR_F32) {
+        unsigned* status = status_word();
+        if (!status) return OASR_ERR_CUDA;
+        chunk_attn_f32_kernel<FUSED><<<static_cast<unsigned>(B) * H, 128, 0, stream>>>(
+            static_cast<const float*>(q), static_cast<const float*>(k_new),
+            static_cast<const float*>(v_new), static_cast<float*>(k_pool),
+            static_cast<float*>(v_pool), num_blocks, block_size, bt, mbps, cs,
+            static_cast<const float*>(u), static_cast<const float*>(vb),
+            static_cast<const float*>(rel), R, static_cast<float*>(out), T, H, scale, status);
+        return launch_status();
+    }
+    const int f = FUSED ? 8 : 0;
+    if (T <= 16)
+        return launch_bf16<1, 3, FUSED>(q, k_new, v_new, k_pool, v_pool, num_blocks, block_size,
+                                        bt, mbps, cs, u, vb, rel, R, out, B, T, H, scale, stream,
+                                        f + 0);
+    if (T <= 32)
+        return launch_bf16<2, 3, FUSED>(q, k_new, v_new, k_pool, v_pool, num_blocks, block_size,
+                                        bt, mbps, cs, u, vb, rel, R, out, B, T, H, scale, stream,
+                                        f + 1);
+    return launch_bf16<4, 2, FUSED>(q, k_new, v_new, k_pool, v_pool, num_blocks, block_size, bt,
+                                    mbps, cs, u, vb, rel, R, out, B, T, H, scale, stream, f + 2);
+}
+
+}  // namespace
+}  // namespace oasr
+
+extern "C" oasr_status oasr_chunk_relattn_paged(
+    const void* q, const void* k_pool, const void* v_pool, int num_blocks, int block_size,
+    const int32_t* block_table, int max_blocks_per_seq, const int32_t* cache_seqlens,
+    const void* pos_bias_u, const void* pos_bias_v, const void* rel, int R, void* out, int B,
+    int T, int H, int D, float scale, oasr_dtype dt, cudaStream_t stream)
+{
+    return oasr::dispatch<false>(q, nullptr, nullptr, const_cast<void*>(k_pool),
+                                 const_cast<void*>(v_pool), num_blocks, block_size, block_table,
+                                 max_blocks_per_seq, cache_seqlens, pos_bias_u, pos_bias_v, rel,
+                                 R, out, B, T, H, D, scale, dt, stream);
+}
+
+extern "C" oasr_status oasr_chunk_step_paged(
+    const void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+    int num_blocks, int block_size, const int32_t* block_table, int max_blocks_per_seq,
+    const int32_t* cache_seqlens, const void* pos_bias_u, const void* pos_bias_v, const void* rel,
+    int R, void* out, int B, int T, int H, int D, float scale, oasr_dtype dt, cudaStream_t stream)
+{
+    return oasr::dispatch<true>(q, k_new, v_new, k_pool, v_pool, num_blocks, block_size,
+                                block_table, max_blocks_per_seq, cache_seqlens, pos_bias_u,
+                                pos_bias_v, rel, R, out, B, T, H, D, scale, dt, stream);
+}

@@ -1,0 +1,302 @@
+"""GPU parity: the CUDA path against the fp64 oracle, through the C ABI.
+
+Every workload of the five configurations is checked: element by element where the
+oracle finishes in seconds, else on sampled output rows the oracle computes one by
+one.  Edge cases cover ragged pages and stages, every supported chunk-tile shape,
+block sizes 8..256, empty caches, longer tables, invalid block ids and packed rows
+with empty, single-frame and tile-straddling segments.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_chunk_gb300 import capi
+from paged_kv_chunk_gb300 import synthetic as syn
+
+from helpers import (check_close, dev, dev_pool, gpu_stream_inputs, host_pool, oracle_chunk,
+                     sample_rows, stream_case, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean_status():
+    capi.oasr_device_status(clear=True)
+    yield
+
+
+def _run_step(cfg, x, fused):
+    d = gpu_stream_inputs(x, cfg.dtype)
+    if fused:
+        out = capi.oasr_chunk_step_paged(d["q"], d["k_new"], d["v_new"], d["k_pool"], d["v_pool"],
+                                         d["block_table"], d["cache_seqlens"], d["pos_bias_u"],
+                                         d["pos_bias_v"], d["rel"])
+    else:
+        capi.oasr_paged_append(d["k_new"], d["v_new"], d["k_pool"], d["v_pool"], d["block_table"],
+                               d["cache_seqlens"])
+        out = capi.oasr_chunk_relattn_paged(d["q"], d["k_pool"], d["v_pool"], d["block_table"],
+                                            d["cache_seqlens"], d["pos_bias_u"], d["pos_bias_v"],
+                                            d["rel"])
+    torch.cuda.synchronize()
+    return out, d
+
+
+FULL = [syn.TINY, syn.SMALL]
+SAMPLED = [syn.LARGE] + list(syn.SWEEP)
+
+
+# ------------------------------------------------------------------------- append
+
+
+@pytest.mark.parametrize("cfg", [syn.TINY, syn.SMALL, syn.LARGE, syn.SWEEP[0], syn.SWEEP[-1]],
+                         ids=lambda c: c.name)
+def test_append_bit_exact(cfg):
+    x = stream_case(cfg)
+    d = gpu_stream_inputs(x, cfg.dtype)
+    capi.oasr_paged_append(d["k_new"], d["v_new"], d["k_pool"], d["v_pool"], d["block_table"],
+                           d["cache_seqlens"])
+    kp, vp = x["k_pool"].copy(), x["v_pool"].copy()
+    skipped = oracle.paged_append(syn.to_bits(x["k_new"], cfg.dtype),
+                                  syn.to_bits(x["v_new"], cfg.dtype), kp, vp, x["block_table"],
+                                  x["cache_seqlens"])
+    assert skipped == 0
+    np.testing.assert_array_equal(host_pool(d["k_pool"], cfg.dtype), kp)
+    np.testing.assert_array_equal(host_pool(d["v_pool"], cfg.dtype), vp)
+    assert capi.oasr_device_status() == 0
+
+
+def test_append_skips_bad_blocks_and_flags():
+    cfg = syn.StreamingConfig("bad", B=3, H=2, D=64, T=5, C=6, block_size=8, dtype="bf16", seed=7)
+    x = stream_case(cfg)
+    bt = x["block_table"].copy()
+    bt[1, 1] = cfg.pool_blocks + 5          # stream 1's chunk page points outside the pool
+    x["block_table"] = bt
+    d = gpu_stream_inputs(x, cfg.dtype)
+    capi.oasr_paged_append(d["k_new"], d["v_new"], d["k_pool"], d["v_pool"], d["block_table"],
+                           d["cache_seqlens"])
+    kp, vp = x["k_pool"].copy(), x["v_pool"].copy()
+    skipped = oracle.paged_append(syn.to_bits(x["k_new"], "bf16"), syn.to_bits(x["v_new"], "bf16"),
+                                  kp, vp, bt, x["cache_seqlens"])
+    assert skipped > 0
+    np.testing.assert_array_equal(host_pool(d["k_pool"], "bf16"), kp)
+    assert capi.oasr_device_status() & capi.STATUS_BOUNDS_BIT
+
+
+# ---------------------------------------------------------------- chunk attention
+
+
+@pytest.mark.parametrize("cfg", FULL, ids=lambda c: c.name)
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
+def test_chunk_attention_full(cfg, fused):
+    x = stream_case(cfg)
+    out, _ = _run_step(cfg, x, fused)
+    ref = oracle_chunk(x)
+    check_close(to_np(out), ref, cfg.dtype, cfg.name)
+    assert capi.oasr_device_status() == 0
+
+
+@pytest.mark.parametrize("cfg", SAMPLED, ids=lambda c: c.name)
+def test_chunk_attention_sampled_full_size(cfg):
+    """Full-size workload in the launch configuration the benchmark times (fused step);
+    2048 sampled output rows compared with the oracle, plus the two-call path."""
+    x = stream_case(cfg)
+    out, _ = _run_step(cfg, x, fused=True)
+    rng = np.random.default_rng(cfg.seed + 1)
+    rows = sample_rows(rng, cfg.B, cfg.T, cfg.H, 2048)
+    ref = oracle_chunk(x, rows=rows)
+    got = to_np(out)
+    b, i, h = rows[:, 0], rows[:, 1], rows[:, 2]
+    check_close(got[b, i, h], ref[b, i, h], cfg.dtype, cfg.name)
+    out2, _ = _run_step(cfg, x, fused=False)
+    assert torch.equal(out, out2), "fused step and append + attention differ"
+    assert capi.oasr_device_status() == 0
+
+
+def test_fused_step_writes_the_same_pool():
+    cfg = syn.SMALL
+    x = stream_case(cfg)
+    _, d1 = _run_step(cfg, x, fused=True)
+    _, d2 = _run_step(cfg, x, fused=False)
+    assert torch.equal(d1["k_pool"].view(torch.int16), d2["k_pool"].view(torch.int16))
+    assert torch.equal(d1["v_pool"].view(torch.int16), d2["v_pool"].view(torch.int16))
+
+
+def test_paging_permutation_is_invisible():
+    """Results are bit-identical whichever physical blocks the table names."""
+    cfg = syn.SMALL
+    x0 = stream_case(cfg)
+    n_pages = cfg.mbps
+    ident = np.arange(cfg.B * n_pages, dtype=np.int32).reshape(cfg.B, n_pages)
+    x1 = stream_case(cfg, block_table=ident)
+    rev = (cfg.pool_blocks - 1 - ident).astype(np.int32)
+    x2 = stream_case(cfg, block_table=rev)
+    outs = [_run_step(cfg, x, fused=True)[0] for x in (x0, x1, x2)]
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+EDGE = [
+    # (B, H, T, C, block_size, R extra, dtype)
+    (2, 2, 1, 0, 16, 0, "bf16"),       # a single key
+    (3, 2, 1, 7, 8, 0, "bf16"),        # T=1 decode-like step
+    (2, 3, 4, 5, 8, 0, "bf16"),        # ragged page and stage
+    (2, 2, 16, 0, 16, 0, "bf16"),      # no cache
+    (2, 2, 16, 48, 16, 3, "bf16"),     # keys end exactly on a stage; longer table
+    (3, 2, 16, 113, 32, 0, "bf16"),    # ragged 32-row page
+    (2, 2, 13, 200, 64, 0, "bf16"),    # block = stage
+    (2, 2, 16, 300, 128, 0, "bf16"),   # a stage inside a page
+    (2, 2, 16, 270, 256, 5, "bf16"),   # largest block
+    (2, 2, 17, 40, 16, 0, "bf16"),     # two m-tiles, ragged
+    (2, 2, 32, 96, 16, 0, "bf16"),     # two m-tiles, full
+    (2, 2, 33, 20, 16, 0, "bf16"),     # four m-tiles, ragged
+    (2, 2, 64, 130, 16, 0, "bf16"),    # four m-tiles, full
+    (2, 2, 5, 77, 8, 2, "f32"),
+    (2, 3, 40, 33, 16, 0, "f32"),
+    (1, 1, 1, 0, 8, 0, "f32"),
+]
+
+
+@pytest.mark.parametrize("B,H,T,C,bs,extra,dtype", EDGE)
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
+def test_chunk_attention_edge_cases(B, H, T, C, bs, extra, dtype, fused):
+    cfg = syn.StreamingConfig("edge", B=B, H=H, D=64, T=T, C=C, block_size=bs, dtype=dtype,
+                              seed=31 + T + C)
+    x = stream_case(cfg, R=cfg.R + extra)
+    out, _ = _run_step(cfg, x, fused)
+    check_close(to_np(out), oracle_chunk(x), dtype, f"edge B{B} H{H} T{T} C{C} bs{bs}")
+    assert capi.oasr_device_status() == 0
+
+
+def test_chunk_scale_argument():
+    cfg = syn.StreamingConfig("scale", B=2, H=2, D=64, T=8, C=24, block_size=16, dtype="bf16",
+                              seed=5)
+    x = stream_case(cfg)
+    d = gpu_stream_inputs(x, "bf16")
+    capi.oasr_paged_append(d["k_new"], d["v_new"], d["k_pool"], d["v_pool"], d["block_table"],
+                           d["cache_seqlens"])
+    out = capi.oasr_chunk_relattn_paged(d["q"], d["k_pool"], d["v_pool"], d["block_table"],
+                                        d["cache_seqlens"], d["pos_bias_u"], d["pos_bias_v"],
+                                        d["rel"], scale=0.9)
+    check_close(to_np(out), oracle_chunk(x, scale=0.9), "bf16", "scale 0.9")
+
+
+def test_invalid_block_id_is_flagged_and_contained():
+    """A bad block id in one stream's table raises the bounds bit; the other streams'
+    rows are still exact and nothing is read or written outside the pool."""
+    cfg = syn.StreamingConfig("badid", B=3, H=2, D=64, T=8, C=40, block_size=16, dtype="bf16",
+                              seed=9)
+    x = stream_case(cfg)
+    bt = x["block_table"].copy()
+    bt[1, 0] = -3
+    bt[1, 1] = cfg.pool_blocks + 100
+    d = gpu_stream_inputs(x, "bf16")
+    d["block_table"] = torch.from_numpy(bt).cuda()
+    out = capi.oasr_chunk_step_paged(d["q"], d["k_new"], d["v_new"], d["k_pool"], d["v_pool"],
+                                     d["block_table"], d["cache_seqlens"], d["pos_bias_u"],
+                                     d["pos_bias_v"], d["rel"])
+    torch.cuda.synchronize()
+    assert capi.oasr_device_status() & capi.STATUS_BOUNDS_BIT
+    ref = oracle_chunk(x)
+    got = to_np(out)
+    for b in (0, 2):
+        check_close(got[b], ref[b], "bf16", f"stream {b}")
+
+
+# ----------------------------------------------------------------------- packed
+
+
+def _packed_case(lengths, dtype="bf16", seed=3, H=2, R_extra=0):
+    cfg = syn.PackedConfig("p", num_seqs=len(lengths), min_len=1, max_len=max(max(lengths), 1),
+                           H=H, D=64, dtype=dtype, seed=seed)
+    x = syn.packed_inputs(cfg, lengths=lengths)
+    if R_extra:
+        rng = np.random.default_rng(seed + 99)
+        x["rel"] = syn.normal(rng, (x["rel"].shape[0] + R_extra, H, 64), dtype)
+    return cfg, x
+
+
+def _run_packed(x, dtype):
+    d = {k: dev(x[k], dtype) for k in ("q", "k", "v", "pos_bias_u", "pos_bias_v", "rel")}
+    cu = torch.from_numpy(x["cu_seqlens"]).cuda()
+    out = capi.oasr_packed_relattn_varlen(d["q"], d["k"], d["v"], cu, max(x["max_seqlen"], 1),
+                                          d["pos_bias_u"], d["pos_bias_v"], d["rel"])
+    torch.cuda.synchronize()
+    return out
+
+
+def _oracle_packed(x, rows=None):
+    return oracle.packed_relattn(x["q"], x["k"], x["v"], x["cu_seqlens"], x["pos_bias_u"],
+                                 x["pos_bias_v"], x["rel"], rows=rows)
+
+
+@pytest.mark.parametrize("lengths", [
+    [1], [64], [65], [7, 0, 130, 1, 64, 200, 3], [300, 299, 1, 0, 0, 150],
+], ids=str)
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_packed_full(lengths, dtype):
+    _, x = _packed_case(lengths, dtype=dtype)
+    out = _run_packed(x, dtype)
+    check_close(to_np(out), _oracle_packed(x), dtype, f"packed {lengths}")
+    assert capi.oasr_device_status() == 0
+
+
+def test_packed_longer_table():
+    _, x = _packed_case([90, 33], R_extra=10)
+    out = _run_packed(x, "bf16")
+    check_close(to_np(out), _oracle_packed(x), "bf16", "longer table")
+
+
+def test_packed_full_size_sampled():
+    """The 256-utterance packed row: 4096 sampled (token, head) rows plus every row of
+    the shortest and the longest segment."""
+    cfg = syn.PACKED
+    x = syn.packed_inputs(cfg)
+    out = _run_packed(x, cfg.dtype)
+    rng = np.random.default_rng(77)
+    total = int(x["cu_seqlens"][-1])
+    t = rng.choice(total, size=4096, replace=False)
+    h = rng.integers(0, cfg.H, size=4096)
+    rows = [np.stack([t, h], 1)]
+    for s in (int(np.argmin(x["lengths"])), int(np.argmax(x["lengths"]))):
+        a, e = x["cu_seqlens"][s], x["cu_seqlens"][s + 1]
+        tt = np.repeat(np.arange(a, e), cfg.H)
+        hh = np.tile(np.arange(cfg.H), e - a)
+        rows.append(np.stack([tt, hh], 1))
+    rows = np.concatenate(rows).astype(np.int32)
+    ref = _oracle_packed(x, rows=rows)
+    got = to_np(out)
+    check_close(got[rows[:, 0], rows[:, 1]], ref[rows[:, 0], rows[:, 1]], cfg.dtype, "packed full")
+    assert capi.oasr_device_status() == 0
+
+
+def test_packed_segment_order_and_concatenation():
+    lengths = [70, 5, 129]
+    _, x = _packed_case(lengths, seed=11)
+    full = _run_packed(x, "bf16")
+    cu = x["cu_seqlens"]
+    for s in range(len(lengths)):
+        a, e = cu[s], cu[s + 1]
+        alone = dict(x, q=x["q"][a:e], k=x["k"][a:e], v=x["v"][a:e],
+                     cu_seqlens=np.array([0, e - a], np.int32), max_seqlen=int(e - a))
+        assert torch.equal(_run_packed(alone, "bf16"), full[a:e])
+
+
+def test_streaming_rows_equal_packed_rows_gpu():
+    """Chunk attention at cache C equals rows C..C+T-1 of the packed attention over one
+    segment of C+T frames (same keys; same rel rows), on the GPU."""
+    B, H, T, C = 1, 2, 16, 80
+    cfg = syn.StreamingConfig("sp", B=B, H=H, D=64, T=T, C=C, block_size=16, dtype="bf16",
+                              seed=21)
+    L = C + T
+    rng = np.random.default_rng(5)
+    relp = syn.normal(rng, (2 * L - 1, H, 64), "bf16")
+    x = stream_case(cfg)
+    x["rel"] = relp[: cfg.R]
+    out_s, _ = _run_step(cfg, x, fused=True)
+    qq = np.concatenate([syn.normal(rng, (C, H, 64), "bf16"), x["q"][0]])
+    px = dict(q=qq, k=np.concatenate([x["cache_k"][0], x["k_new"][0]]),
+              v=np.concatenate([x["cache_v"][0], x["v_new"][0]]),
+              cu_seqlens=np.array([0, L], np.int32), pos_bias_u=x["pos_bias_u"],
+              pos_bias_v=x["pos_bias_v"], rel=relp, max_seqlen=L)
+    out_p = _run_packed(px, "bf16")
+    check_close(to_np(out_s[0]), to_np(out_p[C:]), "bf16", "streaming vs packed")
