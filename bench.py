@@ -56,7 +56,10 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="conformer_small", choices=sorted(syn.STREAMING_CONFIGS))
+    ap.add_argument("--config", default="conformer_small",
+                    choices=sorted(syn.STREAMING_CONFIGS) + [syn.PACKED.name])
+    ap.add_argument("--two-call", action="store_true",
+                    help="time oasr_paged_append + oasr_chunk_relattn_paged instead of the fused step")
     ap.add_argument("--layers", type=int, default=0,
                     help="distinct layer pools per step (0: enough for 4x L2)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -84,6 +87,26 @@ def workload_bytes(cfg, fused=True):
     b += cfg.R * row                    # read the shared rel table once
     b += chunk                          # write out
     return b
+
+
+def packed_flops(lengths, H, D):
+    """Algorithmic flops of one packed call: per (query, key) pair of a segment and head,
+    the content dot, the position dot and the P.V row each take 2*D flops."""
+    L = np.asarray(lengths, dtype=np.float64)
+    return float((L * L).sum()) * H * 6 * D
+
+
+def packed_bytes(total, R, H, D, es=2):
+    return (4 * total + R) * H * D * es
+
+
+def measured_tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 def measured_hbm_peak():
@@ -276,7 +299,7 @@ def run_ours(args, cfg, rank, world, local):
     dev = torch.device("cuda", torch.cuda.current_device())
     tdtype = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
     es = 2 if cfg.dtype == "bf16" else 4
-    touched = workload_bytes(cfg)
+    touched = workload_bytes(cfg, fused=not args.two_call)
     layers = args.layers or max(1, math.ceil(4 * L2_BYTES / touched))
     rng = np.random.default_rng(cfg.seed + 1000 * rank)
     gen = torch.Generator(device=dev)
@@ -303,8 +326,12 @@ def run_ours(args, cfg, rank, world, local):
         for l in range(layers):
             kp, vp = pools[l]
             u, vb, rel = params[l]
-            capi.oasr_chunk_step_paged(x[l, 0], x[l, 1], x[l, 2], kp, vp, bt, cs, u, vb, rel,
-                                       out=out[l])
+            if args.two_call:
+                capi.oasr_paged_append(x[l, 1], x[l, 2], kp, vp, bt, cs)
+                capi.oasr_chunk_relattn_paged(x[l, 0], kp, vp, bt, cs, u, vb, rel, out=out[l])
+            else:
+                capi.oasr_chunk_step_paged(x[l, 0], x[l, 1], x[l, 2], kp, vp, bt, cs, u, vb, rel,
+                                           out=out[l])
 
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
@@ -384,7 +411,7 @@ def run_ours(args, cfg, rank, world, local):
         return
     peak, peak_kind = measured_hbm_peak()
     achieved = touched / (launch_us * 1e-6) / 1e9
-    traffic = profiled_traffic(cfg.name)
+    traffic = None if args.two_call else profiled_traffic(cfg.name)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
@@ -399,10 +426,11 @@ def run_ours(args, cfg, rank, world, local):
                    "soak_s": args.soak_seconds},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "chunk_attn_bf16_kernel (fused append + attention)",
+                     "kernel": ("paged_append_kernel + chunk_attn_bf16_kernel" if args.two_call
+                                else "chunk_attn_bf16_kernel (fused append + attention)"),
                      "algorithmic_bytes_per_launch": touched,
                      "avg_launch_us": launch_us, "peak_kind": peak_kind},
-        "gpu_launches": args.steps * layers,
+        "gpu_launches": args.steps * layers * (2 if args.two_call else 1),
         "clocks": clocks,
     }
     if e2e:
@@ -412,8 +440,77 @@ def run_ours(args, cfg, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def run_packed(args, rank, world, local):
+    """The offline packed row: one call = one attention layer over all utterances."""
+    from paged_kv_chunk_gb300 import build as pkg_build
+    from paged_kv_chunk_gb300 import capi
+    pkg_build.build()
+    capi.load()
+    cfg = syn.PACKED
+    x = syn.packed_inputs(cfg, cfg.seed + 1000 * rank)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = {k: torch.from_numpy(x[k]).to(torch.bfloat16).to(dev)
+         for k in ("q", "k", "v", "pos_bias_u", "pos_bias_v", "rel")}
+    cu = torch.from_numpy(x["cu_seqlens"]).to(dev)
+    out = torch.empty_like(d["q"])
+    total = int(x["cu_seqlens"][-1])
+
+    def call():
+        capi.oasr_packed_relattn_varlen(d["q"], d["k"], d["v"], cu, x["max_seqlen"],
+                                        d["pos_bias_u"], d["pos_bias_v"], d["rel"], out=out)
+
+    stream = torch.cuda.Stream(device=dev)
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize()
+        t_end = time.perf_counter() + args.soak_seconds
+        while time.perf_counter() < t_end:
+            call()
+            stream.synchronize()
+        barrier(world)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            call()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    if rank != 0:
+        return
+    per_call_s = ms / 1e3 / args.steps
+    flops = packed_flops(x["lengths"], cfg.H, cfg.D)
+    peak, kind = measured_tensor_peak()
+    achieved = flops / per_call_s / 1e12
+    line = {
+        "metric": METRIC, "value": total * args.steps * world / (ms / 1e3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "packed_varlen_offline", "num_seqs": cfg.num_seqs,
+                   "lengths": f"U{{{cfg.min_len}..{cfg.max_len}}}", "total_frames": total,
+                   "H": cfg.H, "D": cfg.D, "rel_rows": int(x["rel"].shape[0]),
+                   "l2": f"inputs larger than L2: {packed_bytes(total, x['rel'].shape[0], cfg.H, cfg.D) / 1e6:.0f} MB per call"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "packed_attn_bf16_kernel", "algorithmic_flops_per_launch": flops,
+                     "avg_launch_us": per_call_s * 1e6, "peak_kind": kind},
+        "gpu_launches": args.steps, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.config == syn.PACKED.name:
+        rank, world, local = dist_setup()
+        run_packed(args, rank, world, local)
+        return
     cfg = syn.STREAMING_CONFIGS[args.config]
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))

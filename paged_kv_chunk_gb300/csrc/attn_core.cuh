@@ -1,77 +1,54 @@
-// Per-stage warp compute shared by the streaming (paged) and packed (varlen) bf16
-// attention kernels.
+// Per-warp attention unit shared by the streaming (paged) and packed (varlen) bf16
+// kernels: 16 query rows of one head against one stage of 64 keys.
 //
-// A CTA of 4 warps owns one query tile of Tp = 16*MT rows of one head and walks the keys
-// in stages of 64.  Warp w takes m-tile (w % MT) and the key slice (w / MT) of each stage
-// (KG = 4/MT slices of NK = 64/KG keys).  Per stage and warp:
+// A CTA has kConsumerWarps consumer warps and one producer warp.  The producer streams
+// stages of 64 keys (K rows, V rows and the rel band they need) into a ring of smem
+// slots with TMA, completing a `full` mbarrier per slot; consumers release a slot by
+// arriving on its `empty` mbarrier.  Consumer warp w owns m-tile (w % MT) of the CTA's
+// Tp = 16*MT query rows and the stages s with s % KG == w / MT (KG = 4/MT), so each warp
+// works on whole stages:
 //
-//   S  = Q . K^T + (u . k_j)                  mma.sync m16n8k16 bf16, fp32 accumulators
-//                                              seeded with the per-key u.k_j (fp32)
-//   G  = Q . Rband^T + (v . r_m)               the same for the rel rows of the band
-//   S += G[i][j + 15 - i]                      rel_shift skew through a per-warp smem tile
-//   S  = S * scale * log2(e), keys past the end masked to -inf
+//   S  = bf16(q+u) . K^T                       mma.sync m16n8k16, fp32 accumulators
+//   G  = bf16(q+v) . Rband^T                   80 band columns for the 64 keys
+//   S += G[i][j + 15 - i]                      rel_shift skew through a smem tile
+//   S  = S * scale * log2(e), keys past the end -> -inf
 //   online softmax (running max/sum per row, fp32, exp2)
-//   O += P . V                                 P rounded to bf16 in registers
+//   O += P . V                                 P rounded to bf16; V rows past the end
+//                                              are zeroed in registers
 //
-// Score convention (Scheduler page, section 4.3; Model Layer page, fixed_attention_window
-// row and Nemotron ASR section): s_ij = scale * ((q_i+u).k_j + (q_i+v).rel[rho]),
-// rho = off + j - i, where the kernel chooses `off` for its mode.  The band loaded for a
-// stage of keys [j0, j0+64) and query rows [i0, i0+Tp) is rel rows
-// [off + j0 - i0 - (Tp-1), +64+Tp); warp (mt, kg) reads band columns starting at
-// o_w = Tp - 16 - 16*mt + kg*NK, and element (i', jl) of its tile uses column jl + 15 - i'.
+// Score (Scheduler page, section 4.3; Model Layer page, fixed_attention_window row and
+// Nemotron ASR section): s_ij = scale * ((q_i+u).k_j + (q_i+v).rel[rho]), rho = off + j - i
+// with `off` chosen by the kernel's mode.  For keys [j0, j0+64) and query rows [i0, i0+Tp)
+// a stage's band is rel rows [off + j0 - i0 - (Tp-1), +64+Tp); warp m-tile mt reads band rows
+// from o = Tp - 16 - 16*mt, and element (i', j) of its tile uses band column j + 15 - i'.
 #pragma once
 
 #include "ptx.cuh"
 
 namespace oasr {
 
-constexpr int kHeadDim = 64;    // head dimension of the tensor-core path
-constexpr int kStageKeys = 64;  // keys per pipeline stage
-constexpr int kRowBytes = 128;  // one bf16 row of kHeadDim
-constexpr int kThreads = 128;   // 4 warps per CTA
+constexpr int kHeadDim = 64;               // head dimension of the tensor-core path
+constexpr int kStageKeys = 64;             // keys per stage
+constexpr int kRowBytes = 128;             // one bf16 row of kHeadDim
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kBandCols = kStageKeys + 16; // band columns one warp computes per stage
+constexpr int kGW = kBandCols + 4;         // skew scratch row stride (floats)
+constexpr int kGBytes = 16 * kGW * 4;      // skew scratch of one warp
+constexpr int kOW = kHeadDim + 4;          // combine scratch row stride (floats)
 
 template <int MT_>
 struct Tile {
-    static constexpr int MT = MT_;                // 16-row m-tiles per CTA
-    static constexpr int KG = 4 / MT;             // key slices per stage
-    static constexpr int NK = kStageKeys / KG;    // keys per warp per stage
-    static constexpr int Tp = 16 * MT;            // padded query rows
-    static constexpr int RB = kStageKeys + Tp;    // rel band rows per stage
-    static constexpr int NBAND = NK + 16;         // band columns per warp
-    static constexpr int GW = NBAND + 4;          // skew scratch row stride (floats)
-    static constexpr int OW = kHeadDim + 4;       // combine scratch row stride (floats)
-};
-
-// Shared-memory plan (byte offsets from a 1024-byte aligned base).  K/V/R/Q tiles are
-// written by TMA with 128-byte swizzling.  After the key loop the K/V stage area is
-// reused for the cross-warp combine.
-template <int MT, int NS, int EXTRA = 0>
-struct SmemPlan {
-    using TL = Tile<MT>;
-    static constexpr int kKV = kStageKeys * kRowBytes;
-    static constexpr int kR = TL::RB * kRowBytes;
-    static constexpr int off_k = 0;
-    static constexpr int off_v = off_k + NS * kKV;
-    static constexpr int off_r = off_v + NS * kKV;
-    static constexpr int off_q = off_r + NS * kR;
-    static constexpr int off_g = off_q + TL::Tp * kRowBytes;
-    static constexpr int off_uk = off_g + 4 * 16 * TL::GW * 4;
-    static constexpr int off_vr = off_uk + NS * kStageKeys * 4;
-    static constexpr int off_u = off_vr + NS * TL::RB * 4;
-    static constexpr int off_vb = off_u + kHeadDim * 4;
-    static constexpr int off_bar = off_vb + kHeadDim * 4;
-    static constexpr int off_extra = off_bar + (NS + 1) * 8;
-    static constexpr int bytes = off_extra + EXTRA + 1024;
-    static constexpr int off_comb_o = off_k;
-    static constexpr int off_comb_ml = off_k + TL::KG * TL::Tp * TL::OW * 4;
-    static_assert(off_r % 1024 == 0 && off_q % 1024 == 0 && kR % 1024 == 0, "TMA tiles");
-    static_assert(off_comb_ml + 2 * TL::KG * TL::Tp * 4 <= off_r, "combine area");
+    static constexpr int MT = MT_;                  // 16-row m-tiles of the CTA
+    static constexpr int KG = kConsumerWarps / MT;  // stage groups
+    static constexpr int Tp = 16 * MT;              // padded query rows
+    static constexpr int RB = kStageKeys + Tp;      // band rows per stage
 };
 
 struct WarpAcc {
     float o[8][4];  // 16 rows x 64 dims: n-tile dt holds dims [8dt, 8dt+8)
     float m[2];     // running max (log2 units) of rows g and g+8
-    float l[2];     // running sum (this thread's columns only)
+    float l[2];     // running sum over this thread's columns
 };
 
 __device__ __forceinline__ void acc_init(WarpAcc& a)
@@ -84,147 +61,95 @@ __device__ __forceinline__ void acc_init(WarpAcc& a)
     a.l[0] = a.l[1] = 0.f;
 }
 
-// A fragments of the warp's 16 query rows (4 k-steps of 16 dims) from a swizzled Q tile.
-__device__ __forceinline__ void load_q_frags(uint32_t q_s, int mt, int lane, uint32_t (&qa)[4][4])
-{
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-        ldsm_x4(q_s + swz128(16 * mt + (lane & 15), 2 * ks + (lane >> 4)), qa[ks][0], qa[ks][1],
-                qa[ks][2], qa[ks][3]);
-}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// fp32 dot product of the 64-wide bf16 row `r` of a swizzled tile with vec (fp32, smem).
-__device__ __forceinline__ float dot_row_bf16(const uint8_t* tile, int r, const float* vec)
+// A fragments of bf16(q + u) and bf16(q + v) for the warp's 16 query rows (rows 16*mt..)
+// of a swizzled Q tile; u, v are fp32 in smem.  Rounding q + u to bf16 changes a score
+// by ~2^-9 of one term, far below the bf16 output rounding.
+__device__ __forceinline__ void make_q_frags(uint32_t q_s, const float* u, const float* v, int mt,
+                                             int lane, uint32_t (&qu)[4][4], uint32_t (&qv)[4][4])
 {
-    float acc = 0.f;
+    const int t4 = lane & 3;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(tile + swz128(r, c));
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    for (int ks = 0; ks < 4; ++ks) {
+        uint32_t r[4];
+        ldsm_x4(q_s + swz128(16 * mt + (lane & 15), 2 * ks + (lane >> 4)), r[0], r[1], r[2], r[3]);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float lo = __uint_as_float(w[e] << 16);
-            const float hi = __uint_as_float(w[e] & 0xffff0000u);
-            acc = fmaf(lo, vec[8 * c + 2 * e], acc);
-            acc = fmaf(hi, vec[8 * c + 2 * e + 1], acc);
+        for (int i = 0; i < 4; ++i) {
+            const int c = 16 * ks + ((i >> 1) << 3) + 2 * t4;   // r0,r1: cols 2t; r2,r3: 8+2t
+            const float lo = bf16_lo(r[i]), hi = bf16_hi(r[i]);
+            qu[ks][i] = pack_bf16(lo + u[c], hi + u[c + 1]);
+            qv[ks][i] = pack_bf16(lo + v[c], hi + v[c + 1]);
         }
     }
-    return acc;
 }
 
-// Cooperative per-stage prologue (all 128 threads): u.k for the stage's keys, v.r for its
-// band rows, and zeroed V rows past the last valid key (their p is 0, but 0 * NaN is not).
-template <int MT>
-__device__ __forceinline__ void stage_prologue(const uint8_t* k_tile, uint8_t* v_tile,
-                                               const uint8_t* r_tile, const float* s_u,
-                                               const float* s_vb, float* uk, float* vr,
-                                               int kvalid, int tid)
+// One warp, one stage.  k_s, v_s: shared addresses of the stage's 64 K and V rows;
+// band_s: shared address of the stage's band tile, band_o: first band row this warp uses;
+// g: this warp's skew scratch [16][kGW] floats (may alias the band tile once the band
+// MMAs are done); kvalid: keys [0, kvalid) of the stage exist.
+__device__ __forceinline__ void warp_stage(WarpAcc& acc, const uint32_t (&qu)[4][4],
+                                           const uint32_t (&qv)[4][4], uint32_t k_s, uint32_t v_s,
+                                           uint32_t band_s, int band_o, float* g, int kvalid,
+                                           float scale_log2, int lane)
 {
-    using TL = Tile<MT>;
-    if (tid < kStageKeys) {
-        uk[tid] = (tid < kvalid) ? dot_row_bf16(k_tile, tid, s_u) : 0.f;
-    } else {
-        for (int r = tid - kStageKeys; r < TL::RB; r += kThreads - kStageKeys)
-            vr[r] = dot_row_bf16(r_tile, r, s_vb);
-    }
-    if (kvalid < kStageKeys) {
-        const int n16 = (kStageKeys - kvalid) * (kRowBytes / 16);
-        uint4* base = reinterpret_cast<uint4*>(v_tile + kvalid * kRowBytes);
-        for (int i = tid; i < n16; i += kThreads) base[i] = make_uint4(0u, 0u, 0u, 0u);
-    }
-}
-
-// One stage of one warp; see the file comment.  k_s, v_s, r_s: shared addresses of the
-// stage's K (64 rows), V (64 rows) and band (RB rows) tiles.  gw: this warp's skew scratch.
-template <int MT>
-__device__ __forceinline__ void stage_compute(WarpAcc& acc, const uint32_t (&qa)[4][4],
-                                              uint32_t k_s, uint32_t v_s, uint32_t r_s,
-                                              const float* uk, const float* vr, float* gw,
-                                              int kvalid, float scale_log2, int mt, int kg,
-                                              int lane)
-{
-    using TL = Tile<MT>;
-    constexpr int NK = TL::NK;
-    constexpr int NT = NK / 8;            // key n-tiles
-    constexpr int NB = TL::NBAND / 8;     // band n-tiles
-    constexpr int GW = TL::GW;
     const int g4 = lane >> 2, t4 = lane & 3, mi = lane >> 3;
-    const int kb = kg * NK;
-
-    // ---- content scores, accumulators seeded with u.k_j
-    float s[NT][4];
+    float s[8][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const float2 ukv = *reinterpret_cast<const float2*>(uk + kb + 8 * nt + 2 * t4);
-        s[nt][0] = ukv.x;
-        s[nt][1] = ukv.y;
-        s[nt][2] = ukv.x;
-        s[nt][3] = ukv.y;
-    }
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
-        for (int np = 0; np < NT / 2; ++np) {
-            const int row = kb + 16 * np + ((mi >> 1) << 3) + (lane & 7);
+        for (int np = 0; np < 4; ++np) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(k_s + swz128(row, 2 * ks + (mi & 1)), b0, b1, b2, b3);
-            mma_bf16_16816(s[2 * np], qa[ks], b0, b1);
-            mma_bf16_16816(s[2 * np + 1], qa[ks], b2, b3);
+            ldsm_x4(k_s + swz128(16 * np + ((mi >> 1) << 3) + (lane & 7), 2 * ks + (mi & 1)), b0,
+                    b1, b2, b3);
+            mma_bf16_16816(s[2 * np], qu[ks], b0, b1);
+            mma_bf16_16816(s[2 * np + 1], qu[ks], b2, b3);
         }
     }
-
-    // ---- position scores on the band, seeded with v.r_m, staged for the skew
-    const int ow = TL::Tp - 16 - 16 * mt + kb;
     {
-        float gacc[NB][4];
+        float gacc[kBandCols / 8][4];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-            const float2 vv = *reinterpret_cast<const float2*>(vr + ow + 8 * nb + 2 * t4);
-            gacc[nb][0] = vv.x;
-            gacc[nb][1] = vv.y;
-            gacc[nb][2] = vv.x;
-            gacc[nb][3] = vv.y;
-        }
+        for (int nb = 0; nb < kBandCols / 8; ++nb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) gacc[nb][e] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
-            for (int np = 0; np < NB / 2; ++np) {
-                const int row = ow + 16 * np + ((mi >> 1) << 3) + (lane & 7);
+            for (int np = 0; np < kBandCols / 16; ++np) {
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4(r_s + swz128(row, 2 * ks + (mi & 1)), b0, b1, b2, b3);
-                mma_bf16_16816(gacc[2 * np], qa[ks], b0, b1);
-                mma_bf16_16816(gacc[2 * np + 1], qa[ks], b2, b3);
+                ldsm_x4(band_s + swz128(band_o + 16 * np + ((mi >> 1) << 3) + (lane & 7),
+                                        2 * ks + (mi & 1)),
+                        b0, b1, b2, b3);
+                mma_bf16_16816(gacc[2 * np], qv[ks], b0, b1);
+                mma_bf16_16816(gacc[2 * np + 1], qv[ks], b2, b3);
             }
         }
+        __syncwarp();   // every lane's band reads are done before the scratch (maybe aliasing) is written
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-            *reinterpret_cast<float2*>(gw + g4 * GW + 8 * nb + 2 * t4) =
+        for (int nb = 0; nb < kBandCols / 8; ++nb) {
+            *reinterpret_cast<float2*>(g + g4 * kGW + 8 * nb + 2 * t4) =
                 make_float2(gacc[nb][0], gacc[nb][1]);
-            *reinterpret_cast<float2*>(gw + (g4 + 8) * GW + 8 * nb + 2 * t4) =
+            *reinterpret_cast<float2*>(g + (g4 + 8) * kGW + 8 * nb + 2 * t4) =
                 make_float2(gacc[nb][2], gacc[nb][3]);
         }
     }
     __syncwarp();
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int jl = 8 * nt + 2 * t4 + e;
-            s[nt][e] += gw[g4 * GW + jl + 15 - g4];
-            s[nt][2 + e] += gw[(g4 + 8) * GW + jl + 7 - g4];
-        }
-    }
-    __syncwarp();
-
-    // ---- scale, mask, online softmax
     float mx0 = acc.m[0], mx1 = acc.m[1];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
+    for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const bool ok = (kb + 8 * nt + 2 * t4 + e) < kvalid;
-            s[nt][e] = ok ? s[nt][e] * scale_log2 : -INFINITY;
-            s[nt][2 + e] = ok ? s[nt][2 + e] * scale_log2 : -INFINITY;
+            const int j = 8 * nt + 2 * t4 + e;
+            const bool ok = j < kvalid;
+            const float b0 = g[g4 * kGW + j + 15 - g4];
+            const float b1 = g[(g4 + 8) * kGW + j + 7 - g4];
+            s[nt][e] = ok ? (s[nt][e] + b0) * scale_log2 : -INFINITY;
+            s[nt][2 + e] = ok ? (s[nt][2 + e] + b1) * scale_log2 : -INFINITY;
         }
         mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
         mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
@@ -235,21 +160,23 @@ __device__ __forceinline__ void stage_compute(WarpAcc& acc, const uint32_t (&qa)
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
     const float base0 = (mx0 == -INFINITY) ? 0.f : mx0;
     const float base1 = (mx1 == -INFINITY) ? 0.f : mx1;
-    const float alpha0 = exp2f(acc.m[0] - base0);
-    const float alpha1 = exp2f(acc.m[1] - base1);
-    acc.m[0] = mx0;
-    acc.m[1] = mx1;
-    acc.l[0] *= alpha0;
-    acc.l[1] *= alpha1;
+    if (mx0 != acc.m[0] || mx1 != acc.m[1]) {
+        const float alpha0 = exp2f(acc.m[0] - base0);
+        const float alpha1 = exp2f(acc.m[1] - base1);
+        acc.l[0] *= alpha0;
+        acc.l[1] *= alpha1;
 #pragma unroll
-    for (int dt = 0; dt < 8; ++dt) {
-        acc.o[dt][0] *= alpha0;
-        acc.o[dt][1] *= alpha0;
-        acc.o[dt][2] *= alpha1;
-        acc.o[dt][3] *= alpha1;
+        for (int dt = 0; dt < 8; ++dt) {
+            acc.o[dt][0] *= alpha0;
+            acc.o[dt][1] *= alpha0;
+            acc.o[dt][2] *= alpha1;
+            acc.o[dt][3] *= alpha1;
+        }
+        acc.m[0] = mx0;
+        acc.m[1] = mx1;
     }
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
+    for (int nt = 0; nt < 8; ++nt) {
         s[nt][0] = exp2f(s[nt][0] - base0);
         s[nt][1] = exp2f(s[nt][1] - base0);
         s[nt][2] = exp2f(s[nt][2] - base1);
@@ -257,76 +184,97 @@ __device__ __forceinline__ void stage_compute(WarpAcc& acc, const uint32_t (&qa)
         acc.l[0] += s[nt][0] + s[nt][1];
         acc.l[1] += s[nt][2] + s[nt][3];
     }
-
-    // ---- O += P . V
+    const bool tail = kvalid < kStageKeys;
 #pragma unroll
-    for (int kk = 0; kk < NK / 16; ++kk) {
+    for (int kk = 0; kk < 4; ++kk) {
         const uint32_t pa[4] = {pack_bf16(s[2 * kk][0], s[2 * kk][1]),
                                 pack_bf16(s[2 * kk][2], s[2 * kk][3]),
                                 pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]),
                                 pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3])};
-        const int row = kb + 16 * kk + ((mi & 1) << 3) + (lane & 7);
+        const int row = 16 * kk + ((mi & 1) << 3) + (lane & 7);
+        // keys held by this lane's B fragments: b0,b2 -> 16kk+2t(+1), b1,b3 -> 16kk+8+2t(+1)
+        const int k0 = 16 * kk + 2 * t4;
 #pragma unroll
         for (int dp = 0; dp < 4; ++dp) {
             uint32_t b0, b1, b2, b3;
             ldsm_x4_t(v_s + swz128(row, 2 * dp + (mi >> 1)), b0, b1, b2, b3);
+            if (tail) {   // V rows past the last key may hold anything (0 * NaN is NaN)
+                const uint32_t m0 = (k0 < kvalid ? 0xffffu : 0u) | (k0 + 1 < kvalid ? 0xffff0000u : 0u);
+                const uint32_t m1 =
+                    (k0 + 8 < kvalid ? 0xffffu : 0u) | (k0 + 9 < kvalid ? 0xffff0000u : 0u);
+                b0 &= m0;
+                b2 &= m0;
+                b1 &= m1;
+                b3 &= m1;
+            }
             mma_bf16_16816(acc.o[2 * dp], pa, b0, b1);
             mma_bf16_16816(acc.o[2 * dp + 1], pa, b2, b3);
         }
     }
 }
 
-// Write the warp's partial (O, m, l) into the combine area: comb_o [KG][Tp][OW],
-// comb_m / comb_l [KG][Tp].  Call after the key loop's last __syncthreads.
-template <int MT>
-__device__ __forceinline__ void write_partial(WarpAcc& acc, float* comb_o, float* comb_m,
-                                              float* comb_l, int mt, int kg, int lane)
+// Quad-reduce the row sums (each thread held its own columns' share).
+__device__ __forceinline__ void acc_reduce_l(WarpAcc& acc)
 {
-    using TL = Tile<MT>;
-    acc.l[0] += __shfl_xor_sync(0xffffffffu, acc.l[0], 1);
-    acc.l[0] += __shfl_xor_sync(0xffffffffu, acc.l[0], 2);
-    acc.l[1] += __shfl_xor_sync(0xffffffffu, acc.l[1], 1);
-    acc.l[1] += __shfl_xor_sync(0xffffffffu, acc.l[1], 2);
-    const int g4 = lane >> 2, t4 = lane & 3;
-    const int r0 = kg * TL::Tp + 16 * mt + g4;
 #pragma unroll
-    for (int dt = 0; dt < 8; ++dt) {
-        *reinterpret_cast<float2*>(comb_o + r0 * TL::OW + 8 * dt + 2 * t4) =
-            make_float2(acc.o[dt][0], acc.o[dt][1]);
-        *reinterpret_cast<float2*>(comb_o + (r0 + 8) * TL::OW + 8 * dt + 2 * t4) =
-            make_float2(acc.o[dt][2], acc.o[dt][3]);
-    }
-    if (t4 == 0) {
-        comb_m[r0] = acc.m[0];
-        comb_m[r0 + 8] = acc.m[1];
-        comb_l[r0] = acc.l[0];
-        comb_l[r0 + 8] = acc.l[1];
+    for (int r = 0; r < 2; ++r) {
+        acc.l[r] += __shfl_xor_sync(0xffffffffu, acc.l[r], 1);
+        acc.l[r] += __shfl_xor_sync(0xffffffffu, acc.l[r], 2);
     }
 }
 
-// Merge the KG partials of query row `row` (dims [d0, d0+8)) and return 8 bf16 packed.
-template <int MT>
-__device__ __forceinline__ uint4 combine_row8(const float* comb_o, const float* comb_m,
-                                              const float* comb_l, int row, int d0)
+// Write the warp's partial (O, m, l) of its 16 rows into comb_o [.][kOW], comb_m, comb_l at
+// row offset r0 (call acc_reduce_l first).
+__device__ __forceinline__ void write_partial(const WarpAcc& acc, float* comb_o, float* comb_m,
+                                              float* comb_l, int r0, int lane)
 {
-    using TL = Tile<MT>;
-    float mstar = -INFINITY;
+    const int g4 = lane >> 2, t4 = lane & 3;
 #pragma unroll
-    for (int k = 0; k < TL::KG; ++k) mstar = fmaxf(mstar, comb_m[k * TL::Tp + row]);
+    for (int dt = 0; dt < 8; ++dt) {
+        *reinterpret_cast<float2*>(comb_o + (r0 + g4) * kOW + 8 * dt + 2 * t4) =
+            make_float2(acc.o[dt][0], acc.o[dt][1]);
+        *reinterpret_cast<float2*>(comb_o + (r0 + g4 + 8) * kOW + 8 * dt + 2 * t4) =
+            make_float2(acc.o[dt][2], acc.o[dt][3]);
+    }
+    if (t4 == 0) {
+        comb_m[r0 + g4] = acc.m[0];
+        comb_m[r0 + g4 + 8] = acc.m[1];
+        comb_l[r0 + g4] = acc.l[0];
+        comb_l[r0 + g4 + 8] = acc.l[1];
+    }
+}
+
+// Merge the nparts partials of query row `row` (stride `pstride` rows between partials),
+// dims [d0, d0+8), and return them as 8 bf16.
+__device__ __forceinline__ uint4 combine_row8(const float* comb_o, const float* comb_m,
+                                              const float* comb_l, int nparts, int pstride,
+                                              int row, int d0)
+{
+    float mstar = -INFINITY;
+    for (int k = 0; k < nparts; ++k) mstar = fmaxf(mstar, comb_m[k * pstride + row]);
     float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float L = 0.f;
-#pragma unroll
-    for (int k = 0; k < TL::KG; ++k) {
-        const float mk = comb_m[k * TL::Tp + row];
+    for (int k = 0; k < nparts; ++k) {
+        const float mk = comb_m[k * pstride + row];
         const float w = (mk == -INFINITY) ? 0.f : exp2f(mk - mstar);
-        L += w * comb_l[k * TL::Tp + row];
-        const float* src = comb_o + (k * TL::Tp + row) * TL::OW + d0;
+        L += w * comb_l[k * pstride + row];
+        const float* src = comb_o + (k * pstride + row) * kOW + d0;
 #pragma unroll
         for (int d = 0; d < 8; ++d) o[d] += w * src[d];
     }
     const float inv = 1.f / L;
     return make_uint4(pack_bf16(o[0] * inv, o[1] * inv), pack_bf16(o[2] * inv, o[3] * inv),
                       pack_bf16(o[4] * inv, o[5] * inv), pack_bf16(o[6] * inv, o[7] * inv));
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 }  // namespace oasr

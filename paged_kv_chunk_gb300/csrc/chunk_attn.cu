@@ -39,19 +39,40 @@ struct ChunkArgs {
     float scale_log2;        // scale * log2(e)
 };
 
-__device__ __forceinline__ float bf16_bits_to_f32(uint16_t x)
-{
-    return __uint_as_float(static_cast<uint32_t>(x) << 16);
-}
+// Shared-memory plan of the streaming kernel (byte offsets from a 1024-aligned base).
+// Slot i holds one stage: K rows [64][128 B], V rows [64][128 B], rel band [RB][128 B], all
+// 128-byte swizzled by TMA.  With one m-tile the skew scratch of the consuming warp reuses
+// the slot's band tile; otherwise each consumer warp has its own scratch.  After the key
+// loop the slots hold the cross-warp combine.
+template <int MT, int NS>
+struct ChunkSmem {
+    using TL = Tile<MT>;
+    static constexpr bool kGInBand = MT == 1;
+    static constexpr int kBand = TL::RB * kRowBytes;
+    static constexpr int kSlot = 2 * kStageKeys * kRowBytes + kBand;
+    static constexpr int off_slots = 0;
+    static constexpr int off_q = NS * kSlot;
+    static constexpr int off_g = off_q + TL::Tp * kRowBytes;
+    static constexpr int off_u = off_g + (kGInBand ? 0 : kConsumerWarps * kGBytes);
+    static constexpr int off_vb = off_u + kHeadDim * 4;
+    static constexpr int off_bar = off_vb + kHeadDim * 4;   // full[NS], empty[NS], q
+    static constexpr int bytes = off_bar + (2 * NS + 1) * 8 + 1024;
+    static constexpr int comb_o = 0;
+    static constexpr int comb_m = comb_o + TL::KG * TL::Tp * kOW * 4;
+    static constexpr int comb_l = comb_m + TL::KG * TL::Tp * 4;
+    static_assert(kSlot % 1024 == 0 && off_q % 1024 == 0, "TMA tiles need 1024-byte alignment");
+    static_assert(!kGInBand || kGBytes <= kBand, "skew scratch must fit the band tile");
+    static_assert(comb_l + TL::KG * TL::Tp * 4 <= NS * kSlot, "combine area");
+};
 
 template <int MT, int NS, bool FUSED>
-__global__ void __launch_bounds__(kThreads) chunk_attn_bf16_kernel(
+__global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
     const ChunkArgs a)
 {
     using TL = Tile<MT>;
-    using SP = SmemPlan<MT, NS>;
+    using SP = ChunkSmem<MT, NS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -69,24 +90,28 @@ __global__ void __launch_bounds__(kThreads) chunk_attn_bf16_kernel(
     const int n_stages = (K + kStageKeys - 1) / kStageKeys;
     const int off = a.R - T - C;   // rho = off + j - i
     const uint32_t bar_full = sb + SP::off_bar;
-    const uint32_t bar_q = bar_full + NS * 8;
+    const uint32_t bar_empty = bar_full + NS * 8;
+    const uint32_t bar_q = bar_empty + NS * 8;
     float* s_u = reinterpret_cast<float*>(sm + SP::off_u);
     float* s_vb = reinterpret_cast<float*>(sm + SP::off_vb);
+    __shared__ int s_failed;
 
     if (tid == 0) {
-        for (int i = 0; i < NS; ++i) mbar_init(bar_full + 8 * i, 1);
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_empty + 8 * i, MT);
+        }
         mbar_init(bar_q, 1);
         fence_mbar_init();
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
-        prefetch_tensormap(&tm_r);
+        s_failed = 0;
     }
     __syncthreads();
 
-    // Issue stage s into buffer s % NS (thread 0 only).
+    // Stage s into slot s % NS (producer lane only).
     auto issue = [&](int s) {
-        const int buf = s % NS;
-        const uint32_t bar = bar_full + 8 * buf;
+        const int slot = s % NS;
+        const uint32_t bar = bar_full + 8 * slot;
+        const uint32_t base = sb + SP::off_slots + slot * SP::kSlot;
         const int j0 = s * kStageKeys;
         const int box = a.box_rows;
         int rows[kStageKeys / 8];
@@ -95,37 +120,42 @@ __global__ void __launch_bounds__(kThreads) chunk_attn_bf16_kernel(
             const int j = j0 + q * box;
             if (j >= K) break;
             const int lb = j / a.block_size;
-            const int slot = j - lb * a.block_size;
+            const int slot_in_block = j - lb * a.block_size;
             const int blk = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + lb);
             if (blk < 0 || blk >= a.num_blocks) {
                 err |= kErrBounds;
-                rows[nbox++] = -2 * box;          // outside the pool: the box reads zeros
+                rows[nbox++] = -2 * box;   // outside the pool: the box reads zeros
             } else {
-                rows[nbox++] = blk * a.block_size + slot;
+                rows[nbox++] = blk * a.block_size + slot_in_block;
             }
         }
         mbar_arrive_expect_tx(bar, static_cast<uint32_t>((2 * nbox * box + TL::RB) * kRowBytes));
         const uint64_t pol = policy_evict_first();
         for (int q = 0; q < nbox; ++q) {
-            tma_load_3d_hint(sb + SP::off_k + buf * SP::kKV + q * box * kRowBytes, &tm_k, bar, 0,
-                             h, rows[q], pol);
-            tma_load_3d_hint(sb + SP::off_v + buf * SP::kKV + q * box * kRowBytes, &tm_v, bar, 0,
+            tma_load_3d_hint(base + q * box * kRowBytes, &tm_k, bar, 0, h, rows[q], pol);
+            tma_load_3d_hint(base + kStageKeys * kRowBytes + q * box * kRowBytes, &tm_v, bar, 0,
                              h, rows[q], pol);
         }
-        tma_load_3d(sb + SP::off_r + buf * SP::kR, &tm_r, bar, 0, h, off + j0 - (TL::Tp - 1));
+        tma_load_3d(base + 2 * kStageKeys * kRowBytes, &tm_r, bar, 0, h,
+                    off + j0 - (TL::Tp - 1));
     };
 
     const int pre = n_stages < NS ? n_stages : NS;
     const int first_chunk_stage = FUSED ? C / kStageKeys : n_stages;
-    if (tid == 0) {
+    int issued = 0;
+    const bool producer = warp == kConsumerWarps;
+    if (producer && lane == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_r);
         mbar_arrive_expect_tx(bar_q, TL::Tp * kRowBytes);
         tma_load_3d(sb + SP::off_q, &tm_q, bar_q, 0, h, b * T);
-        for (int s = 0; s < pre && s < first_chunk_stage; ++s) issue(s);
+        for (; issued < pre && issued < first_chunk_stage; ++issued) issue(issued);
     }
     if (tid < kHeadDim)
-        s_u[tid] = bf16_bits_to_f32(__ldg(a.pos_bias_u + h * kHeadDim + tid));
-    else
-        s_vb[tid - kHeadDim] = bf16_bits_to_f32(__ldg(a.pos_bias_v + h * kHeadDim + tid - kHeadDim));
+        s_u[tid] = bf16_lo(__ldg(a.pos_bias_u + h * kHeadDim + tid));
+    else if (tid < 2 * kHeadDim)
+        s_vb[tid - kHeadDim] = bf16_lo(__ldg(a.pos_bias_v + h * kHeadDim + tid - kHeadDim));
     if constexpr (FUSED) {
         // This head's slice of the chunk: T rows x 8 vectors of 16 B, for K and for V.
         for (int idx = tid; idx < 2 * T * 8; idx += kThreads) {
@@ -146,62 +176,66 @@ __global__ void __launch_bounds__(kThreads) chunk_attn_bf16_kernel(
             *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
         }
         fence_proxy_async_global();
-        __syncthreads();
-        if (tid == 0)
-            for (int s = first_chunk_stage; s < pre; ++s) issue(s);
-    } else {
-        __syncthreads();
     }
+    __syncthreads();
 
-    const int mt = warp % MT, kg = warp / MT;
-    float* gw = reinterpret_cast<float*>(sm + SP::off_g) + warp * 16 * TL::GW;
-    uint32_t qa[4][4];
-    WarpAcc acc;
-    acc_init(acc);
-    bool failed = __syncthreads_or(!mbar_wait(bar_q, 0));
-    int s = 0;
-    if (!failed) {
-        load_q_frags(sb + SP::off_q, mt, lane, qa);
-        for (; s < n_stages; ++s) {
-            const int buf = s % NS;
-            const bool ok = mbar_wait(bar_full + 8 * buf, (s / NS) & 1);
-            const int kvalid = min(kStageKeys, K - s * kStageKeys);
-            float* uk = reinterpret_cast<float*>(sm + SP::off_uk) + buf * kStageKeys;
-            float* vr = reinterpret_cast<float*>(sm + SP::off_vr) + buf * TL::RB;
-            if (ok)
-                stage_prologue<MT>(sm + SP::off_k + buf * SP::kKV, sm + SP::off_v + buf * SP::kKV,
-                                   sm + SP::off_r + buf * SP::kR, s_u, s_vb, uk, vr, kvalid, tid);
-            if (__syncthreads_or(!ok)) { failed = true; break; }
-            stage_compute<MT>(acc, qa, sb + SP::off_k + buf * SP::kKV,
-                              sb + SP::off_v + buf * SP::kKV, sb + SP::off_r + buf * SP::kR, uk,
-                              vr, gw, kvalid, a.scale_log2, mt, kg, lane);
-            __syncthreads();
-            if (tid == 0 && s + NS < n_stages) {
-                fence_proxy_async_smem();
-                issue(s + NS);
+    if (producer) {
+        if (lane == 0) {
+            for (; issued < n_stages; ++issued) {
+                const int slot = issued % NS;
+                if (issued >= NS &&
+                    !mbar_wait(bar_empty + 8 * slot, ((issued / NS) - 1) & 1)) {
+                    err |= kErrTimeout;
+                    break;
+                }
+                issue(issued);
             }
-        }
-    }
-    if (failed) {
-        // Let the copies still in flight land before the CTA's shared memory is released.
-        if (tid == 0) {
-            const int issued = min(n_stages, s + NS);
-            for (int s2 = s; s2 < issued; ++s2)
-                mbar_wait(bar_full + 8 * (s2 % NS), (s2 / NS) & 1, 100000000ull);
-            err |= kErrTimeout;
         }
         if (err) atomicOr(a.status, err);
         return;
     }
 
-    float* comb_o = reinterpret_cast<float*>(sm + SP::off_comb_o);
-    float* comb_m = reinterpret_cast<float*>(sm + SP::off_comb_ml);
-    float* comb_l = comb_m + TL::KG * TL::Tp;
-    write_partial<MT>(acc, comb_o, comb_m, comb_l, mt, kg, lane);
-    __syncthreads();
-    for (int idx = tid; idx < T * 8; idx += kThreads) {
+    // ---- consumers
+    const int mt = warp % MT, kg = warp / MT;
+    bool failed = !mbar_wait(bar_q, 0);
+    uint32_t qu[4][4], qv[4][4];
+    WarpAcc acc;
+    acc_init(acc);
+    if (!failed) {
+        make_q_frags(sb + SP::off_q, s_u, s_vb, mt, lane, qu, qv);
+        float* gw = reinterpret_cast<float*>(sm + SP::off_g) + warp * (kGBytes / 4);
+        for (int s = kg; s < n_stages; s += TL::KG) {
+            const int slot = s % NS;
+            if (!mbar_wait(bar_full + 8 * slot, (s / NS) & 1)) { failed = true; break; }
+            const uint32_t base = sb + SP::off_slots + slot * SP::kSlot;
+            const uint32_t band = base + 2 * kStageKeys * kRowBytes;
+            float* g = SP::kGInBand
+                           ? reinterpret_cast<float*>(sm + SP::off_slots + slot * SP::kSlot +
+                                                      2 * kStageKeys * kRowBytes)
+                           : gw;
+            warp_stage(acc, qu, qv, base, base + kStageKeys * kRowBytes, band,
+                       TL::Tp - 16 - 16 * mt, g, min(kStageKeys, K - s * kStageKeys),
+                       a.scale_log2, lane);
+            if (SP::kGInBand) fence_proxy_async_smem();   // the next TMA into this slot
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+        }
+    }
+    if (failed) s_failed = 1;
+    named_bar_sync(1, 32 * kConsumerWarps);
+    if (s_failed) {
+        if (tid == 0) atomicOr(a.status, err | kErrTimeout);
+        return;
+    }
+    float* comb_o = reinterpret_cast<float*>(sm + SP::comb_o);
+    float* comb_m = reinterpret_cast<float*>(sm + SP::comb_m);
+    float* comb_l = reinterpret_cast<float*>(sm + SP::comb_l);
+    acc_reduce_l(acc);
+    write_partial(acc, comb_o, comb_m, comb_l, kg * TL::Tp + 16 * mt, lane);
+    named_bar_sync(1, 32 * kConsumerWarps);
+    for (int idx = tid; idx < T * 8; idx += 32 * kConsumerWarps) {
         const int row = idx >> 3, d0 = (idx & 7) * 8;
-        const uint4 v = combine_row8<MT>(comb_o, comb_m, comb_l, row, d0);
+        const uint4 v = combine_row8(comb_o, comb_m, comb_l, TL::KG, TL::Tp, row, d0);
         *reinterpret_cast<uint4*>(a.out + ((static_cast<long long>(b) * T + row) * a.H + h) *
                                               kHeadDim + d0) = v;
     }
@@ -345,7 +379,7 @@ oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, voi
     unsigned* status = status_word();
     if (!status) return OASR_ERR_CUDA;
     auto kern = chunk_attn_bf16_kernel<MT, NS, FUSED>;
-    constexpr int smem = SmemPlan<MT, NS>::bytes;
+    constexpr int smem = ChunkSmem<MT, NS>::bytes;
     if (!ensure_smem(kern, smem, g_smem_done[slot])) return OASR_ERR_CUDA;
     ChunkArgs a;
     a.k_new = static_cast<const uint16_t*>(k_new);
@@ -405,7 +439,7 @@ oasr_status dispatch(const void* q, const void* k_new, const void* v_new, void* 
     }
     const int f = FUSED ? 8 : 0;
     if (T <= 16)
-        return launch_bf16<1, 3, FUSED>(q, k_new, v_new, k_pool, v_pool, num_blocks, block_size,
+        return launch_bf16<1, 4, FUSED>(q, k_new, v_new, k_pool, v_pool, num_blocks, block_size,
                                         bt, mbps, cs, u, vb, rel, R, out, B, T, H, scale, stream,
                                         f + 0);
     if (T <= 32)
