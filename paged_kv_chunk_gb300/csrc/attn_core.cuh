@@ -213,194 +213,6 @@ __device__ __forceinline__ void warp_stage(WarpAcc& acc, const uint32_t (&qu)[4]
     }
 }
 
-// Variant of warp_stage for a CTA whose position term is precomputed: gs points at
-// row 0 of a [16][gsw] fp32 tile holding (q_i+v).rel[rho(i, j)] for every key j (already
-// skewed), so a stage only adds gs[i][j0 + j].  Same masking and softmax as warp_stage.
-__device__ __forceinline__ void warp_stage_pre(WarpAcc& acc, const uint32_t (&qu)[4][4],
-                                               uint32_t k_s, uint32_t v_s, const float* gs,
-                                               int gsw, int j0, int kvalid, float scale_log2,
-                                               int lane)
-{
-    const int g4 = lane >> 2, t4 = lane & 3, mi = lane >> 3;
-    float s[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-        const float2 p0 = *reinterpret_cast<const float2*>(gs + g4 * gsw + j0 + 8 * nt + 2 * t4);
-        const float2 p1 =
-            *reinterpret_cast<const float2*>(gs + (g4 + 8) * gsw + j0 + 8 * nt + 2 * t4);
-        s[nt][0] = p0.x;
-        s[nt][1] = p0.y;
-        s[nt][2] = p1.x;
-        s[nt][3] = p1.y;
-    }
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(k_s + swz128(16 * np + ((mi >> 1) << 3) + (lane & 7), 2 * ks + (mi & 1)), b0,
-                    b1, b2, b3);
-            mma_bf16_16816(s[2 * np], qu[ks], b0, b1);
-            mma_bf16_16816(s[2 * np + 1], qu[ks], b2, b3);
-        }
-    }
-    float mx0 = acc.m[0], mx1 = acc.m[1];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const bool ok = 8 * nt + 2 * t4 + e < kvalid;
-            s[nt][e] = ok ? s[nt][e] * scale_log2 : -INFINITY;
-            s[nt][2 + e] = ok ? s[nt][2 + e] * scale_log2 : -INFINITY;
-        }
-        mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-        mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float base0 = (mx0 == -INFINITY) ? 0.f : mx0;
-    const float base1 = (mx1 == -INFINITY) ? 0.f : mx1;
-    if (mx0 != acc.m[0] || mx1 != acc.m[1]) {
-        const float alpha0 = exp2f(acc.m[0] - base0);
-        const float alpha1 = exp2f(acc.m[1] - base1);
-        acc.l[0] *= alpha0;
-        acc.l[1] *= alpha1;
-#pragma unroll
-        for (int dt = 0; dt < 8; ++dt) {
-            acc.o[dt][0] *= alpha0;
-            acc.o[dt][1] *= alpha0;
-            acc.o[dt][2] *= alpha1;
-            acc.o[dt][3] *= alpha1;
-        }
-        acc.m[0] = mx0;
-        acc.m[1] = mx1;
-    }
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-        s[nt][0] = exp2f(s[nt][0] - base0);
-        s[nt][1] = exp2f(s[nt][1] - base0);
-        s[nt][2] = exp2f(s[nt][2] - base1);
-        s[nt][3] = exp2f(s[nt][3] - base1);
-        acc.l[0] += s[nt][0] + s[nt][1];
-        acc.l[1] += s[nt][2] + s[nt][3];
-    }
-    const bool tail = kvalid < kStageKeys;
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t pa[4] = {pack_bf16(s[2 * kk][0], s[2 * kk][1]),
-                                pack_bf16(s[2 * kk][2], s[2 * kk][3]),
-                                pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]),
-                                pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3])};
-        const int row = 16 * kk + ((mi & 1) << 3) + (lane & 7);
-        const int k0 = 16 * kk + 2 * t4;
-#pragma unroll
-        for (int dp = 0; dp < 4; ++dp) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(v_s + swz128(row, 2 * dp + (mi >> 1)), b0, b1, b2, b3);
-            if (tail) {
-                const uint32_t m0 = (k0 < kvalid ? 0xffffu : 0u) | (k0 + 1 < kvalid ? 0xffff0000u : 0u);
-                const uint32_t m1 =
-                    (k0 + 8 < kvalid ? 0xffffu : 0u) | (k0 + 9 < kvalid ? 0xffff0000u : 0u);
-                b0 &= m0;
-                b2 &= m0;
-                b1 &= m1;
-                b3 &= m1;
-            }
-            mma_bf16_16816(acc.o[2 * dp], pa, b0, b1);
-            mma_bf16_16816(acc.o[2 * dp + 1], pa, b2, b3);
-        }
-    }
-}
-
-// Position term of 16 query rows against every key, computed once per CTA.
-//
-// The dot product over d is invariant under a permutation of d applied to both operands,
-// so the band product uses the order in which lane t of a quad holds dims
-// [16t, 16t+16) for all four k-steps (logical k = 16ks + 8h + 2t + e <-> d = 16t + 4ks +
-// 2h + e).  Each lane then reads its B fragments for a rel row with two 16-byte loads
-// straight from global memory (the table is small and shared by the cohort, so it sits
-// in L2), and no shared memory is staged for it.
-//
-// qv_perm: A fragments of bf16(q+v) in that order.  For band rows m = 8nb + (0..7) (rel
-// row rho = rho0 + m; rows outside [0, R) read as zeros), G[i][m] lands skewed at
-// gs[i][m - 15 + i] when that key exists.
-__device__ __forceinline__ void make_qv_perm(uint32_t q_s, const float* v, int lane,
-                                             uint32_t (&qv)[4][4])
-{
-    const int g4 = lane >> 2, t4 = lane & 3;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {          // rows g4 and g4 + 8
-        const int row = g4 + 8 * half;
-        uint32_t w[8];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {               // 16-byte chunks 2t, 2t+1 of the row
-            uint4 x;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
-                         : "r"(q_s + swz128(row, 2 * t4 + c)));
-            w[4 * c + 0] = x.x;
-            w[4 * c + 1] = x.y;
-            w[4 * c + 2] = x.z;
-            w[4 * c + 3] = x.w;
-        }
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {        // word 2ks+hh holds d = 16t + 4ks + 2hh + {0,1}
-                const int d = 16 * t4 + 4 * ks + 2 * hh;
-                const uint32_t word = w[2 * ks + hh];
-                qv[ks][2 * hh + half] =
-                    pack_bf16(bf16_lo(word) + v[d], bf16_hi(word) + v[d + 1]);
-            }
-        }
-    }
-}
-
-// Position-term tiles nb = nb0, nb0 + step, ... (< n_bt) of one warp.  Loads for up to
-// kPosBatch tiles are issued before any of them is used, so the L2 round trips overlap.
-constexpr int kPosBatch = 8;
-
-__device__ __forceinline__ void pos_term_tiles(const uint32_t (&qv)[4][4], const uint16_t* rel_h,
-                                               int H, int R, int rho0, int nb0, int step, int n_bt,
-                                               int K, float* gs, int gsw, int lane)
-{
-    const int g4 = lane >> 2, t4 = lane & 3;
-    for (int nb_base = nb0; nb_base < n_bt; nb_base += kPosBatch * step) {
-        uint4 lo[kPosBatch], hi[kPosBatch];
-#pragma unroll
-        for (int u = 0; u < kPosBatch; ++u) {
-            const int nb = nb_base + u * step;
-            const int rho = rho0 + 8 * nb + g4;
-            lo[u] = make_uint4(0u, 0u, 0u, 0u);
-            hi[u] = lo[u];
-            if (nb < n_bt && rho >= 0 && rho < R) {
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    rel_h + static_cast<long long>(rho) * H * kHeadDim + 16 * t4);
-                lo[u] = __ldg(src);
-                hi[u] = __ldg(src + 1);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kPosBatch; ++u) {
-            const int nb = nb_base + u * step;
-            if (nb >= n_bt) break;
-            const uint32_t w[8] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w,
-                                   hi[u].x, hi[u].y, hi[u].z, hi[u].w};
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) mma_bf16_16816(acc, qv[ks], w[2 * ks], w[2 * ks + 1]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = g4 + 8 * (e >> 1);
-                const int j = 8 * nb + 2 * t4 + (e & 1) - 15 + i;
-                if (j >= 0 && j < K) gs[i * gsw + j] = acc[e];
-            }
-        }
-    }
-}
-
 // Quad-reduce the row sums (each thread held its own columns' share).
 __device__ __forceinline__ void acc_reduce_l(WarpAcc& acc)
 {

@@ -44,6 +44,9 @@ struct ChunkArgs {
 // 128-byte swizzled by TMA.  With one m-tile the skew scratch of the consuming warp reuses
 // the slot's band tile; otherwise each consumer warp has its own scratch.  After the key
 // loop the slots hold the cross-warp combine.
+// Block-table entries a CTA caches in shared memory.
+constexpr int kMaxPages = 512;
+
 template <int MT, int NS>
 struct ChunkSmem {
     using TL = Tile<MT>;
@@ -55,7 +58,8 @@ struct ChunkSmem {
     static constexpr int off_g = off_q + TL::Tp * kRowBytes;
     static constexpr int off_u = off_g + (kGInBand ? 0 : kConsumerWarps * kGBytes);
     static constexpr int off_vb = off_u + kHeadDim * 4;
-    static constexpr int off_bar = off_vb + kHeadDim * 4;   // full[NS], empty[NS], q
+    static constexpr int off_bt = off_vb + kHeadDim * 4;    // the stream's block-table row
+    static constexpr int off_bar = off_bt + kMaxPages * 4;  // full[NS], empty[NS], q
     static constexpr int bytes = off_bar + (2 * NS + 1) * 8 + 1024;
     static constexpr int comb_o = 0;
     static constexpr int comb_m = comb_o + TL::KG * TL::Tp * kOW * 4;
@@ -96,6 +100,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     float* s_vb = reinterpret_cast<float*>(sm + SP::off_vb);
     __shared__ int s_failed;
 
+    int* s_bt = reinterpret_cast<int*>(sm + SP::off_bt);
     if (tid == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(bar_full + 8 * i, 1);
@@ -105,6 +110,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         fence_mbar_init();
         s_failed = 0;
     }
+    const int n_pages = (K + a.block_size - 1) / a.block_size;   // <= kMaxPages (host check)
+    for (int i = tid; i < n_pages; i += kThreads)
+        s_bt[i] = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + i);
     __syncthreads();
 
     // Stage s into slot s % NS (producer lane only).
@@ -121,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
             if (j >= K) break;
             const int lb = j / a.block_size;
             const int slot_in_block = j - lb * a.block_size;
-            const int blk = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + lb);
+            const int blk = s_bt[lb];
             if (blk < 0 || blk >= a.num_blocks) {
                 err |= kErrBounds;
                 rows[nbox++] = -2 * box;   // outside the pool: the box reads zeros
@@ -236,235 +244,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     for (int idx = tid; idx < T * 8; idx += 32 * kConsumerWarps) {
         const int row = idx >> 3, d0 = (idx & 7) * 8;
         const uint4 v = combine_row8(comb_o, comb_m, comb_l, TL::KG, TL::Tp, row, d0);
-        *reinterpret_cast<uint4*>(a.out + ((static_cast<long long>(b) * T + row) * a.H + h) *
-                                              kHeadDim + d0) = v;
-    }
-    if (err) atomicOr(a.status, err);
-}
-
-// ------------------------------------------------------ T <= 16: position term up front
-//
-// For chunks of at most 16 frames the whole position term of the CTA's (stream, head),
-// (q_i+v).rel[rho(i, j)] for all 16 rows and all K keys, fits in shared memory, stored
-// already skewed.  Warp roles:
-//   warps 0-3  consumers: stage s goes to warp s % 4; content product, softmax, P.V;
-//   warp 4     producer: caches the stream's block-table row in shared memory, then
-//              issues each stage's K/V page boxes with TMA into a ring of 16 KB slots;
-//   warps 5-6  position term: warp 5 + (s % 2) computes the band tiles stage s needs
-//              (B fragments straight from the L2-resident table, see pos_term_tiles)
-//              and arrives on that stage's `pos` mbarrier.
-// So the position term is computed off the consumers' critical path, and the slots carry
-// K and V only, which lets more stages be in flight per SM.
-
-constexpr int kPosWarps = 2;
-constexpr int kPreThreads = 32 * (kConsumerWarps + 1 + kPosWarps);
-constexpr int kPreMaxSlots = 8;
-constexpr int kPreMaxStages = 64;       // keys <= 4096
-constexpr int kPreMaxPages = 512;       // block-table entries cached per stream
-
-struct PreSmem {
-    int ns, gsw;
-    int off_q, off_gs, off_u, off_vb, off_bt, off_bar, bytes;
-    __host__ __device__ PreSmem(int ns_, int gsw_) : ns(ns_), gsw(gsw_)
-    {
-        off_q = ns * 2 * kStageKeys * kRowBytes;
-        off_gs = off_q + 16 * kRowBytes;
-        off_u = off_gs + 16 * gsw * 4;
-        off_vb = off_u + kHeadDim * 4;
-        off_bt = off_vb + kHeadDim * 4;
-        off_bar = off_bt + kPreMaxPages * 4;   // full[8], empty[8], q, pos[64]
-        bytes = off_bar + (2 * kPreMaxSlots + 1 + kPreMaxStages) * 8 + 1024;
-    }
-};
-
-// Row stride of the skewed position tile for at most `cap` keys: whole stages, and
-// 8 (mod 32) floats so that the per-stage float2 reads of 8 rows hit distinct banks.
-inline int pre_gsw(int cap) { return (cap + kStageKeys - 1) / kStageKeys * kStageKeys + 8; }
-
-template <bool FUSED>
-__global__ void __launch_bounds__(kPreThreads) chunk_attn_pre_kernel(
-    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_v, const ChunkArgs a, const uint16_t* __restrict__ rel,
-    int ns, int gsw)
-{
-    const PreSmem SP(ns, gsw);
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t sb = smem_addr(sm);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.x / a.H, h = blockIdx.x - (blockIdx.x / a.H) * a.H;
-    const int T = a.T;
-    unsigned err = 0;
-
-    int C = __ldg(a.cache_seqlens + b);
-    if (C < 0) { C = 0; err |= kErrBounds; }
-    int K = C + T;
-    const int cap = a.mbps * a.block_size;
-    if (K > cap) { K = cap; err |= kErrBounds; }
-    const int n_stages = (K + kStageKeys - 1) / kStageKeys;
-    const int off = a.R - T - C;   // rho = off + j - i
-    const uint32_t bar_full = sb + SP.off_bar;
-    const uint32_t bar_empty = bar_full + kPreMaxSlots * 8;
-    const uint32_t bar_q = bar_empty + kPreMaxSlots * 8;
-    const uint32_t bar_pos = bar_q + 8;
-    float* s_u = reinterpret_cast<float*>(sm + SP.off_u);
-    float* s_vb = reinterpret_cast<float*>(sm + SP.off_vb);
-    float* gs = reinterpret_cast<float*>(sm + SP.off_gs);
-    int* s_bt = reinterpret_cast<int*>(sm + SP.off_bt);
-    __shared__ int s_failed;
-
-    if (tid == 0) {
-        for (int i = 0; i < ns; ++i) {
-            mbar_init(bar_full + 8 * i, 1);
-            mbar_init(bar_empty + 8 * i, 1);
-        }
-        mbar_init(bar_q, 1);
-        for (int i = 0; i < n_stages; ++i) mbar_init(bar_pos + 8 * i, 1);
-        fence_mbar_init();
-        s_failed = 0;
-    }
-    // The stream's block-table row (the pages holding keys [0, K)).
-    const int n_pages = (K + a.block_size - 1) / a.block_size;
-    for (int i = tid; i < n_pages; i += kPreThreads)
-        s_bt[i] = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + i);
-    if (tid < kHeadDim)
-        s_u[tid] = bf16_lo(__ldg(a.pos_bias_u + h * kHeadDim + tid));
-    else if (tid < 2 * kHeadDim)
-        s_vb[tid - kHeadDim] = bf16_lo(__ldg(a.pos_bias_v + h * kHeadDim + tid - kHeadDim));
-    __syncthreads();
-
-    auto issue = [&](int s) {   // stage s into slot s % ns (producer lane only)
-        const int slot = s % ns;
-        const uint32_t bar = bar_full + 8 * slot;
-        const uint32_t base = sb + slot * 2 * kStageKeys * kRowBytes;
-        const int j0 = s * kStageKeys;
-        const int box = a.box_rows;
-        const int nbox = min(kStageKeys / box, (K - j0 + box - 1) / box);
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(2 * nbox * box * kRowBytes));
-        const uint64_t pol = policy_evict_first();
-        for (int q = 0; q < nbox; ++q) {
-            const int j = j0 + q * box;
-            const int lb = j / a.block_size;
-            const int blk = s_bt[lb];
-            int row = blk * a.block_size + (j - lb * a.block_size);
-            if (blk < 0 || blk >= a.num_blocks) {
-                err |= kErrBounds;
-                row = -2 * box;   // outside the pool: the box reads zeros
-            }
-            tma_load_3d_hint(base + q * box * kRowBytes, &tm_k, bar, 0, h, row, pol);
-            tma_load_3d_hint(base + kStageKeys * kRowBytes + q * box * kRowBytes, &tm_v, bar, 0, h,
-                             row, pol);
-        }
-    };
-
-    const int pre = n_stages < ns ? n_stages : ns;
-    const int first_chunk_stage = FUSED ? C / kStageKeys : n_stages;
-    int issued = 0;
-    const bool producer = warp == kConsumerWarps;
-    if (producer && lane == 0) {
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
-        mbar_arrive_expect_tx(bar_q, 16 * kRowBytes);
-        tma_load_3d(sb + SP.off_q, &tm_q, bar_q, 0, h, b * T);
-        for (; issued < pre && issued < first_chunk_stage; ++issued) issue(issued);
-    }
-    if constexpr (FUSED) {
-        for (int idx = tid; idx < 2 * T * 8; idx += kPreThreads) {
-            const int kv = idx >= T * 8;
-            const int rem = idx - kv * T * 8;
-            const int t = rem >> 3, c = rem & 7;
-            const int p = C + t;
-            const int lb = p / a.block_size;
-            if (lb >= a.mbps) { err |= kErrBounds; continue; }
-            const int slot = p - lb * a.block_size;
-            const int blk = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + lb);
-            if (blk < 0 || blk >= a.num_blocks) { err |= kErrBounds; continue; }
-            const uint16_t* src = (kv ? a.v_new : a.k_new) +
-                                  ((static_cast<long long>(b) * T + t) * a.H + h) * kHeadDim + c * 8;
-            uint16_t* dst = (kv ? a.v_pool : a.k_pool) +
-                            ((static_cast<long long>(blk) * a.block_size + slot) * a.H + h) * kHeadDim +
-                            c * 8;
-            *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
-        }
-        fence_proxy_async_global();
-        __syncthreads();
-    }
-
-    if (producer) {
-        if (lane == 0) {
-            for (; issued < n_stages; ++issued) {
-                const int slot = issued % ns;
-                if (issued >= ns && !mbar_wait(bar_empty + 8 * slot, ((issued / ns) - 1) & 1)) {
-                    err |= kErrTimeout;
-                    break;
-                }
-                issue(issued);
-            }
-        }
-        if (err) atomicOr(a.status, err);
-        return;
-    }
-
-    if (warp > kConsumerWarps) {
-        // ---- position-term warps
-        const int pw = warp - kConsumerWarps - 1;
-        if (!mbar_wait(bar_q, 0)) {
-            atomicOr(a.status, kErrTimeout);
-            return;   // consumers time out on the pos barriers
-        }
-        uint32_t qv[4][4];
-        make_qv_perm(sb + SP.off_q, s_vb, lane, qv);
-        const int n_bt = (K + 15 + 7) / 8;
-        const uint16_t* rel_h = rel + h * kHeadDim;
-        for (int s = pw; s < n_stages; s += kPosWarps) {
-            const int nb0 = 8 * s, nb1 = min(n_bt, 8 * s + 10);   // tiles stage s reads
-            pos_term_tiles(qv, rel_h, a.H, a.R, off - 15, nb0, 1, nb1, K, gs, gsw, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_pos + 8 * s);
-        }
-        return;
-    }
-
-    // ---- consumers
-    bool failed = !mbar_wait(bar_q, 0);
-    uint32_t qu[4][4];
-    WarpAcc acc;
-    acc_init(acc);
-    if (!failed) {
-        {
-            uint32_t unused[4][4];
-            make_q_frags(sb + SP.off_q, s_u, s_vb, 0, lane, qu, unused);
-        }
-        for (int s = warp; s < n_stages; s += kConsumerWarps) {
-            const int slot = s % ns;
-            if (!mbar_wait(bar_full + 8 * slot, (s / ns) & 1) || !mbar_wait(bar_pos + 8 * s, 0)) {
-                failed = true;
-                break;
-            }
-            const uint32_t base = sb + slot * 2 * kStageKeys * kRowBytes;
-            warp_stage_pre(acc, qu, base, base + kStageKeys * kRowBytes, gs, gsw,
-                           s * kStageKeys, min(kStageKeys, K - s * kStageKeys), a.scale_log2, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
-        }
-    }
-    if (failed) s_failed = 1;
-    named_bar_sync(1, 32 * kConsumerWarps);
-    if (s_failed) {
-        if (tid == 0) atomicOr(a.status, err | kErrTimeout);
-        return;
-    }
-    // partials of the 4 warps (each over its own stages) -> slots area
-    float* comb_o = reinterpret_cast<float*>(sm);
-    float* comb_m = comb_o + kConsumerWarps * 16 * kOW;
-    float* comb_l = comb_m + kConsumerWarps * 16;
-    acc_reduce_l(acc);
-    write_partial(acc, comb_o, comb_m, comb_l, warp * 16, lane);
-    named_bar_sync(1, 32 * kConsumerWarps);
-    for (int idx = tid; idx < T * 8; idx += 32 * kConsumerWarps) {
-        const int row = idx >> 3, d0 = (idx & 7) * 8;
-        const uint4 v = combine_row8(comb_o, comb_m, comb_l, kConsumerWarps, 16, row, d0);
         *reinterpret_cast<uint4*>(a.out + ((static_cast<long long>(b) * T + row) * a.H + h) *
                                               kHeadDim + d0) = v;
     }
@@ -633,65 +412,6 @@ oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, voi
     return launch_status();
 }
 
-int g_smem_done_pre[2][64];
-
-// Launch the T <= 16 kernel with as many K/V slots as fit next to the position tile
-// (two CTAs per SM when possible).  Returns OASR_ERR_UNSUPPORTED when the tile for the
-// block table's capacity does not fit at all.
-template <bool FUSED>
-oasr_status launch_pre(const void* q, const void* k_new, const void* v_new, void* k_pool,
-                       void* v_pool, int num_blocks, int block_size, const int32_t* bt, int mbps,
-                       const int32_t* cs, const void* u, const void* vb, const void* rel, int R,
-                       void* out, int B, int T, int H, float scale, cudaStream_t stream)
-{
-    const long long cap = static_cast<long long>(mbps) * block_size;
-    if (cap > kPreMaxStages * kStageKeys || (cap + block_size - 1) / block_size > kPreMaxPages)
-        return OASR_ERR_UNSUPPORTED;
-    const int gsw = pre_gsw(static_cast<int>(cap));
-    constexpr int kTwoPerSm = 113 * 1024;
-    constexpr int kOnePerSm = 226 * 1024;
-    int ns = kPreMaxSlots;
-    while (ns > 4 && PreSmem(ns, gsw).bytes > kTwoPerSm) --ns;
-    if (PreSmem(ns, gsw).bytes > kTwoPerSm) {
-        ns = kPreMaxSlots;
-        while (ns > 2 && PreSmem(ns, gsw).bytes > kOnePerSm) --ns;
-        if (PreSmem(ns, gsw).bytes > kOnePerSm) return OASR_ERR_UNSUPPORTED;
-    }
-    const int smem = PreSmem(ns, gsw).bytes;
-    CUtensorMap tm_q, tm_k, tm_v;
-    const int box = block_size < kStageKeys ? block_size : kStageKeys;
-    if (!encode_rows_bf16(&tm_q, q, static_cast<long long>(B) * T, H, 16) ||
-        !encode_rows_bf16(&tm_k, k_pool, static_cast<long long>(num_blocks) * block_size, H, box) ||
-        !encode_rows_bf16(&tm_v, v_pool, static_cast<long long>(num_blocks) * block_size, H, box))
-        return OASR_ERR_INVALID_ARG;
-    unsigned* status = status_word();
-    if (!status) return OASR_ERR_CUDA;
-    auto kern = chunk_attn_pre_kernel<FUSED>;
-    if (!ensure_smem(kern, smem, g_smem_done_pre[FUSED ? 1 : 0])) return OASR_ERR_CUDA;
-    ChunkArgs a;
-    a.k_new = static_cast<const uint16_t*>(k_new);
-    a.v_new = static_cast<const uint16_t*>(v_new);
-    a.k_pool = static_cast<uint16_t*>(k_pool);
-    a.v_pool = static_cast<uint16_t*>(v_pool);
-    a.block_table = bt;
-    a.cache_seqlens = cs;
-    a.pos_bias_u = static_cast<const uint16_t*>(u);
-    a.pos_bias_v = static_cast<const uint16_t*>(vb);
-    a.out = static_cast<uint16_t*>(out);
-    a.status = status;
-    a.num_blocks = num_blocks;
-    a.block_size = block_size;
-    a.mbps = mbps;
-    a.T = T;
-    a.H = H;
-    a.R = R;
-    a.box_rows = box;
-    a.scale_log2 = scale * 1.4426950408889634f;
-    kern<<<static_cast<unsigned>(B) * H, kPreThreads, smem, stream>>>(
-        tm_q, tm_k, tm_v, a, static_cast<const uint16_t*>(rel), ns, gsw);
-    return launch_status();
-}
-
 template <bool FUSED>
 oasr_status dispatch(const void* q, const void* k_new, const void* v_new, void* k_pool,
                      void* v_pool, int num_blocks, int block_size, const int32_t* bt, int mbps,
@@ -709,6 +429,7 @@ oasr_status dispatch(const void* q, const void* k_new, const void* v_new, void* 
     if (D != kHeadDim || T > 64) return OASR_ERR_UNSUPPORTED;
     if (block_size < 8 || block_size > 256 || (block_size & (block_size - 1)))
         return OASR_ERR_UNSUPPORTED;
+    if (dt == OASR_BF16 && mbps > kMaxPages) return OASR_ERR_UNSUPPORTED;
     if (static_cast<long long>(B) * H > 0x7fffffffLL) return OASR_ERR_UNSUPPORTED;
     const void* ptrs[] = {q, k_pool, v_pool, u, vb, rel, out, FUSED ? k_new : q,
                           FUSED ? v_new : q};
@@ -726,15 +447,10 @@ oasr_status dispatch(const void* q, const void* k_new, const void* v_new, void* 
         return launch_status();
     }
     const int f = FUSED ? 8 : 0;
-    if (T <= 16) {
-        const oasr_status st = launch_pre<FUSED>(q, k_new, v_new, k_pool, v_pool, num_blocks,
-                                                 block_size, bt, mbps, cs, u, vb, rel, R, out, B,
-                                                 T, H, scale, stream);
-        if (st != OASR_ERR_UNSUPPORTED) return st;
+    if (T <= 16)
         return launch_bf16<1, 4, FUSED>(q, k_new, v_new, k_pool, v_pool, num_blocks, block_size,
                                         bt, mbps, cs, u, vb, rel, R, out, B, T, H, scale, stream,
                                         f + 0);
-    }
     if (T <= 32)
         return launch_bf16<2, 3, FUSED>(q, k_new, v_new, k_pool, v_pool, num_blocks, block_size,
                                         bt, mbps, cs, u, vb, rel, R, out, B, T, H, scale, stream,

@@ -150,6 +150,9 @@ EDGE = [
     (2, 2, 32, 96, 16, 0, "bf16"),     # two m-tiles, full
     (2, 2, 33, 20, 16, 0, "bf16"),     # four m-tiles, ragged
     (2, 2, 64, 130, 16, 0, "bf16"),    # four m-tiles, full
+    (3, 1, 16, 100, 16, 0, "bf16"),    # one head per CTA
+    (2, 6, 9, 70, 32, 0, "bf16"),      # two heads per CTA
+    (2, 4, 16, 530, 32, 0, "bf16"),    # key range split in two, ragged
     (2, 2, 5, 77, 8, 2, "f32"),
     (2, 3, 40, 33, 16, 0, "f32"),
     (1, 1, 1, 0, 8, 0, "f32"),
