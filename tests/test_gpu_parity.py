@@ -303,3 +303,85 @@ def test_streaming_rows_equal_packed_rows_gpu():
               pos_bias_v=x["pos_bias_v"], rel=relp, max_seqlen=L)
     out_p = _run_packed(px, "bf16")
     check_close(to_np(out_s[0]), to_np(out_p[C:]), "bf16", "streaming vs packed")
+
+
+# ------------------------------------------- heterogeneous offsets, padding lane
+
+
+def _hetero_inputs(Cs, T, H, bs, seed, R):
+    """Streams with different cache lengths sharing one rel table of R rows."""
+    rng = np.random.default_rng(seed)
+    B = len(Cs)
+    cmax = max(Cs)
+    pages = -(-(cmax + T) // bs)
+    nb = 2 * B * pages
+    x = {
+        "q": syn.normal(rng, (B, T, H, 64), "bf16"),
+        "k_new": syn.normal(rng, (B, T, H, 64), "bf16"),
+        "v_new": syn.normal(rng, (B, T, H, 64), "bf16"),
+        "pos_bias_u": syn.normal(rng, (H, 64), "bf16"),
+        "pos_bias_v": syn.normal(rng, (H, 64), "bf16"),
+        "rel": syn.normal(rng, (R, H, 64), "bf16"),
+        "block_table": syn.block_table(rng, B, pages, nb),
+        "cache_seqlens": np.array(Cs, np.int32),
+        "caches": [(syn.normal(rng, (1, c, H, 64), "bf16"), syn.normal(rng, (1, c, H, 64), "bf16"))
+                   for c in Cs],
+    }
+    kp = syn.canary_pool(nb, bs, H, 64, "bf16")
+    vp = syn.canary_pool(nb, bs, H, 64, "bf16")
+    for b, (ck, cv) in enumerate(x["caches"]):
+        if Cs[b]:
+            oracle.paged_append(syn.to_bits(ck, "bf16"), syn.to_bits(cv, "bf16"), kp, vp,
+                                x["block_table"][b:b + 1], np.zeros(1, np.int32))
+    x["k_pool"], x["v_pool"] = kp, vp
+    return x
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
+def test_heterogeneous_cache_lengths_one_launch(fused):
+    """Streams at different offsets in one launch (Scheduler page, section 4.3): each reads
+    its own cache_seqlens and indexes the shared table at distance C_b + i - j."""
+    Cs, T, H, bs = [0, 17, 64, 130, 255, 3], 16, 4, 16
+    R = max(Cs) + 2 * T - 1 + 4
+    x = _hetero_inputs(Cs, T, H, bs, seed=123, R=R)
+    cfg = syn.StreamingConfig("het", B=len(Cs), H=H, D=64, T=T, C=max(Cs), block_size=bs,
+                              dtype="bf16", seed=0)
+    out, _ = _run_step(cfg, x, fused)
+    got = to_np(out)
+    for b, C in enumerate(Cs):
+        ck, cv = x["caches"][b]
+        ref = oracle.chunk_relattn(x["q"][b:b + 1], ck, cv, x["k_new"][b:b + 1],
+                                   x["v_new"][b:b + 1], x["pos_bias_u"], x["pos_bias_v"], x["rel"])
+        check_close(got[b:b + 1], ref, "bf16", f"stream {b} (C={C})")
+    assert capi.oasr_device_status() == 0
+
+
+def test_padding_lanes_share_a_scratch_block():
+    """Padding rows whose block tables point only at one scratch block outside the
+    streams' pages (ASR Engine page, section 9, padding lane) compute garbage only for
+    themselves: the real streams' rows and pages are exact."""
+    cfg = syn.StreamingConfig("pad", B=3, H=4, D=64, T=16, C=80, block_size=16, dtype="bf16",
+                              seed=77)
+    x = stream_case(cfg)
+    n_pad = 2
+    scratch = cfg.pool_blocks - 1
+    assert scratch not in x["block_table"]
+    bt = np.concatenate([x["block_table"], np.full((n_pad, cfg.mbps), scratch, np.int32)])
+    xp = dict(x)
+    for k in ("q", "k_new", "v_new"):
+        xp[k] = np.concatenate([x[k], np.zeros((n_pad,) + x[k].shape[1:], np.float32)])
+    xp["block_table"] = bt
+    xp["cache_seqlens"] = np.concatenate([x["cache_seqlens"], np.zeros(n_pad, np.int32)])
+    cfgp = syn.StreamingConfig("pad", B=cfg.B + n_pad, H=4, D=64, T=16, C=80, block_size=16,
+                               dtype="bf16", seed=77, num_blocks=cfg.pool_blocks,
+                               max_blocks_per_seq=cfg.mbps)
+    out, d = _run_step(cfgp, xp, fused=True)
+    check_close(to_np(out[: cfg.B]), oracle_chunk(x), "bf16", "real streams")
+    kp = host_pool(d["k_pool"], "bf16")
+    expect = x["k_pool"].copy()
+    oracle.paged_append(syn.to_bits(x["k_new"], "bf16"), syn.to_bits(x["v_new"], "bf16"), expect,
+                        x["v_pool"].copy(), x["block_table"], x["cache_seqlens"])
+    used = np.zeros(cfg.pool_blocks, bool)
+    used[x["block_table"].ravel()] = True
+    np.testing.assert_array_equal(kp[used], expect[used])
+    assert capi.oasr_device_status() == 0
