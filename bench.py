@@ -498,7 +498,7 @@ def run_packed(args, rank, world, local):
                    "l2": f"inputs larger than L2: {packed_bytes(total, x['rel'].shape[0], cfg.H, cfg.D) / 1e6:.0f} MB per call"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": None,
-                     "kernel": "packed_attn_bf16_kernel", "algorithmic_flops_per_launch": flops,
+                     "kernel": "packed_attn_tc_kernel", "algorithmic_flops_per_launch": flops,
                      "avg_launch_us": per_call_s * 1e6, "peak_kind": kind},
         "gpu_launches": args.steps, "clocks": clocks,
     }

@@ -1,0 +1,652 @@
+// Packed varlen bidirectional rel-pos attention on the 5th-generation tensor cores
+// (tcgen05 + TMEM), bf16.  Used by oasr_packed_relattn_varlen for bf16 inputs.
+//
+// ASR Engine page, section 4.1 (sequence packing: one gapless varlen row); Model Layer
+// page, engine-facing surface table (forward_offline_packed) and Nemotron ASR section
+// (Transformer-XL rel_shift).  Segment s owns rows [cu[s], cu[s+1]); query i and key j of
+// one segment score s_ij = scale * ((q_i+u).k_j + (q_i+v).rel[z - (i - j)]), z = (R-1)/2.
+//
+// Persistent CTAs (one per SM) walk work items (128-query tile of a segment, head).  For a
+// tile of 128 queries against a stage of 128 keys, in tensor memory (TMEM lane = query row):
+//   S [128 x 128] = bf16(q+u) . K^T     columns [0,128)    tcgen05.mma M128 N128, A and B in smem
+//   G [128 x 256] = bf16(q+v) . Band^T  columns [128,384)  M128 N256; the band is the 256 rel
+//                   rows z - i0 + j0 - 127 ... the tile reaches, and row i, key j uses band
+//                   row 127 - i + j
+//   O [128 x 64] += P . V               columns [384,448)  M128 N64, A = P from TMEM, B = V
+//                                                          as an MN-major smem operand
+//   P [128 x 128] bf16                  columns [448,512)
+// Warp roles (320 threads):
+//   warps 0-7  softmax.  Warps w and w+4 share TMEM lane quadrant w and the 32 query rows in
+//              it; warp w takes keys 0-63 of each stage, warp w+4 keys 64-127, and the pair
+//              swaps row maxima and sums through shared memory.  Each thread loads its S half
+//              row and, through a shared staging tile, its skewed half row of G; masks keys
+//              past the segment; keeps the running max (O is rescaled in TMEM only when the
+//              max grows by more than 2^8) and sum; writes its half row of bf16 P to TMEM; at
+//              the end of the tile normalises and stores its half of the O row.
+//   warp 8     MMA issuer (one thread): S and G of stage s+1 as soon as the softmax warps have
+//              read stage s's, then P.V of stage s.
+//   warp 9     TMA producer: K, band and V tiles into a two-slot ring.
+// Every wait is bounded; a wait that runs out raises the timeout bit and aborts the CTA's
+// remaining work, after which the CTA still drains its copies and tensor-core work and frees
+// its TMEM.
+#include "attn_core.cuh"
+#include "host_common.h"
+#include "ptx.cuh"
+
+namespace oasr {
+namespace {
+
+constexpr int kTcMaxSeqs = 1024;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kTcThreads = 32 * (kSoftmaxWarps + 2);
+constexpr int kMmaWarp = kSoftmaxWarps, kTmaWarp = kSoftmaxWarps + 1;
+constexpr int kBM = 128;                 // queries per tile
+constexpr int kBN = 128;                 // keys per stage
+constexpr int kBand = 256;               // band rows per stage
+constexpr int kTmemCols = 512;
+constexpr int kColS = 0, kColG = 128, kColO = 384, kColP = 448;
+constexpr int kStgW = 68;                // staging row stride (floats): conflict-free both ways
+constexpr int kStgWarpBytes = 32 * kStgW * 4;
+constexpr int kStgOverlay = 5;           // warps whose staging overlays the stage's K and band tiles
+
+struct TcSmem {
+    static constexpr int k_tile = kBN * kRowBytes;               // 16 KB
+    static constexpr int band_tile = kBand * kRowBytes;          // 32 KB
+    static constexpr int v_tile = kBN * kRowBytes;               // 16 KB
+    static constexpr int slot = k_tile + band_tile + v_tile;     // 64 KB: K | band | V
+    static constexpr int off_band = k_tile;
+    static constexpr int off_v = k_tile + band_tile;
+    static_assert(kStgOverlay * kStgWarpBytes <= k_tile + band_tile, "staging overlay");
+    static constexpr int off_slot = 0;                           // 2 slots
+    static constexpr int off_qu = 2 * slot;                      // 16 KB
+    static constexpr int off_qv = off_qu + kBM * kRowBytes;      // 16 KB
+    static constexpr int off_stg = off_qv + kBM * kRowBytes;     // dedicated staging
+    static constexpr int off_xm = off_stg + (kSoftmaxWarps - kStgOverlay) * kStgWarpBytes;
+    static constexpr int off_cu = off_xm + 2 * 2 * kBM * 4;      // [exchange parity][half][row]
+    static constexpr int off_tile = off_cu + (kTcMaxSeqs + 1) * 4;
+    static constexpr int off_misc = off_tile + (kTcMaxSeqs + 1) * 4;   // wsum[16], tmem, abort
+    static constexpr int off_bar = (off_misc + 128 + 7) & ~7;
+    static constexpr int n_bars = 2 + 2 + 7 + 4;
+    static constexpr int bytes = off_bar + n_bars * 8 + 1024;
+};
+
+struct TcArgs {
+    const uint16_t* q;
+    const int32_t* cu_seqlens;
+    const uint16_t* pos_bias_u;
+    const uint16_t* pos_bias_v;
+    uint16_t* out;
+    unsigned* status;
+    int num_seqs, total, H, z;
+    float scale_log2;
+};
+
+// --------------------------------------------------------------- tcgen05 helpers
+
+// Shared-memory matrix descriptor: 128-byte swizzle, version 1; SBO = stride between
+// 8-row groups (1024 B for 128-byte rows); LBO unused for these shapes.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr)
+{
+    return static_cast<uint64_t>((addr >> 4) & 0x3FFF) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M x N, B MN-major if b_mn.
+__host__ __device__ constexpr uint32_t idesc(int M, int N, int b_mn)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D (TMEM) [+]= A (smem) . B (smem)
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, int acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+
+// D (TMEM) [+]= A (TMEM) . B (smem)
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id, int acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b), "r"(id), "r"(acc));
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+#define OASR_TMEM_LD32(taddr, r)                                                                   \
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"  \
+                 "%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,"    \
+                 "%31}, [%32];"                                                                     \
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),          \
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),        \
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),    \
+                   "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),    \
+                   "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),    \
+                   "=r"(r[30]), "=r"(r[31])                                                         \
+                 : "r"(taddr))
+
+#define OASR_TMEM_ST32(taddr, r)                                                                   \
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"  \
+                 "%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,"    \
+                 "%30,%31,%32};" ::"r"(taddr),                                                     \
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),       \
+                 "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),   \
+                 "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]),            \
+                 "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]),            \
+                 "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])            \
+                 : "memory")
+
+#define OASR_TMEM_ST16(taddr, r)                                                                   \
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"  \
+                 "%11,%12,%13,%14,%15,%16};" ::"r"(taddr),                                         \
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),       \
+                 "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),   \
+                 "r"(r[14]), "r"(r[15])                                                            \
+                 : "memory")
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Bounded wait that also gives up as soon as another role has aborted the CTA.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        for (int k = 0; k < 32; ++k)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    const __grid_constant__ CUtensorMap tm_r, const TcArgs a)
+{
+    using SP = TcSmem;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sb = smem_addr(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    unsigned err = 0;
+    int* s_cu = reinterpret_cast<int*>(sm + SP::off_cu);
+    int* s_tile = reinterpret_cast<int*>(sm + SP::off_tile);
+    int* s_wsum = reinterpret_cast<int*>(sm + SP::off_misc);
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + SP::off_misc + 64);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SP::off_misc + 68);
+    const uint32_t bar_full = sb + SP::off_bar;        // [2] TMA stage landed
+    const uint32_t bar_empty = bar_full + 16;          // [2] stage slot free (after P.V)
+    const uint32_t bar_sg_full = bar_empty + 16;       // S and G in TMEM
+    const uint32_t bar_sg_free = bar_sg_full + 8;      // softmax warps have read S and G
+    const uint32_t bar_p_full = bar_sg_free + 8;       // P written to TMEM
+    const uint32_t bar_pv_done = bar_p_full + 8;       // P.V finished
+    const uint32_t bar_q_ready = bar_pv_done + 8;      // bf16(q+u), bf16(q+v) written
+    const uint32_t bar_q_free = bar_q_ready + 8;       // last S/G MMA of an item finished
+    const uint32_t bar_drain = bar_q_free + 8;         // everything the MMA issuer issued finished
+    const uint32_t bar_pair = bar_drain + 8;           // [4] softmax warp pair exchanged a value
+    const int ns = a.num_seqs;
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_empty + 8 * i, 1);
+        }
+        mbar_init(bar_sg_full, 1);
+        mbar_init(bar_sg_free, kSoftmaxWarps);
+        mbar_init(bar_p_full, kSoftmaxWarps);
+        mbar_init(bar_pv_done, 1);
+        mbar_init(bar_q_ready, kSoftmaxWarps);
+        mbar_init(bar_q_free, 1);
+        mbar_init(bar_drain, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(bar_pair + 8 * i, 64);
+        fence_mbar_init();
+        *s_abort = 0;
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(s_tmem)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    // segment starts and the exclusive prefix of per-segment 128-row tile counts
+    for (int i = tid; i <= ns; i += kTcThreads) {
+        int c = __ldg(a.cu_seqlens + i);
+        if (c < 0 || c > a.total) { err |= kErrBounds; c = c < 0 ? 0 : a.total; }
+        s_cu[i] = c;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    {
+        const int per = (ns + kTcThreads - 1) / kTcThreads;
+        int mine = 0;
+        for (int k = 0; k < per; ++k) {
+            const int s = tid * per + k;
+            if (s < ns) {
+                const int L = s_cu[s + 1] - s_cu[s];
+                if (L < 0) err |= kErrBounds;
+                mine += L > 0 ? (L + kBM - 1) / kBM : 0;
+            }
+        }
+        int incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) s_wsum[warp] = incl;
+        __syncthreads();
+        int base = incl - mine;
+        for (int w = 0; w < warp; ++w) base += s_wsum[w];
+        for (int k = 0; k < per; ++k) {
+            const int s = tid * per + k;
+            if (s < ns) {
+                s_tile[s] = base;
+                const int L = s_cu[s + 1] - s_cu[s];
+                base += L > 0 ? (L + kBM - 1) / kBM : 0;
+            }
+        }
+        if (tid == kTcThreads - 1) {
+            int t = 0;
+            for (int w = 0; w < kTcThreads / 32; ++w) t += s_wsum[w];
+            s_tile[ns] = t;
+        }
+        __syncthreads();
+    }
+    const long long n_items = static_cast<long long>(s_tile[ns]) * a.H;
+    auto decode = [&](long long item, int& start, int& L, int& i0, int& h) {
+        const int tile = static_cast<int>(item / a.H);
+        h = static_cast<int>(item - static_cast<long long>(tile) * a.H);
+        int lo = 0, hi = ns - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_tile[mid] <= tile) lo = mid; else hi = mid - 1;
+        }
+        start = s_cu[lo];
+        L = s_cu[lo + 1] - start;
+        i0 = (tile - s_tile[lo]) * kBM;
+    };
+
+    // Softmax warps take every wait together: a warp-wide vote keeps the warp converged for
+    // the .sync.aligned tensor-memory instructions even if one lane's wait runs out.
+    auto warp_wait = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, wait_or_abort(bar, parity, s_abort)) != 0;
+    };
+
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+            prefetch_tensormap(&tm_r);
+            const uint64_t pol = policy_evict_last();   // K/V tiles are re-read by every query tile
+            int g = 0;
+            bool ok = true;
+            for (long long item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+                int start, L, i0, h;
+                decode(item, start, L, i0, h);
+                const int n_st = (L + kBN - 1) / kBN;
+                for (int s = 0; s < n_st; ++s, ++g) {
+                    const int slot = g & 1;
+                    if (g >= 2 && !wait_or_abort(bar_empty + 8 * slot, ((g >> 1) - 1) & 1, s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t base = sb + SP::off_slot + slot * SP::slot;
+                    const uint32_t bar = bar_full + 8 * slot;
+                    mbar_arrive_expect_tx(bar, SP::slot);
+                    tma_load_3d_hint(base, &tm_k, bar, 0, h, start + s * kBN, pol);
+                    tma_load_3d(base + SP::off_band, &tm_r, bar, 0, h, a.z - i0 + s * kBN - (kBM - 1));
+                    tma_load_3d_hint(base + SP::off_v, &tm_v, bar, 0, h, start + s * kBN, pol);
+                }
+            }
+            // no copy may still be landing when the CTA exits
+            for (int u = g - 2; u < g; ++u)
+                if (u >= 0 && !mbar_wait(bar_full + 8 * (u & 1), (u >> 1) & 1)) *s_abort = 1;
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc(kBM, kBN, 0), id_g = idesc(kBM, kBand, 0),
+                               id_o = idesc(kBM, 64, 1);
+            int g = 0, it = 0, sg = 0, nq = 0, npv = 0;
+            auto issue_sg = [&](int slot) {
+                const uint32_t base = sb + SP::off_slot + slot * SP::slot;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    umma_ss(tmem + kColS, sdesc(sb + SP::off_qu + 32 * k), sdesc(base + 32 * k), id_s, k > 0);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    umma_ss(tmem + kColG, sdesc(sb + SP::off_qv + 32 * k),
+                            sdesc(base + SP::off_band + 32 * k), id_g, k > 0);
+                umma_commit(bar_sg_full);
+                ++sg;
+            };
+            bool ok = true;
+            for (long long item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+                int start, L, i0, h;
+                decode(item, start, L, i0, h);
+                const int n_st = (L + kBN - 1) / kBN;
+                // stage 0 needs this item's q tiles, its slot, and S/G read out
+                ok = wait_or_abort(bar_q_ready, it & 1, s_abort) &&
+                     wait_or_abort(bar_full + 8 * (g & 1), (g >> 1) & 1, s_abort) &&
+                     (sg == 0 || wait_or_abort(bar_sg_free, (sg - 1) & 1, s_abort));
+                if (!ok) break;
+                issue_sg(g & 1);
+                if (n_st == 1) { umma_commit(bar_q_free); ++nq; }
+                for (int s = 0; s < n_st; ++s) {
+                    const int gs = g + s;
+                    if (s + 1 < n_st) {
+                        // S/G of the next stage overlap this stage's softmax
+                        ok = wait_or_abort(bar_full + 8 * ((gs + 1) & 1), ((gs + 1) >> 1) & 1, s_abort) &&
+                             wait_or_abort(bar_sg_free, (sg - 1) & 1, s_abort);
+                        if (!ok) break;
+                        issue_sg((gs + 1) & 1);
+                        if (s + 2 == n_st) { umma_commit(bar_q_free); ++nq; }
+                    }
+                    ok = wait_or_abort(bar_p_full, gs & 1, s_abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t vbase = sb + SP::off_slot + (gs & 1) * SP::slot + SP::off_v;
+#pragma unroll
+                    for (int k = 0; k < kBN / 16; ++k)
+                        umma_ts(tmem + kColO, tmem + kColP + 8 * k, sdesc(vbase + 2048 * k), id_o,
+                                (s > 0 || k > 0) ? 1 : 0);
+                    umma_commit(bar_pv_done);
+                    umma_commit(bar_empty + 8 * (gs & 1));
+                    ++npv;
+                }
+                g += n_st;
+            }
+            // drain: every MMA issued has finished and every arrival it owes has landed
+            umma_commit(bar_drain);
+            bool drained = mbar_wait(bar_drain, 0);
+            if (nq > 0) drained = mbar_wait(bar_q_free, (nq - 1) & 1) && drained;
+            if (sg > 0) drained = mbar_wait(bar_sg_full, (sg - 1) & 1) && drained;
+            if (npv > 0) drained = mbar_wait(bar_pv_done, (npv - 1) & 1) && drained;
+            for (int u = npv - 2; u < npv; ++u)
+                if (u >= 0) drained = mbar_wait(bar_empty + 8 * (u & 1), (u >> 1) & 1) && drained;
+            if (!drained) *s_abort = 1;
+        }
+    } else if (warp < kSoftmaxWarps) {
+        // ----------------------------------------------------------------- softmax
+        const int quad = warp & 3, hf = warp >> 2;
+        const int r = 32 * quad + lane;         // query row within the tile == TMEM lane
+        const uint32_t tl = tmem + (static_cast<uint32_t>(32 * quad) << 16);
+        // The two warps of a quadrant swap one value per row through shared memory; the
+        // pair's mbarrier phase k completes when both have written exchange k.
+        float* xm = reinterpret_cast<float*>(sm + SP::off_xm);   // [exchange parity][half][row]
+        const uint32_t pbar = bar_pair + 8 * quad;
+        int nx = 0;
+        auto pair_swap = [&](float mine, float& theirs) {
+            float* buf = xm + (nx & 1) * (2 * kBM);
+            buf[hf * kBM + r] = mine;
+            mbar_arrive(pbar);
+            if (!warp_wait(pbar, nx & 1)) return false;
+            theirs = buf[(1 - hf) * kBM + r];
+            ++nx;
+            return true;
+        };
+        int g = 0, it = 0, sg = 0;
+        for (long long item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+            int start, L, i0, h;
+            decode(item, start, L, i0, h);
+            const int n_st = (L + kBN - 1) / kBN;
+            // bf16(q+u) and bf16(q+v): this thread's half row, once the previous item's S/G are done
+            if (it > 0 && !warp_wait(bar_q_free, (it - 1) & 1)) break;
+            {
+                const int qrow = start + i0 + r;
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    a.q + (static_cast<long long>(qrow < a.total ? qrow : 0) * a.H + h) * kHeadDim);
+                const uint4* up = reinterpret_cast<const uint4*>(a.pos_bias_u + h * kHeadDim);
+                const uint4* vp = reinterpret_cast<const uint4*>(a.pos_bias_v + h * kHeadDim);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int c = 4 * hf + cc;
+                    const uint4 qc = qrow < a.total ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 uc = __ldg(up + c), vc = __ldg(vp + c);
+                    const uint32_t w[4] = {qc.x, qc.y, qc.z, qc.w};
+                    const uint32_t wu[4] = {uc.x, uc.y, uc.z, uc.w};
+                    const uint32_t wv[4] = {vc.x, vc.y, vc.z, vc.w};
+                    uint32_t ou[4], ov[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+                        ou[e] = pack_bf16(lo + __uint_as_float(wu[e] << 16), hi + __uint_as_float(wu[e] & 0xffff0000u));
+                        ov[e] = pack_bf16(lo + __uint_as_float(wv[e] << 16), hi + __uint_as_float(wv[e] & 0xffff0000u));
+                    }
+                    const uint32_t offs = static_cast<uint32_t>(r * kRowBytes + ((c ^ (r & 7)) << 4));
+                    *reinterpret_cast<uint4*>(sm + SP::off_qu + offs) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+                    *reinterpret_cast<uint4*>(sm + SP::off_qv + offs) = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_q_ready);
+            }
+            float m_used = -INFINITY, l_sum = 0.f;
+            bool ok = true;
+            for (int s = 0; s < n_st; ++s, ++g) {
+                if (!warp_wait(bar_sg_full, sg & 1)) { ok = false; break; }
+                ++sg;
+                tc_fence_after();
+                uint8_t* slot_p = sm + SP::off_slot + (g & 1) * SP::slot;
+                float sc[64];
+                {
+                    uint32_t sr[64], rr[32];
+                    const uint32_t colg = kColG + static_cast<uint32_t>(96 - 32 * quad + 64 * hf);
+                    OASR_TMEM_LD32(tl + kColS + 64 * hf, sr);
+                    OASR_TMEM_LD32(tl + kColS + 64 * hf + 32, (sr + 32));
+                    OASR_TMEM_LD32(tl + colg, rr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) sc[j] = __uint_as_float(sr[j]);
+                    // position term, skewed: row r needs G[r][127 - r + j].  Per 32-key chunk a
+                    // warp's rows span 63 columns, staged through shared memory (the stage's K
+                    // and band tiles, free once S and G are computed, for the first warps).
+                    float* stg = (warp < kStgOverlay
+                                      ? reinterpret_cast<float*>(slot_p) + warp * (32 * kStgW)
+                                      : reinterpret_cast<float*>(sm + SP::off_stg) +
+                                            (warp - kStgOverlay) * (32 * kStgW)) +
+                                 lane * kStgW;
+                    // chunk c (keys 32c..32c+31 of this half) reads G columns
+                    // colg + 32c ... colg + 32c + 63, staged as two 32-column blocks
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        if (c == 1) {
+                            OASR_TMEM_LD32(tl + colg + 32, rr);
+                            tmem_wait_ld();
+                        }
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            *reinterpret_cast<uint4*>(stg + 4 * k) =
+                                make_uint4(rr[4 * k], rr[4 * k + 1], rr[4 * k + 2], rr[4 * k + 3]);
+                        OASR_TMEM_LD32(tl + colg + 32 * c + 32, rr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            *reinterpret_cast<uint4*>(stg + 32 + 4 * k) =
+                                make_uint4(rr[4 * k], rr[4 * k + 1], rr[4 * k + 2], rr[4 * k + 3]);
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) sc[32 * c + j] += stg[31 - lane + j];
+                        __syncwarp();
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_sg_free);
+                // scale (log2 domain), mask keys past the segment, this half's max
+                const int kv = L - s * kBN - 64 * hf;   // valid keys in this half
+                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+                if (kv >= 64) {
+#pragma unroll
+                    for (int j = 0; j < 64; j += 4) {
+                        sc[j] *= a.scale_log2; sc[j + 1] *= a.scale_log2;
+                        sc[j + 2] *= a.scale_log2; sc[j + 3] *= a.scale_log2;
+                        mx0 = fmaxf(mx0, sc[j]); mx1 = fmaxf(mx1, sc[j + 1]);
+                        mx2 = fmaxf(mx2, sc[j + 2]); mx3 = fmaxf(mx3, sc[j + 3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; j += 4) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sc[j + e] = j + e < kv ? sc[j + e] * a.scale_log2 : -INFINITY;
+                        mx0 = fmaxf(mx0, sc[j]); mx1 = fmaxf(mx1, sc[j + 1]);
+                        mx2 = fmaxf(mx2, sc[j + 2]); mx3 = fmaxf(mx3, sc[j + 3]);
+                    }
+                }
+                float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)), mx_other;
+                if (!pair_swap(mx, mx_other)) { ok = false; break; }
+                mx = fmaxf(mx, mx_other);
+                const bool rescale = mx > m_used + 8.f;   // keeps every P <= 2^8 between rescales
+                const float m_new = rescale ? mx : m_used;
+                // P.V of the previous stage must be done before P and O are touched
+                if (s > 0 && !warp_wait(bar_pv_done, (g - 1) & 1)) { ok = false; break; }
+                if (s > 0 && __any_sync(0xffffffffu, rescale)) {
+                    const float alpha = ex2_approx(m_used - m_new);
+                    l_sum *= alpha;
+                    tc_fence_after();
+                    uint32_t oo[32];
+                    OASR_TMEM_LD32(tl + kColO + 32 * hf, oo);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) oo[j] = __float_as_uint(__uint_as_float(oo[j]) * alpha);
+                    OASR_TMEM_ST32(tl + kColO + 32 * hf, oo);
+                }
+                m_used = m_new;
+                {
+                    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float p0 = ex2_approx(sc[32 * q2 + 2 * j] - m_used);
+                            const float p1 = ex2_approx(sc[32 * q2 + 2 * j + 1] - m_used);
+                            ps0 += p0;
+                            ps1 += p1;
+                            pk[j] = pack_bf16(p0, p1);
+                        }
+                        OASR_TMEM_ST16(tl + kColP + 32 * hf + 16 * q2, pk);
+                    }
+                    l_sum += ps0 + ps1;
+                }
+                // V rows past the segment belong to the next one: zero them so that P = 0
+                // there never meets a non-finite value
+                if (L - s * kBN < kBN) {
+                    if (!warp_wait(bar_full + 8 * (g & 1), (g >> 1) & 1)) { ok = false; break; }
+                    if (r >= L - s * kBN) {
+                        uint4* vrow = reinterpret_cast<uint4*>(slot_p + SP::off_v + r * kRowBytes) + 4 * hf;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) vrow[c] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_p_full);
+            }
+            if (!ok) break;
+            // O half row of this tile: wait for the last P.V, combine the pair's sums, store
+            if (!warp_wait(bar_pv_done, (g - 1) & 1)) break;
+            float l_other;
+            if (!pair_swap(l_sum, l_other)) break;
+            const float l_row = l_sum + l_other;
+            tc_fence_after();
+            uint32_t oo[32];
+            OASR_TMEM_LD32(tl + kColO + 32 * hf, oo);
+            tmem_wait_ld();
+            const int row = i0 + r;
+            if (row < L) {
+                const float inv = 1.f / l_row;
+                uint4* dst = reinterpret_cast<uint4*>(
+                                 a.out + (static_cast<long long>(start + row) * a.H + h) * kHeadDim) + 4 * hf;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    dst[c] = make_uint4(
+                        pack_bf16(__uint_as_float(oo[8 * c]) * inv, __uint_as_float(oo[8 * c + 1]) * inv),
+                        pack_bf16(__uint_as_float(oo[8 * c + 2]) * inv, __uint_as_float(oo[8 * c + 3]) * inv),
+                        pack_bf16(__uint_as_float(oo[8 * c + 4]) * inv, __uint_as_float(oo[8 * c + 5]) * inv),
+                        pack_bf16(__uint_as_float(oo[8 * c + 6]) * inv, __uint_as_float(oo[8 * c + 7]) * inv));
+            }
+            tc_fence_before();
+        }
+    }
+    // every role has stopped issuing and the MMA issuer has drained the tensor pipe
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+    if (tid == 0 && *s_abort) err |= kErrTimeout;
+    if (err) atomicOr(a.status, err);
+}
+
+int g_smem_done_tc[64];
+
+}  // namespace
+
+// Host launcher used by oasr_packed_relattn_varlen (bf16).
+oasr_status launch_packed_tc(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                             int num_seqs, int total, const void* pos_bias_u,
+                             const void* pos_bias_v, const void* rel, int R, void* out, int H,
+                             float scale, cudaStream_t stream)
+{
+    if (num_seqs > kTcMaxSeqs) return OASR_ERR_UNSUPPORTED;
+    CUtensorMap tm_k, tm_v, tm_r;
+    if (!encode_rows_bf16(&tm_k, k, total, H, kBN) || !encode_rows_bf16(&tm_v, v, total, H, kBN) ||
+        !encode_rows_bf16(&tm_r, rel, R, H, kBand))
+        return OASR_ERR_INVALID_ARG;
+    unsigned* status = status_word();
+    const int sms = sm_count();
+    if (!status || !sms) return OASR_ERR_CUDA;
+    constexpr int smem = TcSmem::bytes;
+    if (!ensure_smem(packed_attn_tc_kernel, smem, g_smem_done_tc)) return OASR_ERR_CUDA;
+    TcArgs a;
+    a.q = static_cast<const uint16_t*>(q);
+    a.cu_seqlens = cu_seqlens;
+    a.pos_bias_u = static_cast<const uint16_t*>(pos_bias_u);
+    a.pos_bias_v = static_cast<const uint16_t*>(pos_bias_v);
+    a.out = static_cast<uint16_t*>(out);
+    a.status = status;
+    a.num_seqs = num_seqs;
+    a.total = total;
+    a.H = H;
+    a.z = (R - 1) / 2;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    const long long items_bound = ((static_cast<long long>(total) + kBM - 1) / kBM + num_seqs) * H;
+    const int grid = static_cast<int>(items_bound < sms ? items_bound : sms);
+    packed_attn_tc_kernel<<<grid, kTcThreads, smem, stream>>>(tm_k, tm_v, tm_r, a);
+    return launch_status();
+}
+
+}  // namespace oasr

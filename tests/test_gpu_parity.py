@@ -234,6 +234,7 @@ def _oracle_packed(x, rows=None):
 
 @pytest.mark.parametrize("lengths", [
     [1], [64], [65], [7, 0, 130, 1, 64, 200, 3], [300, 299, 1, 0, 0, 150],
+    [128], [129], [256, 255, 257, 127],
 ], ids=str)
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_packed_full(lengths, dtype):
