@@ -78,8 +78,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     using TL = Tile<MT>;
     using SP = ChunkSmem<MT, NS>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned base, derived from the __shared__ array itself so that every access
+    // through it stays a shared-space access
+    uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_addr(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.x / a.H, h = blockIdx.x - (blockIdx.x / a.H) * a.H;

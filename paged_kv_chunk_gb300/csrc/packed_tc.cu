@@ -189,8 +189,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
 {
     using SP = TcSmem;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned base, derived from the __shared__ array itself so that every access
+    // through it stays a shared-space access
+    uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_addr(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     unsigned err = 0;
@@ -405,12 +406,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
         float* xm = reinterpret_cast<float*>(sm + SP::off_xm);   // [exchange parity][half][row]
         const uint32_t pbar = bar_pair + 8 * quad;
         int nx = 0;
-        auto pair_swap = [&](float mine, float& theirs) {
-            float* buf = xm + (nx & 1) * (2 * kBM);
-            buf[hf * kBM + r] = mine;
+        auto pair_post = [&](float mine) {
+            xm[(nx & 1) * (2 * kBM) + hf * kBM + r] = mine;
             mbar_arrive(pbar);
+        };
+        auto pair_collect = [&](float& theirs) {
             if (!warp_wait(pbar, nx & 1)) return false;
-            theirs = buf[(1 - hf) * kBM + r];
+            theirs = xm[(nx & 1) * (2 * kBM) + (1 - hf) * kBM + r];
             ++nx;
             return true;
         };
@@ -470,11 +472,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     // position term, skewed: row r needs G[r][127 - r + j].  Per 32-key chunk a
                     // warp's rows span 63 columns, staged through shared memory (the stage's K
                     // and band tiles, free once S and G are computed, for the first warps).
-                    float* stg = (warp < kStgOverlay
-                                      ? reinterpret_cast<float*>(slot_p) + warp * (32 * kStgW)
-                                      : reinterpret_cast<float*>(sm + SP::off_stg) +
-                                            (warp - kStgOverlay) * (32 * kStgW)) +
-                                 lane * kStgW;
+                    float* stg = reinterpret_cast<float*>(
+                        (warp < kStgOverlay ? slot_p + warp * (32 * kStgW * 4)
+                                            : sm + SP::off_stg + (warp - kStgOverlay) * (32 * kStgW * 4)) +
+                        lane * (kStgW * 4));
                     // chunk c (keys 32c..32c+31 of this half) reads G columns
                     // colg + 32c ... colg + 32c + 63, staged as two 32-column blocks
 #pragma unroll
@@ -523,12 +524,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     }
                 }
                 float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)), mx_other;
-                if (!pair_swap(mx, mx_other)) { ok = false; break; }
+                pair_post(mx);
+                // P.V of the previous stage must be done before P and O are touched
+                if (s > 0 && !warp_wait(bar_pv_done, (g - 1) & 1)) { ok = false; break; }
+                if (!pair_collect(mx_other)) { ok = false; break; }
                 mx = fmaxf(mx, mx_other);
                 const bool rescale = mx > m_used + 8.f;   // keeps every P <= 2^8 between rescales
                 const float m_new = rescale ? mx : m_used;
-                // P.V of the previous stage must be done before P and O are touched
-                if (s > 0 && !warp_wait(bar_pv_done, (g - 1) & 1)) { ok = false; break; }
                 if (s > 0 && __any_sync(0xffffffffu, rescale)) {
                     const float alpha = ex2_approx(m_used - m_new);
                     l_sum *= alpha;
@@ -578,7 +580,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             // O half row of this tile: wait for the last P.V, combine the pair's sums, store
             if (!warp_wait(bar_pv_done, (g - 1) & 1)) break;
             float l_other;
-            if (!pair_swap(l_sum, l_other)) break;
+            pair_post(l_sum);
+            if (!pair_collect(l_other)) break;
             const float l_row = l_sum + l_other;
             tc_fence_after();
             uint32_t oo[32];
@@ -631,6 +634,11 @@ oasr_status launch_packed_tc(const void* q, const void* k, const void* v, const 
     if (!status || !sms) return OASR_ERR_CUDA;
     constexpr int smem = TcSmem::bytes;
     if (!ensure_smem(packed_attn_tc_kernel, smem, g_smem_done_tc)) return OASR_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, packed_attn_tc_kernel, kTcThreads, smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+        return OASR_ERR_CUDA;
     TcArgs a;
     a.q = static_cast<const uint16_t*>(q);
     a.cu_seqlens = cu_seqlens;
