@@ -48,6 +48,7 @@ UNIT = "frames/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["chunk_attn.cu", "attn_core.cuh", "ptx.cuh"]
+PACKED_SOURCES = ["packed_tc.cu", "attn_core.cuh", "ptx.cuh"]
 
 
 def parse_args():
@@ -119,24 +120,24 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_digest():
+def source_digest(sources=None):
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in (sources or KERNEL_SOURCES):
         with open(os.path.join(ROOT, "paged_kv_chunk_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(cfg_name):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"chunk_step_{cfg_name}.md")
+def profiled_traffic(profile_name, sources=None):
+    """DRAM bytes per launch from the committed ncu summary profiles/<profile_name>.md, if it
+    was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{profile_name}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
     m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not (m_sha and m_tr) or m_sha.group(1) != source_digest():
+    if not (m_sha and m_tr) or m_sha.group(1) != source_digest(sources):
         return None
     return float(m_tr.group(1))
 
@@ -411,7 +412,7 @@ def run_ours(args, cfg, rank, world, local):
         return
     peak, peak_kind = measured_hbm_peak()
     achieved = touched / (launch_us * 1e-6) / 1e9
-    traffic = None if args.two_call else profiled_traffic(cfg.name)
+    traffic = None if args.two_call else profiled_traffic(f"chunk_step_{cfg.name}")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
@@ -497,7 +498,7 @@ def run_packed(args, rank, world, local):
                    "H": cfg.H, "D": cfg.D, "rel_rows": int(x["rel"].shape[0]),
                    "l2": f"inputs larger than L2: {packed_bytes(total, x['rel'].shape[0], cfg.H, cfg.D) / 1e6:.0f} MB per call"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": profiled_traffic("packed_varlen", PACKED_SOURCES),
                      "kernel": "packed_attn_tc_kernel", "algorithmic_flops_per_launch": flops,
                      "avg_launch_us": per_call_s * 1e6, "peak_kind": kind},
         "gpu_launches": args.steps, "clocks": clocks,
