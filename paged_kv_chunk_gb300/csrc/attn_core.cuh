@@ -6,7 +6,8 @@
 // slots with TMA, completing a `full` mbarrier per slot; consumers release a slot by
 // arriving on its `empty` mbarrier.  Consumer warp w owns m-tile (w % MT) of the CTA's
 // Tp = 16*MT query rows and the stages s with s % KG == w / MT (KG = 4/MT), so each warp
-// works on whole stages:
+// works on whole stages (warp_stage); with one m-tile the four warps instead split every
+// stage into 16-key slices (warp_slice16).  Per unit of work:
 //
 //   S  = bf16(q+u) . K^T                       mma.sync m16n8k16, fp32 accumulators
 //   G  = bf16(q+v) . Rband^T                   80 band columns for the 64 keys
@@ -210,6 +211,128 @@ __device__ __forceinline__ void warp_stage(WarpAcc& acc, const uint32_t (&qu)[4]
             mma_bf16_16816(acc.o[2 * dp], pa, b0, b1);
             mma_bf16_16816(acc.o[2 * dp + 1], pa, b2, b3);
         }
+    }
+}
+
+// One warp, 16 query rows, one 16-key slice of a stage (the four consumer warps of a
+// one-m-tile CTA split every stage this way, so a stage is consumed in a quarter of the
+// latency).  k_s, v_s: shared addresses of the slice's first K and V rows; band_s: the
+// slice's first band row (32 band rows: element (i, j) of the slice uses band row
+// j + 15 - i); g: 16 x 32 floats of skew scratch, which may alias the slice's K rows (they
+// are dead once S is formed); kvalid: keys [0, kvalid) of the slice exist (kvalid > 0).
+// Scratch column c of row r is stored at c ^ (8 * (r & 3)): the fragment stores are
+// conflict-free, the skewed reads at most 2-way.
+__device__ __forceinline__ void warp_slice16(WarpAcc& acc, const uint32_t (&qu)[4][4],
+                                             const uint32_t (&qv)[4][4], uint32_t k_s, uint32_t v_s,
+                                             uint32_t band_s, float* g, int kvalid, float scale_log2,
+                                             int lane)
+{
+    const int g4 = lane >> 2, t4 = lane & 3, mi = lane >> 3;
+    float s[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(k_s + swz128(((mi >> 1) << 3) + (lane & 7), 2 * ks + (mi & 1)), b0, b1, b2, b3);
+        mma_bf16_16816(s[0], qu[ks], b0, b1);
+        mma_bf16_16816(s[1], qu[ks], b2, b3);
+    }
+    {
+        float gacc[4][4];
+#pragma unroll
+        for (int nb = 0; nb < 4; ++nb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) gacc[nb][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+            for (int np = 0; np < 2; ++np) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(band_s + swz128(16 * np + ((mi >> 1) << 3) + (lane & 7), 2 * ks + (mi & 1)),
+                        b0, b1, b2, b3);
+                mma_bf16_16816(gacc[2 * np], qv[ks], b0, b1);
+                mma_bf16_16816(gacc[2 * np + 1], qv[ks], b2, b3);
+            }
+        }
+        __syncwarp();   // every lane's K reads are done before the scratch (aliasing them) is written
+        const int sw0 = 8 * (g4 & 3);   // rows g4 and g4 + 8 share the swizzle
+#pragma unroll
+        for (int nb = 0; nb < 4; ++nb) {
+            *reinterpret_cast<float2*>(g + g4 * 32 + ((8 * nb + 2 * t4) ^ sw0)) =
+                make_float2(gacc[nb][0], gacc[nb][1]);
+            *reinterpret_cast<float2*>(g + (g4 + 8) * 32 + ((8 * nb + 2 * t4) ^ sw0)) =
+                make_float2(gacc[nb][2], gacc[nb][3]);
+        }
+    }
+    __syncwarp();
+    const int sw0 = 8 * (g4 & 3);
+    float mx0 = acc.m[0], mx1 = acc.m[1];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int j = 8 * nt + 2 * t4 + e;
+            const bool ok = j < kvalid;
+            const float b0 = g[g4 * 32 + ((j + 15 - g4) ^ sw0)];
+            const float b1 = g[(g4 + 8) * 32 + ((j + 7 - g4) ^ sw0)];
+            s[nt][e] = ok ? (s[nt][e] + b0) * scale_log2 : -INFINITY;
+            s[nt][2 + e] = ok ? (s[nt][2 + e] + b1) * scale_log2 : -INFINITY;
+        }
+        mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+        mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float base0 = (mx0 == -INFINITY) ? 0.f : mx0;
+    const float base1 = (mx1 == -INFINITY) ? 0.f : mx1;
+    if (mx0 != acc.m[0] || mx1 != acc.m[1]) {
+        const float alpha0 = exp2f(acc.m[0] - base0);
+        const float alpha1 = exp2f(acc.m[1] - base1);
+        acc.l[0] *= alpha0;
+        acc.l[1] *= alpha1;
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt) {
+            acc.o[dt][0] *= alpha0;
+            acc.o[dt][1] *= alpha0;
+            acc.o[dt][2] *= alpha1;
+            acc.o[dt][3] *= alpha1;
+        }
+        acc.m[0] = mx0;
+        acc.m[1] = mx1;
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        s[nt][0] = exp2f(s[nt][0] - base0);
+        s[nt][1] = exp2f(s[nt][1] - base0);
+        s[nt][2] = exp2f(s[nt][2] - base1);
+        s[nt][3] = exp2f(s[nt][3] - base1);
+        acc.l[0] += s[nt][0] + s[nt][1];
+        acc.l[1] += s[nt][2] + s[nt][3];
+    }
+    const uint32_t pa[4] = {pack_bf16(s[0][0], s[0][1]), pack_bf16(s[0][2], s[0][3]),
+                            pack_bf16(s[1][0], s[1][1]), pack_bf16(s[1][2], s[1][3])};
+    const int row = ((mi & 1) << 3) + (lane & 7);
+    const int k0 = 2 * t4;   // keys of this lane's B fragments: b0,b2 -> 2t(+1), b1,b3 -> 8+2t(+1)
+    const bool tail = kvalid < 16;
+    const uint32_t m0 = (k0 < kvalid ? 0xffffu : 0u) | (k0 + 1 < kvalid ? 0xffff0000u : 0u);
+    const uint32_t m1 = (k0 + 8 < kvalid ? 0xffffu : 0u) | (k0 + 9 < kvalid ? 0xffff0000u : 0u);
+#pragma unroll
+    for (int dp = 0; dp < 4; ++dp) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(v_s + swz128(row, 2 * dp + (mi >> 1)), b0, b1, b2, b3);
+        if (tail) {   // V rows past the last key may hold anything (0 * NaN is NaN)
+            b0 &= m0;
+            b2 &= m0;
+            b1 &= m1;
+            b3 &= m1;
+        }
+        mma_bf16_16816(acc.o[2 * dp], pa, b0, b1);
+        mma_bf16_16816(acc.o[2 * dp + 1], pa, b2, b3);
     }
 }
 

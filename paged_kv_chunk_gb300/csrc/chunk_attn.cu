@@ -8,13 +8,18 @@
 // one table serves the cohort, distances cache + i - j; Nemotron ASR section: rel_shift
 // order, so the row for query i and key j is rho = (R - T - C) + j - i.
 //
-// bf16 path (the hot path): one CTA per (stream, head), 4 warps.  Keys are streamed in
-// stages of 64 through a TMA pipeline: each stage is one box per block-table page for K
-// and for V (the page's rows of this head, 128 B each, 128-byte swizzled) plus one box of
-// the rel band; all arrive on one mbarrier.  The per-stage math is in attn_core.cuh.
-// The fused variant first writes this head's slice of the chunk into the pool with
-// 16-byte stores, fences them against the async proxy, and only then issues the stages
-// that cover the chunk; stages that hold only cached keys are issued before the writes.
+// bf16 path (the hot path): one CTA per (stream, head), 4 consumer warps and a TMA
+// producer warp.  Keys are streamed in stages of 64 through a TMA pipeline: each stage is
+// one box per block-table page for K and for V (the page's rows of this head, 128 B each,
+// 128-byte swizzled) plus one box of the rel band; all arrive on one mbarrier.  The
+// per-stage math is in attn_core.cuh.
+// Fused variant (append + attention): when every page the chunk lands in is a valid block
+// of the table, stage 0 is the chunk itself, read by TMA straight from k_new / v_new, and
+// the pool stages cover only the cached keys [0, C); the consumers write the chunk into
+// the pool meanwhile, a side effect no stage of this launch reads.  Otherwise (a chunk past
+// the table or in an invalid block) the stages cover [0, C + T) from the pool and those
+// holding the chunk are issued only after the consumers' 16-byte stores of it are fenced
+// against the async proxy, so the error handling of the append applies unchanged.
 //
 // f32 path: a SIMT kernel (one warp per query row, lanes over keys, fp32 FMA and expf).
 #include "attn_core.cuh"
@@ -59,8 +64,8 @@ struct ChunkSmem {
     static constexpr int off_u = off_g + (kGInBand ? 0 : kConsumerWarps * kGBytes);
     static constexpr int off_vb = off_u + kHeadDim * 4;
     static constexpr int off_bt = off_vb + kHeadDim * 4;    // the stream's block-table row
-    static constexpr int off_bar = off_bt + kMaxPages * 4;  // full[NS], empty[NS], q
-    static constexpr int bytes = off_bar + (2 * NS + 1) * 8 + 1024;
+    static constexpr int off_bar = off_bt + kMaxPages * 4;  // full[NS], empty[NS], q, written
+    static constexpr int bytes = off_bar + (2 * NS + 2) * 8 + 1024;
     static constexpr int comb_o = 0;
     static constexpr int comb_m = comb_o + TL::KG * TL::Tp * kOW * 4;
     static constexpr int comb_l = comb_m + TL::KG * TL::Tp * 4;
@@ -73,6 +78,7 @@ template <int MT, int NS, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
+    const __grid_constant__ CUtensorMap tm_kn, const __grid_constant__ CUtensorMap tm_vn,
     const ChunkArgs a)
 {
     using TL = Tile<MT>;
@@ -92,11 +98,11 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     int K = C + T;
     const int cap = a.mbps * a.block_size;
     if (K > cap) { K = cap; err |= kErrBounds; }
-    const int n_stages = (K + kStageKeys - 1) / kStageKeys;
     const int off = a.R - T - C;   // rho = off + j - i
     const uint32_t bar_full = sb + SP::off_bar;
     const uint32_t bar_empty = bar_full + NS * 8;
     const uint32_t bar_q = bar_empty + NS * 8;
+    const uint32_t bar_written = bar_q + 8;   // fused: the chunk is in the pool and fenced
     float* s_u = reinterpret_cast<float*>(sm + SP::off_u);
     float* s_vb = reinterpret_cast<float*>(sm + SP::off_vb);
     __shared__ int s_failed;
@@ -105,9 +111,11 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     if (tid == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(bar_full + 8 * i, 1);
-            mbar_init(bar_empty + 8 * i, MT);
+            // one m-tile: all consumer warps read every stage (16-key slices)
+            mbar_init(bar_empty + 8 * i, MT == 1 ? kConsumerWarps : MT);
         }
         mbar_init(bar_q, 1);
+        mbar_init(bar_written, 32 * kConsumerWarps);
         fence_mbar_init();
         s_failed = 0;
     }
@@ -116,18 +124,49 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         s_bt[i] = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + i);
     __syncthreads();
 
+    // Stage plan (every thread derives the same one from the cached table row).
+    bool direct = false;
+    if (FUSED && C + T <= cap) {
+        direct = true;
+        for (int pg = C / a.block_size; pg <= (C + T - 1) / a.block_size; ++pg) {
+            const int blk = s_bt[pg];
+            if (blk < 0 || blk >= a.num_blocks) direct = false;
+        }
+    }
+    const int kc = direct ? C : K;                        // keys served from the pool
+    const int n_pool = (kc + kStageKeys - 1) / kStageKeys;
+    const int n_stages = n_pool + (direct ? 1 : 0);
+    // stage s: first key and number of valid keys
+    auto stage_j0 = [&](int s) { return direct ? (s == 0 ? C : kStageKeys * (s - 1)) : kStageKeys * s; };
+    auto stage_valid = [&](int s) {
+        if (direct && s == 0) return T;
+        const int left = kc - stage_j0(s);
+        return left < kStageKeys ? left : kStageKeys;
+    };
+
     // Stage s into slot s % NS (producer lane only).
     auto issue = [&](int s) {
         const int slot = s % NS;
         const uint32_t bar = bar_full + 8 * slot;
         const uint32_t base = sb + SP::off_slots + slot * SP::kSlot;
-        const int j0 = s * kStageKeys;
+        const int j0 = stage_j0(s);
+        if (direct && s == 0) {
+            // the chunk's own rows: boxes of 16 rows of k_new / v_new (rows past T are masked)
+            const int nb = (T + 15) / 16;
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>((2 * nb * 16 + TL::RB) * kRowBytes));
+            for (int q = 0; q < nb; ++q) {
+                tma_load_3d(base + q * 16 * kRowBytes, &tm_kn, bar, 0, h, b * T + 16 * q);
+                tma_load_3d(base + (kStageKeys + 16 * q) * kRowBytes, &tm_vn, bar, 0, h, b * T + 16 * q);
+            }
+            tma_load_3d(base + 2 * kStageKeys * kRowBytes, &tm_r, bar, 0, h, off + j0 - (TL::Tp - 1));
+            return;
+        }
         const int box = a.box_rows;
         int rows[kStageKeys / 8];
         int nbox = 0;
         for (int q = 0; q < kStageKeys / box; ++q) {
             const int j = j0 + q * box;
-            if (j >= K) break;
+            if (j >= kc) break;
             const int lb = j / a.block_size;
             const int slot_in_block = j - lb * a.block_size;
             const int blk = s_bt[lb];
@@ -149,51 +188,28 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
                     off + j0 - (TL::Tp - 1));
     };
 
-    const int pre = n_stages < NS ? n_stages : NS;
-    const int first_chunk_stage = FUSED ? C / kStageKeys : n_stages;
-    int issued = 0;
     const bool producer = warp == kConsumerWarps;
-    if (producer && lane == 0) {
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
-        prefetch_tensormap(&tm_r);
-        mbar_arrive_expect_tx(bar_q, TL::Tp * kRowBytes);
-        tma_load_3d(sb + SP::off_q, &tm_q, bar_q, 0, h, b * T);
-        for (; issued < pre && issued < first_chunk_stage; ++issued) issue(issued);
-    }
-    if (tid < kHeadDim)
-        s_u[tid] = bf16_lo(__ldg(a.pos_bias_u + h * kHeadDim + tid));
-    else if (tid < 2 * kHeadDim)
-        s_vb[tid - kHeadDim] = bf16_lo(__ldg(a.pos_bias_v + h * kHeadDim + tid - kHeadDim));
-    if constexpr (FUSED) {
-        // This head's slice of the chunk: T rows x 8 vectors of 16 B, for K and for V.
-        for (int idx = tid; idx < 2 * T * 8; idx += kThreads) {
-            const int kv = idx >= T * 8;
-            const int rem = idx - kv * T * 8;
-            const int t = rem >> 3, c = rem & 7;
-            const int p = C + t;
-            const int lb = p / a.block_size;
-            if (lb >= a.mbps) { err |= kErrBounds; continue; }
-            const int slot = p - lb * a.block_size;
-            const int blk = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + lb);
-            if (blk < 0 || blk >= a.num_blocks) { err |= kErrBounds; continue; }
-            const uint16_t* src = (kv ? a.v_new : a.k_new) +
-                                  ((static_cast<long long>(b) * T + t) * a.H + h) * kHeadDim + c * 8;
-            uint16_t* dst = (kv ? a.v_pool : a.k_pool) +
-                            ((static_cast<long long>(blk) * a.block_size + slot) * a.H + h) * kHeadDim +
-                            c * 8;
-            *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
-        }
-        fence_proxy_async_global();
-    }
-    __syncthreads();
-
     if (producer) {
+        // The producer warp only issues copies: no other work shares its warp.
         if (lane == 0) {
-            for (; issued < n_stages; ++issued) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+            prefetch_tensormap(&tm_r);
+            if (direct) {
+                prefetch_tensormap(&tm_kn);
+                prefetch_tensormap(&tm_vn);
+            }
+            mbar_arrive_expect_tx(bar_q, TL::Tp * kRowBytes);
+            tma_load_3d(sb + SP::off_q, &tm_q, bar_q, 0, h, b * T);
+            // without the direct chunk stage, stages from this one on hold chunk rows
+            const int first_chunk_stage = (FUSED && !direct) ? C / kStageKeys : n_stages;
+            for (int issued = 0; issued < n_stages; ++issued) {
                 const int slot = issued % NS;
-                if (issued >= NS &&
-                    !mbar_wait(bar_empty + 8 * slot, ((issued / NS) - 1) & 1)) {
+                if (issued >= NS && !mbar_wait(bar_empty + 8 * slot, ((issued / NS) - 1) & 1)) {
+                    err |= kErrTimeout;
+                    break;
+                }
+                if (issued == first_chunk_stage && !mbar_wait(bar_written, 0)) {
                     err |= kErrTimeout;
                     break;
                 }
@@ -204,6 +220,35 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         return;
     }
 
+    // ---- consumers: u, v; the chunk into the pool (fused); then the stages
+    if (tid < kHeadDim)
+        s_u[tid] = bf16_lo(__ldg(a.pos_bias_u + h * kHeadDim + tid));
+    else
+        s_vb[tid - kHeadDim] = bf16_lo(__ldg(a.pos_bias_v + h * kHeadDim + tid - kHeadDim));
+    if constexpr (FUSED) {
+        // This head's slice of the chunk: T rows x 8 vectors of 16 B, for K and for V.
+        for (int idx = tid; idx < 2 * T * 8; idx += 32 * kConsumerWarps) {
+            const int kv = idx >= T * 8;
+            const int rem = idx - kv * T * 8;
+            const int t = rem >> 3, c = rem & 7;
+            const int p = C + t;
+            const int lb = p / a.block_size;
+            if (lb >= a.mbps || p >= K) { err |= kErrBounds; continue; }
+            const int slot = p - lb * a.block_size;
+            const int blk = s_bt[lb];
+            if (blk < 0 || blk >= a.num_blocks) { err |= kErrBounds; continue; }
+            const uint16_t* src = (kv ? a.v_new : a.k_new) +
+                                  ((static_cast<long long>(b) * T + t) * a.H + h) * kHeadDim + c * 8;
+            uint16_t* dst = (kv ? a.v_pool : a.k_pool) +
+                            ((static_cast<long long>(blk) * a.block_size + slot) * a.H + h) * kHeadDim +
+                            c * 8;
+            *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
+        }
+        fence_proxy_async_global();
+        mbar_arrive(bar_written);
+    }
+    named_bar_sync(1, 32 * kConsumerWarps);
+
     // ---- consumers
     const int mt = warp % MT, kg = warp / MT;
     bool failed = !mbar_wait(bar_q, 0);
@@ -213,6 +258,26 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     if (!failed) {
         make_q_frags(sb + SP::off_q, s_u, s_vb, mt, lane, qu, qv);
         float* gw = reinterpret_cast<float*>(sm + SP::off_g) + warp * (kGBytes / 4);
+        if constexpr (MT == 1) {
+            // every stage: this warp's 16-key slice; its skew scratch overlays its K rows
+            for (int s = 0; s < n_stages; ++s) {
+                const int slot = s % NS;
+                if (!mbar_wait(bar_full + 8 * slot, (s / NS) & 1)) { failed = true; break; }
+                const uint32_t base = sb + SP::off_slots + slot * SP::kSlot;
+                const int kv = stage_valid(s) - 16 * warp;
+                if (kv > 0) {
+                    warp_slice16(acc, qu, qv, base + 16 * warp * kRowBytes,
+                                 base + (kStageKeys + 16 * warp) * kRowBytes,
+                                 base + (2 * kStageKeys + 16 * warp) * kRowBytes,
+                                 reinterpret_cast<float*>(sm + SP::off_slots + slot * SP::kSlot +
+                                                          16 * warp * kRowBytes),
+                                 kv, a.scale_log2, lane);
+                    fence_proxy_async_smem();   // the next TMA into this slot
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+            }
+        } else
         for (int s = kg; s < n_stages; s += TL::KG) {
             const int slot = s % NS;
             if (!mbar_wait(bar_full + 8 * slot, (s / NS) & 1)) { failed = true; break; }
@@ -223,8 +288,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
                                                       2 * kStageKeys * kRowBytes)
                            : gw;
             warp_stage(acc, qu, qv, base, base + kStageKeys * kRowBytes, band,
-                       TL::Tp - 16 - 16 * mt, g, min(kStageKeys, K - s * kStageKeys),
-                       a.scale_log2, lane);
+                       TL::Tp - 16 - 16 * mt, g, stage_valid(s), a.scale_log2, lane);
             if (SP::kGInBand) fence_proxy_async_smem();   // the next TMA into this slot
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
@@ -378,13 +442,22 @@ oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, voi
                         const void* rel, int R, void* out, int B, int T, int H, float scale,
                         cudaStream_t stream, int slot)
 {
-    CUtensorMap tm_q, tm_k, tm_v, tm_r;
+    CUtensorMap tm_q, tm_k, tm_v, tm_r, tm_kn, tm_vn;
     const int box = block_size < kStageKeys ? block_size : kStageKeys;
     if (!encode_rows_bf16(&tm_q, q, static_cast<long long>(B) * T, H, Tile<MT>::Tp) ||
         !encode_rows_bf16(&tm_k, k_pool, static_cast<long long>(num_blocks) * block_size, H, box) ||
         !encode_rows_bf16(&tm_v, v_pool, static_cast<long long>(num_blocks) * block_size, H, box) ||
         !encode_rows_bf16(&tm_r, rel, R, H, Tile<MT>::RB))
         return OASR_ERR_INVALID_ARG;
+    if (FUSED) {
+        // the chunk's rows as TMA sources for the direct chunk stage
+        if (!encode_rows_bf16(&tm_kn, k_new, static_cast<long long>(B) * T, H, 16) ||
+            !encode_rows_bf16(&tm_vn, v_new, static_cast<long long>(B) * T, H, 16))
+            return OASR_ERR_INVALID_ARG;
+    } else {
+        tm_kn = tm_k;
+        tm_vn = tm_v;
+    }
     unsigned* status = status_word();
     if (!status) return OASR_ERR_CUDA;
     auto kern = chunk_attn_bf16_kernel<MT, NS, FUSED>;
@@ -409,7 +482,7 @@ oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, voi
     a.R = R;
     a.box_rows = box;
     a.scale_log2 = scale * 1.4426950408889634f;
-    kern<<<static_cast<unsigned>(B) * H, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, tm_r, a);
+    kern<<<static_cast<unsigned>(B) * H, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, tm_r, tm_kn, tm_vn, a);
     return launch_status();
 }
 

@@ -15,7 +15,7 @@ from paged_kv_chunk_gb300 import capi
 from paged_kv_chunk_gb300 import synthetic as syn
 
 from helpers import (check_close, dev, dev_pool, gpu_stream_inputs, host_pool, oracle_chunk,
-                     sample_rows, stream_case, to_np)
+                     sample_rows, stream_case, to_np, TOL_BF16_INTERNAL)
 
 pytestmark = pytest.mark.gpu
 
@@ -108,8 +108,12 @@ def test_chunk_attention_sampled_full_size(cfg):
     got = to_np(out)
     b, i, h = rows[:, 0], rows[:, 1], rows[:, 2]
     check_close(got[b, i, h], ref[b, i, h], cfg.dtype, cfg.name)
+    # append + attention as two calls: the same result up to summation order (the fused
+    # step may read the chunk as a stage of its own)
     out2, _ = _run_step(cfg, x, fused=False)
-    assert torch.equal(out, out2), "fused step and append + attention differ"
+    got2 = to_np(out2)
+    check_close(got2[b, i, h], ref[b, i, h], cfg.dtype, cfg.name + " two calls")
+    assert float(np.abs(got - got2).max()) <= TOL_BF16_INTERNAL, "fused step and append + attention differ"
     assert capi.oasr_device_status() == 0
 
 
