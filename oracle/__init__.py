@@ -83,6 +83,9 @@ def _load():
         lib.oracle_packed_relattn.restype = L
         lib.oracle_packed_relattn.argtypes = [P, P, P, P, I, I, P, P, P, I, I, I, Dbl,
                                               P, L, P]
+        lib.oracle_packed_relattn_chunked.restype = L
+        lib.oracle_packed_relattn_chunked.argtypes = [P, P, P, P, I, I, P, P, P, I, I, I, Dbl,
+                                                      I, I, P, L, P]
         lib.oracle_num_threads.restype = I
         lib.oracle_num_threads.argtypes = []
         _lib = lib
@@ -203,6 +206,45 @@ def packed_relattn(q, k, v, cu_seqlens, pos_bias_u, pos_bias_v, rel, scale=None,
     bad = lib.oracle_packed_relattn(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), cu.shape[0] - 1,
                                     total, _ptr(u), _ptr(vb), _ptr(rel), R, H, D,
                                     float(scale), rp, nr, _ptr(out))
+    if bad:
+        raise ValueError(f"{bad} rows need rel rows outside [0, {R}) or lie in no segment")
+    return out
+
+
+def packed_relattn_chunked(q, k, v, cu_seqlens, pos_bias_u, pos_bias_v, rel, chunk_size,
+                           left_chunks, scale=None, rows=None) -> np.ndarray:
+    """Chunked-limited packed attention (the Nemotron offline mask), in float64.
+
+    As packed_relattn, but query i of a segment sees key j only when
+    i // chunk_size - left_chunks <= j // chunk_size <= i // chunk_size (positions local to
+    the segment).  Other rows than `rows` are NaN.
+    """
+    lib = _load()
+    if chunk_size < 1 or left_chunks < 0:
+        raise ValueError("chunk_size must be >= 1 and left_chunks >= 0")
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    total, H, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share their shape")
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    if cu.ndim != 1 or cu.shape[0] < 1 or cu[0] != 0 or cu[-1] != total or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens must start at 0, end at total and not decrease")
+    u, vb, rel = _f32(pos_bias_u), _f32(pos_bias_v), _f32(rel)
+    if u.shape != (H, D) or vb.shape != (H, D) or rel.ndim != 3 or rel.shape[1:] != (H, D):
+        raise ValueError("pos biases must be [H, D] and rel [R, H, D]")
+    R = rel.shape[0]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    out = np.full((total, H, D), np.nan, dtype=np.float64)
+    if rows is not None:
+        rows = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 2)
+        rp, nr = _ptr(rows), rows.shape[0]
+    else:
+        rp, nr = None, 0
+    bad = lib.oracle_packed_relattn_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), cu.shape[0] - 1,
+                                            total, _ptr(u), _ptr(vb), _ptr(rel), R, H, D,
+                                            float(scale), int(chunk_size), int(left_chunks), rp, nr,
+                                            _ptr(out))
     if bad:
         raise ValueError(f"{bad} rows need rel rows outside [0, {R}) or lie in no segment")
     return out

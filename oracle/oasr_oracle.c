@@ -35,6 +35,15 @@
  *   [cu[s], cu[s+1]); query i and key j (both local to the segment) see each other
  *   in both directions, with distance i - j and rho = z - (i - j), z = (R-1)/2.
  *
+ *   Chunked-limited packed attention (Model Layer page, Nemotron ASR section: the
+ *   chunked_limited mask applies offline too; a query sees its own chunk of
+ *   num_lookahead_tokens + 1 frames plus (sliding_window - 1) // chunk earlier chunks,
+ *   and the offline pass runs in query blocks scored against their frames plus that
+ *   history).  As the packed attention, but query i of a segment sees key j only if
+ *   i/cs - left <= j/cs <= i/cs, cs = chunk frames, left = earlier chunks (integer
+ *   division of positions local to the segment).  The query blocks are how the pass is
+ *   organised, not what it computes, so the definition below is the masked attention.
+ *
  *   Paged append (ASR Engine page, section 4.3 "Batched paged forward": the chunk's
  *   rows are written through each stream's block_table, and the cache length is
  *   committed afterwards by the caller).  Row t of stream b goes to logical
@@ -260,4 +269,70 @@ int oracle_num_threads(void)
 #else
     return 1;
 #endif
+}
+
+/* Chunked-limited packed attention: the packed attention restricted, per query, to the
+ * keys of its own chunk and the `left` chunks before it (chunk = cs frames of the
+ * segment).  Every key of the segment is tested against that condition. */
+long oracle_packed_relattn_chunked(const float *q, const float *k, const float *v,
+                                   const int32_t *cu_seqlens, int num_seqs, int total,
+                                   const float *u, const float *vb, const float *rel, int R,
+                                   int H, int D, double scale, int cs, int left,
+                                   const int32_t *rows, long n_rows, double *out)
+{
+    long nrow = rows ? n_rows : (long)total * H;
+    int z = (R - 1) / 2;
+    int lmax = 0;
+    for (int s = 0; s < num_seqs; ++s) {
+        int L = cu_seqlens[s + 1] - cu_seqlens[s];
+        if (L > lmax) lmax = L;
+    }
+    long bad = 0;
+#pragma omp parallel reduction(+ : bad)
+    {
+        double *sc = (double *)malloc(sizeof(double) * (size_t)(lmax > 0 ? lmax : 1));
+        const float **vrows = (const float **)malloc(sizeof(float *) * (size_t)(lmax > 0 ? lmax : 1));
+#pragma omp for schedule(dynamic, 16)
+        for (long r = 0; r < nrow; ++r) {
+            int t, h;
+            if (rows) { t = rows[2 * r]; h = rows[2 * r + 1]; }
+            else { h = (int)(r % H); t = (int)(r / H); }
+            double *o = out + ((size_t)t * H + h) * D;
+            int seg = -1;
+            for (int s = 0; s < num_seqs; ++s)
+                if (t >= cu_seqlens[s] && t < cu_seqlens[s + 1]) { seg = s; break; }
+            int ok = seg >= 0;
+            if (ok) {
+                int start = cu_seqlens[seg];
+                int L = cu_seqlens[seg + 1] - start;
+                int i = t - start;
+                const float *qi = q + ((size_t)t * H + h) * D;
+                const float *uh = u + (size_t)h * D;
+                const float *vh = vb + (size_t)h * D;
+                int n = 0;   /* visible keys, in order */
+                for (int j = 0; j < L && ok; ++j) {
+                    if (j / cs < i / cs - left || j / cs > i / cs) continue;
+                    const float *kj = k + ((size_t)(start + j) * H + h) * D;
+                    vrows[n] = v + ((size_t)(start + j) * H + h) * D;
+                    int rho = z - (i - j);
+                    if (rho < 0 || rho >= R) { ok = 0; break; }
+                    const float *rr = rel + ((size_t)rho * H + h) * D;
+                    double ac = 0.0, bd = 0.0;
+                    for (int d = 0; d < D; ++d) {
+                        ac += ((double)qi[d] + (double)uh[d]) * (double)kj[d];
+                        bd += ((double)qi[d] + (double)vh[d]) * (double)rr[d];
+                    }
+                    sc[n++] = (ac + bd) * scale;
+                }
+                if (ok) softmax_pv(sc, n, vrows, D, o);
+            }
+            if (!ok) {
+                for (int d = 0; d < D; ++d) o[d] = NAN;
+                ++bad;
+            }
+        }
+        free(sc);
+        free((void *)vrows);
+    }
+    return bad;
 }

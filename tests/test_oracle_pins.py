@@ -20,6 +20,10 @@ or a transposed operand fails at least one of them:
   concatenation.
 * The paged append matches a hand-worked fixture, skips invalid blocks, and
   round-trips under any block permutation.
+* The chunked-limited (Nemotron offline) mask: SDPA with the chunk window and the
+  rel-pos bias as an explicit float mask; single-frame chunks return their value
+  rows; one chunk per segment is the bidirectional packed attention; the rows of
+  chunk c equal one streaming step with the previous `left` chunks as its cache.
 """
 import json
 import math
@@ -395,3 +399,94 @@ def test_append_bf16_bits_are_copied_exactly():
     np.testing.assert_array_equal(kp[bt[0, 0], 5:8], bits[0])
     np.testing.assert_array_equal(kp[bt[1, 0], 0:3], bits[1])
     assert cfg.B == 2
+
+
+# --------------------------------------------------- chunked-limited (Nemotron offline)
+
+
+def _chunk_allowed(i, j, cs, left):
+    """The chunked_limited window written out: own chunk and `left` earlier chunks."""
+    ci, cj = i // cs, j // cs
+    return ci - left <= cj <= ci
+
+
+def _packed_case(rng, lens, H=2, D=8, extra_rows=0):
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    total = int(cu[-1])
+    R = 2 * max(lens) - 1 + 2 * extra_rows
+    return cu, dict(q=_rand(rng, (total, H, D)), k=_rand(rng, (total, H, D)),
+                    v=_rand(rng, (total, H, D)), pos_bias_u=_rand(rng, (H, D)),
+                    pos_bias_v=_rand(rng, (H, D)), rel=_rand(rng, (R, H, D)))
+
+
+@pytest.mark.parametrize("cs,left", [(4, 1), (3, 0), (2, 5), (5, 2)])
+def test_chunked_is_sdpa_with_window_and_bias_mask(cs, left):
+    rng = np.random.default_rng(21 + cs + left)
+    lens = [11, 1, 7, 16]
+    cu, c = _packed_case(rng, lens, extra_rows=2)
+    H, D = c["q"].shape[1:]
+    R = c["rel"].shape[0]
+    scale = 0.35
+    out = oracle.packed_relattn_chunked(c["q"], c["k"], c["v"], cu, c["pos_bias_u"],
+                                        c["pos_bias_v"], c["rel"], cs, left, scale=scale)
+    largest = (R - 1) // 2          # distance held by row 0 of the packed table
+    row_of_distance = {largest - m: m for m in range(R)}
+    for s in range(len(lens)):
+        a, e = cu[s], cu[s + 1]
+        L = e - a
+        for h in range(H):
+            qh = c["q"][a:e, h].astype(np.float64)
+            qv = qh + c["pos_bias_v"][h]
+            mask = np.full((L, L), -np.inf)
+            for i in range(L):
+                for j in range(L):
+                    if _chunk_allowed(i, j, cs, left):
+                        mask[i, j] = scale * (qv[i] @ c["rel"][row_of_distance[i - j], h])
+            ref = _sdpa(qh + c["pos_bias_u"][h], c["k"][a:e, h], c["v"][a:e, h], scale, mask=mask)
+            np.testing.assert_allclose(out[a:e, h], ref, rtol=0, atol=1e-12)
+
+
+def test_chunked_single_frame_chunks_return_values():
+    rng = np.random.default_rng(31)
+    cu, c = _packed_case(rng, [6, 9])
+    out = oracle.packed_relattn_chunked(c["q"], c["k"], c["v"], cu, c["pos_bias_u"],
+                                        c["pos_bias_v"], c["rel"], 1, 0)
+    np.testing.assert_array_equal(out, c["v"].astype(np.float64))
+
+
+def test_chunked_one_chunk_per_segment_is_bidirectional():
+    rng = np.random.default_rng(32)
+    lens = [13, 4, 20]
+    cu, c = _packed_case(rng, lens)
+    a = oracle.packed_relattn_chunked(c["q"], c["k"], c["v"], cu, c["pos_bias_u"],
+                                      c["pos_bias_v"], c["rel"], max(lens), 0)
+    b = oracle.packed_relattn(c["q"], c["k"], c["v"], cu, c["pos_bias_u"], c["pos_bias_v"],
+                              c["rel"])
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("cs,left", [(4, 2), (3, 1), (8, 7)])
+def test_chunked_rows_equal_a_streaming_step(cs, left):
+    """Each query block is one streaming step whose cache is the previous `left`
+    chunks and whose chunk is the block's own frames (the relative table of the step
+    is the slice of the packed table holding distances C+T-1 down to -(T-1))."""
+    rng = np.random.default_rng(40 + cs)
+    L = 5 * cs + 2                  # a partial last chunk
+    cu, c = _packed_case(rng, [L])
+    H, D = c["q"].shape[1:]
+    Rp = c["rel"].shape[0]
+    zp = (Rp - 1) // 2
+    out = oracle.packed_relattn_chunked(c["q"], c["k"], c["v"], cu, c["pos_bias_u"],
+                                        c["pos_bias_v"], c["rel"], cs, left)
+    for ch in range((L + cs - 1) // cs):
+        i0, i1 = ch * cs, min(L, (ch + 1) * cs)
+        j0 = max(0, (ch - left) * cs)
+        T, C = i1 - i0, i0 - j0
+        Rs = C + 2 * T - 1
+        # streaming row m holds distance (Rs - T) - m = C + T - 1 - m; packed row of that
+        # distance is zp - (C + T - 1 - m)
+        rel_s = c["rel"][zp - (C + T - 1): zp - (C + T - 1) + Rs]
+        step = oracle.chunk_relattn(c["q"][None, i0:i1], c["k"][None, j0:i0], c["v"][None, j0:i0],
+                                    c["k"][None, i0:i1], c["v"][None, i0:i1], c["pos_bias_u"],
+                                    c["pos_bias_v"], rel_s)
+        np.testing.assert_allclose(out[i0:i1], step[0], rtol=0, atol=1e-13)
