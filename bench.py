@@ -58,7 +58,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="conformer_small",
-                    choices=sorted(syn.STREAMING_CONFIGS) + [syn.PACKED.name])
+                    choices=sorted(syn.STREAMING_CONFIGS) + [syn.PACKED.name, NEMOTRON])
     ap.add_argument("--two-call", action="store_true",
                     help="time oasr_paged_append + oasr_chunk_relattn_paged instead of the fused step")
     ap.add_argument("--layers", type=int, default=0,
@@ -95,6 +95,23 @@ def packed_flops(lengths, H, D):
     the content dot, the position dot and the P.V row each take 2*D flops."""
     L = np.asarray(lengths, dtype=np.float64)
     return float((L * L).sum()) * H * 6 * D
+
+
+# The packed row under the Nemotron offline window (chunked_limited: own chunk of 8 frames
+# plus 7 earlier chunks, so a 64-frame query block sees 120 keys).
+NEMOTRON = "nemotron_offline"
+NEMOTRON_CHUNK, NEMOTRON_LEFT = 8, 7
+
+
+def chunked_pairs(lengths, cs, left):
+    """Visible (query, key) pairs of one call under the chunked-limited window."""
+    n = 0
+    for L in np.asarray(lengths, dtype=np.int64):
+        i = np.arange(L)
+        lo = np.maximum(0, (i // cs - left) * cs)
+        hi = np.minimum(L, (i // cs + 1) * cs)
+        n += int((hi - lo).sum())
+    return n
 
 
 def packed_bytes(total, R, H, D, es=2):
@@ -441,8 +458,9 @@ def run_ours(args, cfg, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
-def run_packed(args, rank, world, local):
-    """The offline packed row: one call = one attention layer over all utterances."""
+def run_packed(args, rank, world, local, window=None):
+    """The offline packed row: one call = one attention layer over all utterances
+    (window = (chunk, left) for the chunked-limited Nemotron mask)."""
     from paged_kv_chunk_gb300 import build as pkg_build
     from paged_kv_chunk_gb300 import capi
     pkg_build.build()
@@ -457,8 +475,13 @@ def run_packed(args, rank, world, local):
     total = int(x["cu_seqlens"][-1])
 
     def call():
-        capi.oasr_packed_relattn_varlen(d["q"], d["k"], d["v"], cu, x["max_seqlen"],
-                                        d["pos_bias_u"], d["pos_bias_v"], d["rel"], out=out)
+        if window:
+            capi.oasr_packed_relattn_chunked(d["q"], d["k"], d["v"], cu, x["max_seqlen"],
+                                             d["pos_bias_u"], d["pos_bias_v"], d["rel"], window[0],
+                                             window[1], out=out)
+        else:
+            capi.oasr_packed_relattn_varlen(d["q"], d["k"], d["v"], cu, x["max_seqlen"],
+                                            d["pos_bias_u"], d["pos_bias_v"], d["rel"], out=out)
 
     stream = torch.cuda.Stream(device=dev)
     sampler = ClockSampler(local) if rank == 0 else None
@@ -485,7 +508,10 @@ def run_packed(args, rank, world, local):
     if rank != 0:
         return
     per_call_s = ms / 1e3 / args.steps
-    flops = packed_flops(x["lengths"], cfg.H, cfg.D)
+    if window:
+        flops = float(chunked_pairs(x["lengths"], *window)) * cfg.H * 6 * cfg.D
+    else:
+        flops = packed_flops(x["lengths"], cfg.H, cfg.D)
     peak, kind = measured_tensor_peak()
     achieved = flops / per_call_s / 1e12
     line = {
@@ -493,12 +519,15 @@ def run_packed(args, rank, world, local):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "packed_varlen_offline", "num_seqs": cfg.num_seqs,
+        "config": {"workload": "nemotron_chunked_offline" if window else "packed_varlen_offline",
+                   "num_seqs": cfg.num_seqs,
                    "lengths": f"U{{{cfg.min_len}..{cfg.max_len}}}", "total_frames": total,
                    "H": cfg.H, "D": cfg.D, "rel_rows": int(x["rel"].shape[0]),
+                   **({"chunk_frames": window[0], "left_chunks": window[1]} if window else {}),
                    "l2": f"inputs larger than L2: {packed_bytes(total, x['rel'].shape[0], cfg.H, cfg.D) / 1e6:.0f} MB per call"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic("packed_varlen", PACKED_SOURCES),
+                     "frac": achieved / peak,
+                     "traffic": None if window else profiled_traffic("packed_varlen", PACKED_SOURCES),
                      "kernel": "packed_attn_tc_kernel", "algorithmic_flops_per_launch": flops,
                      "avg_launch_us": per_call_s * 1e6, "peak_kind": kind},
         "gpu_launches": args.steps, "clocks": clocks,
@@ -508,9 +537,10 @@ def run_packed(args, rank, world, local):
 
 def main():
     args = parse_args()
-    if args.config == syn.PACKED.name:
+    if args.config in (syn.PACKED.name, NEMOTRON):
         rank, world, local = dist_setup()
-        run_packed(args, rank, world, local)
+        run_packed(args, rank, world, local,
+                   window=(NEMOTRON_CHUNK, NEMOTRON_LEFT) if args.config == NEMOTRON else None)
         return
     cfg = syn.STREAMING_CONFIGS[args.config]
     if args.impl == "reference":

@@ -113,8 +113,11 @@ oasr_status oasr_chunk_relattn_paged(const void* q, const void* k_pool, const vo
  * One fused streaming step: oasr_paged_append followed by oasr_chunk_relattn_paged, in
  * one launch.  Each (stream, head) program writes its head's slice of the chunk into
  * the pool and then attends over cache + chunk, so the chunk is never re-read from
- * HBM.  Results are identical to the two calls in sequence; the same requirements
- * apply.  Block ids of different streams must not alias a block that this step writes.
+ * HBM (when every page the chunk lands in is a valid block, the attention reads the
+ * chunk's keys straight from k_new / v_new).  Results equal the two calls in sequence up
+ * to floating-point summation order; the pool afterwards is bit-identical.  The same
+ * requirements apply.  Block ids of different streams must not alias a block that this
+ * step writes.
  */
 oasr_status oasr_chunk_step_paged(const void* q, const void* k_new, const void* v_new,
                                   void* k_pool, void* v_pool, int num_blocks, int block_size,
@@ -140,6 +143,27 @@ oasr_status oasr_packed_relattn_varlen(const void* q, const void* k, const void*
                                        const void* pos_bias_v, const void* rel, int R, void* out,
                                        int H, int D, float scale, oasr_dtype dt,
                                        cudaStream_t stream);
+
+/*
+ * Chunked-limited packed attention: the Nemotron offline mask (Model Layer page, Nemotron
+ * ASR section: the chunked_limited mask applies offline too; a query sees its own chunk of
+ * num_lookahead_tokens + 1 frames plus (sliding_window - 1) // chunk earlier chunks, and
+ * the offline pass scores each query block against its own frames plus that history).
+ *
+ * As oasr_packed_relattn_varlen, but query i of a segment attends to key j only when
+ * i / chunk_size - left_chunks <= j / chunk_size <= i / chunk_size (positions local to the
+ * segment, integer division): chunk_size = num_lookahead_tokens + 1, left_chunks =
+ * (sliding_window - 1) / chunk_size.  The work done grows with the segment length, not its
+ * square.  Requirements as for oasr_packed_relattn_varlen, plus chunk_size >= 1 and
+ * left_chunks >= 0 (else OASR_ERR_INVALID_ARG).  A chunk_size of at least every segment
+ * length gives the bidirectional attention.
+ */
+oasr_status oasr_packed_relattn_chunked(const void* q, const void* k, const void* v,
+                                        const int32_t* cu_seqlens, int num_seqs, int max_seqlen,
+                                        int total, const void* pos_bias_u,
+                                        const void* pos_bias_v, const void* rel, int R, void* out,
+                                        int H, int D, float scale, int chunk_size,
+                                        int left_chunks, oasr_dtype dt, cudaStream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char* oasr_status_string(oasr_status status);

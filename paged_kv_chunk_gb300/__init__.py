@@ -8,8 +8,9 @@ Importing this package loads nothing; the library is loaded on first use and a m
 build raises.
 """
 from .capi import (OasrError, oasr_chunk_relattn_paged, oasr_chunk_step_paged,  # noqa: F401
-                   oasr_device_status, oasr_packed_relattn_varlen, oasr_paged_append,
-                   oasr_version)
+                   oasr_device_status, oasr_packed_relattn_chunked, oasr_packed_relattn_varlen,
+                   oasr_paged_append, oasr_version)
 
 __all__ = ["OasrError", "oasr_paged_append", "oasr_chunk_relattn_paged", "oasr_chunk_step_paged",
-           "oasr_packed_relattn_varlen", "oasr_device_status", "oasr_version"]
+           "oasr_packed_relattn_varlen", "oasr_packed_relattn_chunked", "oasr_device_status",
+           "oasr_version"]

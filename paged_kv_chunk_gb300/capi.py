@@ -51,8 +51,10 @@ def load() -> ctypes.CDLL:
         L.oasr_chunk_step_paged.argtypes = [P, P, P, P, P, I, I, P, I, P, P, P, P, I, P, I, I, I,
                                             I, F, I, S]
         L.oasr_packed_relattn_varlen.argtypes = [P, P, P, P, I, I, I, P, P, P, I, P, I, I, F, I, S]
+        L.oasr_packed_relattn_chunked.argtypes = [P, P, P, P, I, I, I, P, P, P, I, P, I, I, F, I, I,
+                                                  I, S]
         for fn in ("oasr_paged_append", "oasr_chunk_relattn_paged", "oasr_chunk_step_paged",
-                   "oasr_packed_relattn_varlen"):
+                   "oasr_packed_relattn_varlen", "oasr_packed_relattn_chunked"):
             getattr(L, fn).restype = I
         L.oasr_status_string.argtypes = [I]
         L.oasr_status_string.restype = ctypes.c_char_p
@@ -199,6 +201,31 @@ def oasr_packed_relattn_varlen(q, k, v, cu_seqlens, max_seqlen, pos_bias_u, pos_
         total, _dev(pos_bias_u, "pos_bias_u", q.dtype), _dev(pos_bias_v, "pos_bias_v", q.dtype),
         _dev(rel, "rel", q.dtype), rel.shape[0], _dev(out, "out", q.dtype), H, D, scale, dt,
         _stream(stream)))
+    return out
+
+
+def oasr_packed_relattn_chunked(q, k, v, cu_seqlens, max_seqlen, pos_bias_u, pos_bias_v, rel,
+                                chunk_size, left_chunks, out=None, scale=None, stream=None):
+    """Chunked-limited packed attention (own chunk + left_chunks earlier chunks per query);
+    returns out [total,H,D]."""
+    L = load()
+    dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty_like(q)
+    total, H, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape or out.shape != q.shape:
+        raise ValueError("q, k, v, out must share their shape [total, H, D]")
+    if tuple(pos_bias_u.shape) != (H, D) or tuple(pos_bias_v.shape) != (H, D):
+        raise ValueError("pos biases must be [H, D]")
+    if rel.dim() != 3 or tuple(rel.shape[1:]) != (H, D):
+        raise ValueError("rel must be [R, H, D]")
+    scale = D ** -0.5 if scale is None else float(scale)
+    _check("oasr_packed_relattn_chunked", L.oasr_packed_relattn_chunked(
+        _dev(q, "q", q.dtype), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype),
+        _dev(cu_seqlens, "cu_seqlens", torch.int32, 1), cu_seqlens.shape[0] - 1, int(max_seqlen),
+        total, _dev(pos_bias_u, "pos_bias_u", q.dtype), _dev(pos_bias_v, "pos_bias_v", q.dtype),
+        _dev(rel, "rel", q.dtype), rel.shape[0], _dev(out, "out", q.dtype), H, D, scale,
+        int(chunk_size), int(left_chunks), dt, _stream(stream)))
     return out
 
 

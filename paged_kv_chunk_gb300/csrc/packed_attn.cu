@@ -22,7 +22,7 @@ __global__ void __launch_bounds__(128) packed_attn_f32_kernel(
     const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
     const int32_t* __restrict__ cu, int num_seqs, int total, const float* __restrict__ u,
     const float* __restrict__ vb, const float* __restrict__ rel, int R, int z,
-    float* __restrict__ out, int H, float scale, unsigned* status)
+    float* __restrict__ out, int H, float scale, int cs, int left, unsigned* status)
 {
     __shared__ float s_qu[4][kHeadDim];
     __shared__ float s_qv[4][kHeadDim];
@@ -45,6 +45,9 @@ __global__ void __launch_bounds__(128) packed_attn_f32_kernel(
         return;
     }
     const int L = end - start, i = t - start;
+    // keys this query sees: the whole segment, or (cs > 0) its own chunk and `left` earlier ones
+    const int kl = cs > 0 ? max(0, (i / cs - left) * cs) : 0;
+    const int kh = cs > 0 ? min(L, (i / cs + 1) * cs) : L;
     const long long qo = (static_cast<long long>(t) * H + h) * kHeadDim;
     for (int d = lane; d < kHeadDim; d += 32) {
         s_qu[warp][d] = q[qo + d] + u[h * kHeadDim + d];
@@ -52,10 +55,10 @@ __global__ void __launch_bounds__(128) packed_attn_f32_kernel(
     }
     __syncwarp();
     float m = -INFINITY, l = 0.f, o0 = 0.f, o1 = 0.f;
-    for (int j0 = 0; j0 < L; j0 += 32) {
+    for (int j0 = kl; j0 < kh; j0 += 32) {
         const int j = j0 + lane;
         float sc = -INFINITY;
-        if (j < L) {
+        if (j < kh) {
             const float4* kr =
                 reinterpret_cast<const float4*>(k + (static_cast<long long>(start + j) * H + h) * kHeadDim);
             float acc = 0.f;
@@ -89,14 +92,14 @@ __global__ void __launch_bounds__(128) packed_attn_f32_kernel(
         for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         const float m_new = fmaxf(m, mx);
         const float alpha = (m == -INFINITY) ? 0.f : expf(m - m_new);
-        const float p = (j < L) ? expf(sc - m_new) : 0.f;
+        const float p = (j < kh) ? expf(sc - m_new) : 0.f;
         float psum = p;
 #pragma unroll
         for (int o = 16; o; o >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
         l = l * alpha + psum;
         o0 *= alpha;
         o1 *= alpha;
-        const int nj = min(32, L - j0);
+        const int nj = min(32, kh - j0);
         for (int jj = 0; jj < nj; ++jj) {
             const float pj = __shfl_sync(0xffffffffu, p, jj);
             const float* vr = v + (static_cast<long long>(start + j0 + jj) * H + h) * kHeadDim;
@@ -115,17 +118,17 @@ __global__ void __launch_bounds__(128) packed_attn_f32_kernel(
 oasr_status launch_packed_tc(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
                              int num_seqs, int total, const void* pos_bias_u,
                              const void* pos_bias_v, const void* rel, int R, void* out, int H,
-                             float scale, cudaStream_t stream);
+                             float scale, int cs, int left, cudaStream_t stream);
 }  // namespace oasr
 
-extern "C" oasr_status oasr_packed_relattn_varlen(const void* q, const void* k, const void* v,
-                                                  const int32_t* cu_seqlens, int num_seqs,
-                                                  int max_seqlen, int total,
-                                                  const void* pos_bias_u, const void* pos_bias_v,
-                                                  const void* rel, int R, void* out, int H, int D,
-                                                  float scale, oasr_dtype dt, cudaStream_t stream)
+namespace oasr {
+namespace {
+
+oasr_status packed_impl(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                        int num_seqs, int max_seqlen, int total, const void* pos_bias_u,
+                        const void* pos_bias_v, const void* rel, int R, void* out, int H, int D,
+                        float scale, int cs, int left, oasr_dtype dt, cudaStream_t stream)
 {
-    using namespace oasr;
     if (!q || !k || !v || !cu_seqlens || !pos_bias_u || !pos_bias_v || !rel || !out)
         return OASR_ERR_INVALID_ARG;
     if (num_seqs <= 0 || max_seqlen <= 0 || total <= 0 || R <= 0 || H <= 0 || D <= 0)
@@ -145,9 +148,38 @@ extern "C" oasr_status oasr_packed_relattn_varlen(const void* q, const void* k, 
             static_cast<const float*>(q), static_cast<const float*>(k),
             static_cast<const float*>(v), cu_seqlens, num_seqs, total,
             static_cast<const float*>(pos_bias_u), static_cast<const float*>(pos_bias_v),
-            static_cast<const float*>(rel), R, z, static_cast<float*>(out), H, scale, status);
+            static_cast<const float*>(rel), R, z, static_cast<float*>(out), H, scale, cs, left,
+            status);
         return launch_status();
     }
     return launch_packed_tc(q, k, v, cu_seqlens, num_seqs, total, pos_bias_u, pos_bias_v, rel, R,
-                            out, H, scale, stream);
+                            out, H, scale, cs, left, stream);
+}
+
+}  // namespace
+}  // namespace oasr
+
+extern "C" oasr_status oasr_packed_relattn_varlen(const void* q, const void* k, const void* v,
+                                                  const int32_t* cu_seqlens, int num_seqs,
+                                                  int max_seqlen, int total,
+                                                  const void* pos_bias_u, const void* pos_bias_v,
+                                                  const void* rel, int R, void* out, int H, int D,
+                                                  float scale, oasr_dtype dt, cudaStream_t stream)
+{
+    return oasr::packed_impl(q, k, v, cu_seqlens, num_seqs, max_seqlen, total, pos_bias_u,
+                             pos_bias_v, rel, R, out, H, D, scale, 0, 0, dt, stream);
+}
+
+extern "C" oasr_status oasr_packed_relattn_chunked(const void* q, const void* k, const void* v,
+                                                   const int32_t* cu_seqlens, int num_seqs,
+                                                   int max_seqlen, int total,
+                                                   const void* pos_bias_u, const void* pos_bias_v,
+                                                   const void* rel, int R, void* out, int H, int D,
+                                                   float scale, int chunk_size, int left_chunks,
+                                                   oasr_dtype dt, cudaStream_t stream)
+{
+    if (chunk_size < 1 || left_chunks < 0) return OASR_ERR_INVALID_ARG;
+    return oasr::packed_impl(q, k, v, cu_seqlens, num_seqs, max_seqlen, total, pos_bias_u,
+                             pos_bias_v, rel, R, out, H, D, scale, chunk_size, left_chunks, dt,
+                             stream);
 }

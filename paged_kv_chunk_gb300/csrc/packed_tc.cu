@@ -78,6 +78,7 @@ struct TcArgs {
     uint16_t* out;
     unsigned* status;
     int num_seqs, total, H, z;
+    int cs, left;            // chunked-limited window (MASKED kernel): chunk frames, earlier chunks
     float scale_log2;
 };
 
@@ -183,6 +184,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 
 // ------------------------------------------------------------------------ kernel
 
+template <bool MASKED>
 __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const __grid_constant__ CUtensorMap tm_r, const TcArgs a)
@@ -281,7 +283,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
         __syncthreads();
     }
     const long long n_items = static_cast<long long>(s_tile[ns]) * a.H;
-    auto decode = [&](long long item, int& start, int& L, int& i0, int& h) {
+    // item -> segment start and length, first query of the tile, head, and the keys
+    // [kl, kh) the tile's queries can see (the whole segment, or with the chunked-limited
+    // window the chunks from the first query's window start to the last query's chunk)
+    auto decode = [&](long long item, int& start, int& L, int& i0, int& h, int& kl, int& kh) {
         const int tile = static_cast<int>(item / a.H);
         h = static_cast<int>(item - static_cast<long long>(tile) * a.H);
         int lo = 0, hi = ns - 1;
@@ -292,6 +297,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
         start = s_cu[lo];
         L = s_cu[lo + 1] - start;
         i0 = (tile - s_tile[lo]) * kBM;
+        kl = 0;
+        kh = L;
+        if (MASKED) {
+            const int ilast = (i0 + kBM < L ? i0 + kBM : L) - 1;
+            kl = (i0 / a.cs - a.left) * a.cs;
+            kl = kl > 0 ? kl : 0;
+            kh = (ilast / a.cs + 1) * a.cs;
+            kh = kh < L ? kh : L;
+        }
     };
 
     // Softmax warps take every wait together: a warp-wide vote keeps the warp converged for
@@ -310,9 +324,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             int g = 0;
             bool ok = true;
             for (long long item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-                int start, L, i0, h;
-                decode(item, start, L, i0, h);
-                const int n_st = (L + kBN - 1) / kBN;
+                int start, L, i0, h, kl, kh;
+                decode(item, start, L, i0, h, kl, kh);
+                const int n_st = (kh - kl + kBN - 1) / kBN;
                 for (int s = 0; s < n_st; ++s, ++g) {
                     const int slot = g & 1;
                     if (g >= 2 && !wait_or_abort(bar_empty + 8 * slot, ((g >> 1) - 1) & 1, s_abort)) {
@@ -322,9 +336,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     const uint32_t base = sb + SP::off_slot + slot * SP::slot;
                     const uint32_t bar = bar_full + 8 * slot;
                     mbar_arrive_expect_tx(bar, SP::slot);
-                    tma_load_3d_hint(base, &tm_k, bar, 0, h, start + s * kBN, pol);
-                    tma_load_3d(base + SP::off_band, &tm_r, bar, 0, h, a.z - i0 + s * kBN - (kBM - 1));
-                    tma_load_3d_hint(base + SP::off_v, &tm_v, bar, 0, h, start + s * kBN, pol);
+                    const int js = kl + s * kBN;   // first key of the stage
+                    tma_load_3d_hint(base, &tm_k, bar, 0, h, start + js, pol);
+                    tma_load_3d(base + SP::off_band, &tm_r, bar, 0, h, a.z - i0 + js - (kBM - 1));
+                    tma_load_3d_hint(base + SP::off_v, &tm_v, bar, 0, h, start + js, pol);
                 }
             }
             // no copy may still be landing when the CTA exits
@@ -352,9 +367,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             };
             bool ok = true;
             for (long long item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
-                int start, L, i0, h;
-                decode(item, start, L, i0, h);
-                const int n_st = (L + kBN - 1) / kBN;
+                int start, L, i0, h, kl, kh;
+                decode(item, start, L, i0, h, kl, kh);
+                const int n_st = (kh - kl + kBN - 1) / kBN;
                 // stage 0 needs this item's q tiles, its slot, and S/G read out
                 ok = wait_or_abort(bar_q_ready, it & 1, s_abort) &&
                      wait_or_abort(bar_full + 8 * (g & 1), (g >> 1) & 1, s_abort) &&
@@ -418,9 +433,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
         };
         int g = 0, it = 0, sg = 0;
         for (long long item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
-            int start, L, i0, h;
-            decode(item, start, L, i0, h);
-            const int n_st = (L + kBN - 1) / kBN;
+            int start, L, i0, h, kl, kh;
+            decode(item, start, L, i0, h, kl, kh);
+            const int n_st = (kh - kl + kBN - 1) / kBN;
             // bf16(q+u) and bf16(q+v): this thread's half row, once the previous item's S/G are done
             if (it > 0 && !warp_wait(bar_q_free, (it - 1) & 1)) break;
             {
@@ -503,10 +518,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_sg_free);
-                // scale (log2 domain), mask keys past the segment, this half's max
-                const int kv = L - s * kBN - 64 * hf;   // valid keys in this half
+                // scale (log2 domain), mask keys this row does not see, this half's max:
+                // the half holds keys jh .. jh+63; row r sees [ka, kb) of them
+                const int jh = kl + s * kBN + 64 * hf;
+                int ka = 0, kb = kh - jh;
+                if (MASKED) {
+                    const int ci = (i0 + r) / a.cs;
+                    const int lo = (ci - a.left) * a.cs - jh, hi = (ci + 1) * a.cs - jh;
+                    ka = lo > 0 ? lo : 0;
+                    kb = hi < kb ? hi : kb;
+                }
                 float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-                if (kv >= 64) {
+                if (ka <= 0 && kb >= 64) {
 #pragma unroll
                     for (int j = 0; j < 64; j += 4) {
                         sc[j] *= a.scale_log2; sc[j + 1] *= a.scale_log2;
@@ -518,7 +541,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
 #pragma unroll
                     for (int j = 0; j < 64; j += 4) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) sc[j + e] = j + e < kv ? sc[j + e] * a.scale_log2 : -INFINITY;
+                        for (int e = 0; e < 4; ++e)
+                            sc[j + e] = (j + e >= ka && j + e < kb) ? sc[j + e] * a.scale_log2 : -INFINITY;
                         mx0 = fmaxf(mx0, sc[j]); mx1 = fmaxf(mx1, sc[j + 1]);
                         mx2 = fmaxf(mx2, sc[j + 2]); mx3 = fmaxf(mx3, sc[j + 3]);
                     }
@@ -543,6 +567,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     OASR_TMEM_ST32(tl + kColO + 32 * hf, oo);
                 }
                 m_used = m_new;
+                // a row that has seen no key yet has max -inf: its P is 0, not NaN
+                const float mref = m_used == -INFINITY ? 0.f : m_used;
                 {
                     float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
@@ -550,8 +576,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                         uint32_t pk[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const float p0 = ex2_approx(sc[32 * q2 + 2 * j] - m_used);
-                            const float p1 = ex2_approx(sc[32 * q2 + 2 * j + 1] - m_used);
+                            const float p0 = ex2_approx(sc[32 * q2 + 2 * j] - mref);
+                            const float p1 = ex2_approx(sc[32 * q2 + 2 * j + 1] - mref);
                             ps0 += p0;
                             ps1 += p1;
                             pk[j] = pack_bf16(p0, p1);
@@ -562,9 +588,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 }
                 // V rows past the segment belong to the next one: zero them so that P = 0
                 // there never meets a non-finite value
-                if (L - s * kBN < kBN) {
+                const int kstage = kh - (kl + s * kBN);   // keys of this stage that exist
+                if (kstage < kBN) {
                     if (!warp_wait(bar_full + 8 * (g & 1), (g >> 1) & 1)) { ok = false; break; }
-                    if (r >= L - s * kBN) {
+                    if (r >= kstage) {
                         uint4* vrow = reinterpret_cast<uint4*>(slot_p + SP::off_v + r * kRowBytes) + 4 * hf;
 #pragma unroll
                         for (int c = 0; c < 4; ++c) vrow[c] = make_uint4(0u, 0u, 0u, 0u);
@@ -614,15 +641,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
     if (err) atomicOr(a.status, err);
 }
 
-int g_smem_done_tc[64];
+int g_smem_done_tc[2][64];
 
 }  // namespace
 
-// Host launcher used by oasr_packed_relattn_varlen (bf16).
+// Host launcher used by oasr_packed_relattn_varlen and oasr_packed_relattn_chunked (bf16);
+// cs > 0 selects the chunked-limited window (own chunk of cs frames and `left` earlier ones).
 oasr_status launch_packed_tc(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
                              int num_seqs, int total, const void* pos_bias_u,
                              const void* pos_bias_v, const void* rel, int R, void* out, int H,
-                             float scale, cudaStream_t stream)
+                             float scale, int cs, int left, cudaStream_t stream)
 {
     if (num_seqs > kTcMaxSeqs) return OASR_ERR_UNSUPPORTED;
     CUtensorMap tm_k, tm_v, tm_r;
@@ -633,10 +661,11 @@ oasr_status launch_packed_tc(const void* q, const void* k, const void* v, const 
     const int sms = sm_count();
     if (!status || !sms) return OASR_ERR_CUDA;
     constexpr int smem = TcSmem::bytes;
-    if (!ensure_smem(packed_attn_tc_kernel, smem, g_smem_done_tc)) return OASR_ERR_CUDA;
+    const bool masked = cs > 0;
+    auto kern = masked ? packed_attn_tc_kernel<true> : packed_attn_tc_kernel<false>;
+    if (!ensure_smem(kern, smem, g_smem_done_tc[masked ? 1 : 0])) return OASR_ERR_CUDA;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, packed_attn_tc_kernel, kTcThreads, smem) !=
-            cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTcThreads, smem) != cudaSuccess ||
         per_sm < 1)
         return OASR_ERR_CUDA;
     TcArgs a;
@@ -650,10 +679,12 @@ oasr_status launch_packed_tc(const void* q, const void* k, const void* v, const 
     a.total = total;
     a.H = H;
     a.z = (R - 1) / 2;
+    a.cs = masked ? cs : 1;
+    a.left = masked ? left : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
     const long long items_bound = ((static_cast<long long>(total) + kBM - 1) / kBM + num_seqs) * H;
     const int grid = static_cast<int>(items_bound < sms ? items_bound : sms);
-    packed_attn_tc_kernel<<<grid, kTcThreads, smem, stream>>>(tm_k, tm_v, tm_r, a);
+    kern<<<grid, kTcThreads, smem, stream>>>(tm_k, tm_v, tm_r, a);
     return launch_status();
 }
 

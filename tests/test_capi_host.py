@@ -16,7 +16,8 @@ def lib():
 def test_exports_every_header_symbol(lib):
     names = capi.header_symbols()
     assert {"oasr_paged_append", "oasr_chunk_relattn_paged", "oasr_chunk_step_paged",
-            "oasr_packed_relattn_varlen", "oasr_status_string", "oasr_device_status",
+            "oasr_packed_relattn_varlen", "oasr_packed_relattn_chunked", "oasr_status_string",
+            "oasr_device_status",
             "oasr_version"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in the header but not exported"
@@ -97,6 +98,25 @@ def test_packed_rejects_bad_arguments(lib, args, expect):
     r = lib.oasr_packed_relattn_varlen(a["q"], a["k"], a["v"], a["cu"], a["ns"], a["maxlen"],
                                        a["total"], a["u"], a["vb"], a["rel"], a["R"], a["out"],
                                        a["H"], a["D"], 0.125, a["dt"], None)
+    assert r == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    (dict(cs=0), capi.OASR_ERR_INVALID_ARG),
+    (dict(left=-1), capi.OASR_ERR_INVALID_ARG),
+    (dict(ns=1025), capi.OASR_ERR_UNSUPPORTED),
+    (dict(D=128), capi.OASR_ERR_UNSUPPORTED),
+    (dict(total=0), capi.OASR_ERR_INVALID_ARG),
+    (dict(cu=None), capi.OASR_ERR_INVALID_ARG),
+    (dict(k=FAKE + 4), capi.OASR_ERR_INVALID_ARG),
+])
+def test_chunked_rejects_bad_arguments(lib, args, expect):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, cu=FAKE, ns=4, maxlen=100, total=300, u=FAKE, vb=FAKE,
+             rel=FAKE, R=199, out=FAKE, H=8, D=64, cs=8, left=7, dt=capi.OASR_BF16)
+    a.update(args)
+    r = lib.oasr_packed_relattn_chunked(a["q"], a["k"], a["v"], a["cu"], a["ns"], a["maxlen"],
+                                        a["total"], a["u"], a["vb"], a["rel"], a["R"], a["out"],
+                                        a["H"], a["D"], 0.125, a["cs"], a["left"], a["dt"], None)
     assert r == expect
 
 

@@ -390,3 +390,72 @@ def test_padding_lanes_share_a_scratch_block():
     used[x["block_table"].ravel()] = True
     np.testing.assert_array_equal(kp[used], expect[used])
     assert capi.oasr_device_status() == 0
+
+
+# ------------------------------------------------- chunked-limited packed (Nemotron offline)
+
+NEMOTRON_CHUNK, NEMOTRON_LEFT = 8, 7   # 64-frame query blocks see 64 + 7 * 8 = 120 keys
+
+
+def _run_chunked(x, dtype, cs, left):
+    d = {k: dev(x[k], dtype) for k in ("q", "k", "v", "pos_bias_u", "pos_bias_v", "rel")}
+    cu = torch.from_numpy(x["cu_seqlens"]).cuda()
+    out = capi.oasr_packed_relattn_chunked(d["q"], d["k"], d["v"], cu, max(x["max_seqlen"], 1),
+                                           d["pos_bias_u"], d["pos_bias_v"], d["rel"], cs, left)
+    torch.cuda.synchronize()
+    return out
+
+
+def _oracle_chunked(x, cs, left, rows=None):
+    return oracle.packed_relattn_chunked(x["q"], x["k"], x["v"], x["cu_seqlens"], x["pos_bias_u"],
+                                         x["pos_bias_v"], x["rel"], cs, left, rows=rows)
+
+
+@pytest.mark.parametrize("cs,left", [(8, 7), (1, 0), (4, 2), (16, 1), (3, 50), (128, 0), (5, 30)],
+                         ids=lambda v: str(v))
+@pytest.mark.parametrize("lengths", [
+    [1], [64], [129], [7, 0, 130, 1, 64, 200, 3], [300, 257, 1, 150],
+], ids=str)
+def test_chunked_full(lengths, cs, left):
+    _, x = _packed_case(lengths, seed=5)
+    out = _run_chunked(x, "bf16", cs, left)
+    check_close(to_np(out), _oracle_chunked(x, cs, left), "bf16", f"chunked {lengths} {cs},{left}")
+    assert capi.oasr_device_status() == 0
+
+
+@pytest.mark.parametrize("cs,left", [(8, 7), (1, 0), (3, 4)], ids=lambda v: str(v))
+def test_chunked_full_f32(cs, left):
+    _, x = _packed_case([70, 1, 33, 140], dtype="f32", seed=6)
+    out = _run_chunked(x, "f32", cs, left)
+    check_close(to_np(out), _oracle_chunked(x, cs, left), "f32", f"chunked f32 {cs},{left}")
+    assert capi.oasr_device_status() == 0
+
+
+def test_chunked_one_chunk_is_the_bidirectional_call():
+    """A chunk as long as every segment is the plain packed attention, bit for bit."""
+    lengths = [300, 1, 129, 64]
+    _, x = _packed_case(lengths, seed=8)
+    a = _run_chunked(x, "bf16", max(lengths), 0)
+    b = _run_packed(x, "bf16")
+    assert torch.equal(a, b)
+
+
+def test_chunked_full_size_sampled():
+    """The 256-utterance packed row under the Nemotron window: 4096 sampled rows plus
+    every row of the shortest and the longest segment."""
+    cfg = syn.PACKED
+    x = syn.packed_inputs(cfg)
+    out = _run_chunked(x, cfg.dtype, NEMOTRON_CHUNK, NEMOTRON_LEFT)
+    rng = np.random.default_rng(78)
+    total = int(x["cu_seqlens"][-1])
+    t = rng.choice(total, size=4096, replace=False)
+    h = rng.integers(0, cfg.H, size=4096)
+    rows = [np.stack([t, h], 1)]
+    for s in (int(np.argmin(x["lengths"])), int(np.argmax(x["lengths"]))):
+        a, e = x["cu_seqlens"][s], x["cu_seqlens"][s + 1]
+        rows.append(np.stack([np.repeat(np.arange(a, e), cfg.H), np.tile(np.arange(cfg.H), e - a)], 1))
+    rows = np.concatenate(rows).astype(np.int32)
+    ref = _oracle_chunked(x, NEMOTRON_CHUNK, NEMOTRON_LEFT, rows=rows)
+    got = to_np(out)
+    check_close(got[rows[:, 0], rows[:, 1]], ref[rows[:, 0], rows[:, 1]], cfg.dtype, "chunked full")
+    assert capi.oasr_device_status() == 0
