@@ -60,13 +60,14 @@ struct TcSmem {
     static constexpr int off_slot = 0;                           // 2 slots
     static constexpr int off_qu = 2 * slot;                      // 16 KB
     static constexpr int off_qv = off_qu + kBM * kRowBytes;      // 16 KB
-    static constexpr int off_stg = off_qv + kBM * kRowBytes;     // dedicated staging
+    static constexpr int off_qbuf = off_qv + kBM * kRowBytes;    // 16 KB: next item's q rows (TMA)
+    static constexpr int off_stg = off_qbuf + kBM * kRowBytes;   // dedicated staging
     static constexpr int off_xm = off_stg + (kSoftmaxWarps - kStgOverlay) * kStgWarpBytes;
     static constexpr int off_cu = off_xm + 2 * 2 * kBM * 4;      // [exchange parity][half][row]
     static constexpr int off_tile = off_cu + (kTcMaxSeqs + 1) * 4;
     static constexpr int off_misc = off_tile + (kTcMaxSeqs + 1) * 4;   // wsum[16], tmem, abort
     static constexpr int off_bar = (off_misc + 128 + 7) & ~7;
-    static constexpr int n_bars = 2 + 2 + 7 + 4;
+    static constexpr int n_bars = 2 + 2 + 7 + 4 + 2;
     static constexpr int bytes = off_bar + n_bars * 8 + 1024;
 };
 
@@ -186,8 +187,8 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 
 template <bool MASKED>
 __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
-    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-    const __grid_constant__ CUtensorMap tm_r, const TcArgs a)
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r, const TcArgs a)
 {
     using SP = TcSmem;
     extern __shared__ uint8_t smem_raw[];
@@ -212,6 +213,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
     const uint32_t bar_q_free = bar_q_ready + 8;       // last S/G MMA of an item finished
     const uint32_t bar_drain = bar_q_free + 8;         // everything the MMA issuer issued finished
     const uint32_t bar_pair = bar_drain + 8;           // [4] softmax warp pair exchanged a value
+    const uint32_t bar_qb_full = bar_pair + 32;        // q rows of the next item landed
+    const uint32_t bar_qb_free = bar_qb_full + 8;      // softmax warps have read the q rows
     const int ns = a.num_seqs;
 
     if (tid == 0) {
@@ -227,6 +230,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
         mbar_init(bar_q_free, 1);
         mbar_init(bar_drain, 1);
         for (int i = 0; i < 4; ++i) mbar_init(bar_pair + 8 * i, 64);
+        mbar_init(bar_qb_full, 1);
+        mbar_init(bar_qb_free, kSoftmaxWarps);
         fence_mbar_init();
         *s_abort = 0;
     }
@@ -317,16 +322,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
     if (warp == kTmaWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
             prefetch_tensormap(&tm_r);
             const uint64_t pol = policy_evict_last();   // K/V tiles are re-read by every query tile
-            int g = 0;
+            int g = 0, itp = 0;
             bool ok = true;
-            for (long long item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+            for (long long item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++itp) {
                 int start, L, i0, h, kl, kh;
                 decode(item, start, L, i0, h, kl, kh);
                 const int n_st = (kh - kl + kBN - 1) / kBN;
+                // the item's 128 q rows, once the softmax warps have read the previous ones
+                if (itp > 0 && !wait_or_abort(bar_qb_free, (itp - 1) & 1, s_abort)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(bar_qb_full, kBM * kRowBytes);
+                tma_load_3d(sb + SP::off_qbuf, &tm_q, bar_qb_full, 0, h, start + i0);
                 for (int s = 0; s < n_st; ++s, ++g) {
                     const int slot = g & 1;
                     if (g >= 2 && !wait_or_abort(bar_empty + 8 * slot, ((g >> 1) - 1) & 1, s_abort)) {
@@ -345,6 +358,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             // no copy may still be landing when the CTA exits
             for (int u = g - 2; u < g; ++u)
                 if (u >= 0 && !mbar_wait(bar_full + 8 * (u & 1), (u >> 1) & 1)) *s_abort = 1;
+            if (itp > 0 && !mbar_wait(bar_qb_full, (itp - 1) & 1)) *s_abort = 1;
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------- MMA issuer
@@ -438,16 +452,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             const int n_st = (kh - kl + kBN - 1) / kBN;
             // bf16(q+u) and bf16(q+v): this thread's half row, once the previous item's S/G are done
             if (it > 0 && !warp_wait(bar_q_free, (it - 1) & 1)) break;
+            if (!warp_wait(bar_qb_full, it & 1)) break;
             {
-                const int qrow = start + i0 + r;
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    a.q + (static_cast<long long>(qrow < a.total ? qrow : 0) * a.H + h) * kHeadDim);
                 const uint4* up = reinterpret_cast<const uint4*>(a.pos_bias_u + h * kHeadDim);
                 const uint4* vp = reinterpret_cast<const uint4*>(a.pos_bias_v + h * kHeadDim);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     const int c = 4 * hf + cc;
-                    const uint4 qc = qrow < a.total ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t offs = static_cast<uint32_t>(r * kRowBytes + ((c ^ (r & 7)) << 4));
+                    const uint4 qc = *reinterpret_cast<const uint4*>(sm + SP::off_qbuf + offs);
                     const uint4 uc = __ldg(up + c), vc = __ldg(vp + c);
                     const uint32_t w[4] = {qc.x, qc.y, qc.z, qc.w};
                     const uint32_t wu[4] = {uc.x, uc.y, uc.z, uc.w};
@@ -459,10 +472,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                         ou[e] = pack_bf16(lo + __uint_as_float(wu[e] << 16), hi + __uint_as_float(wu[e] & 0xffff0000u));
                         ov[e] = pack_bf16(lo + __uint_as_float(wv[e] << 16), hi + __uint_as_float(wv[e] & 0xffff0000u));
                     }
-                    const uint32_t offs = static_cast<uint32_t>(r * kRowBytes + ((c ^ (r & 7)) << 4));
                     *reinterpret_cast<uint4*>(sm + SP::off_qu + offs) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
                     *reinterpret_cast<uint4*>(sm + SP::off_qv + offs) = make_uint4(ov[0], ov[1], ov[2], ov[3]);
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_qb_free);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_q_ready);
@@ -499,16 +513,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                             OASR_TMEM_LD32(tl + colg + 32, rr);
                             tmem_wait_ld();
                         }
+                        // only the 16-byte pieces this row reads (columns 31 - lane .. 62 - lane):
+                        // lanes that skip a piece move no data, so about half the store traffic goes
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
-                            *reinterpret_cast<uint4*>(stg + 4 * k) =
-                                make_uint4(rr[4 * k], rr[4 * k + 1], rr[4 * k + 2], rr[4 * k + 3]);
+                            if (4 * k + 3 >= 31 - lane)
+                                *reinterpret_cast<uint4*>(stg + 4 * k) =
+                                    make_uint4(rr[4 * k], rr[4 * k + 1], rr[4 * k + 2], rr[4 * k + 3]);
                         OASR_TMEM_LD32(tl + colg + 32 * c + 32, rr);
                         tmem_wait_ld();
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
-                            *reinterpret_cast<uint4*>(stg + 32 + 4 * k) =
-                                make_uint4(rr[4 * k], rr[4 * k + 1], rr[4 * k + 2], rr[4 * k + 3]);
+                            if (32 + 4 * k <= 62 - lane)
+                                *reinterpret_cast<uint4*>(stg + 32 + 4 * k) =
+                                    make_uint4(rr[4 * k], rr[4 * k + 1], rr[4 * k + 2], rr[4 * k + 3]);
                         __syncwarp();
 #pragma unroll
                         for (int j = 0; j < 32; ++j) sc[32 * c + j] += stg[31 - lane + j];
@@ -653,8 +671,9 @@ oasr_status launch_packed_tc(const void* q, const void* k, const void* v, const 
                              float scale, int cs, int left, cudaStream_t stream)
 {
     if (num_seqs > kTcMaxSeqs) return OASR_ERR_UNSUPPORTED;
-    CUtensorMap tm_k, tm_v, tm_r;
-    if (!encode_rows_bf16(&tm_k, k, total, H, kBN) || !encode_rows_bf16(&tm_v, v, total, H, kBN) ||
+    CUtensorMap tm_q, tm_k, tm_v, tm_r;
+    if (!encode_rows_bf16(&tm_q, q, total, H, kBM) || !encode_rows_bf16(&tm_k, k, total, H, kBN) ||
+        !encode_rows_bf16(&tm_v, v, total, H, kBN) ||
         !encode_rows_bf16(&tm_r, rel, R, H, kBand))
         return OASR_ERR_INVALID_ARG;
     unsigned* status = status_word();
@@ -684,7 +703,7 @@ oasr_status launch_packed_tc(const void* q, const void* k, const void* v, const 
     a.scale_log2 = scale * 1.4426950408889634f;
     const long long items_bound = ((static_cast<long long>(total) + kBM - 1) / kBM + num_seqs) * H;
     const int grid = static_cast<int>(items_bound < sms ? items_bound : sms);
-    kern<<<grid, kTcThreads, smem, stream>>>(tm_k, tm_v, tm_r, a);
+    kern<<<grid, kTcThreads, smem, stream>>>(tm_q, tm_k, tm_v, tm_r, a);
     return launch_status();
 }
 
