@@ -379,41 +379,63 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 umma_commit(bar_sg_full);
                 ++sg;
             };
-            bool ok = true;
-            for (long long item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+            // One flat walk over the CTA's stages.  The S/G of the next stage, which may be
+            // the next item's first, is issued as soon as this stage's S/G have been read,
+            // so it overlaps this stage's softmax, and across items the next tile's first
+            // products overlap the current tile's last stage and epilogue.
+            long long item = blockIdx.x;
+            int n_st = 0, s = 0;
+            auto item_stages = [&](long long itm) {
                 int start, L, i0, h, kl, kh;
-                decode(item, start, L, i0, h, kl, kh);
-                const int n_st = (kh - kl + kBN - 1) / kBN;
-                // stage 0 needs this item's q tiles, its slot, and S/G read out
-                ok = wait_or_abort(bar_q_ready, it & 1, s_abort) &&
-                     wait_or_abort(bar_full + 8 * (g & 1), (g >> 1) & 1, s_abort) &&
-                     (sg == 0 || wait_or_abort(bar_sg_free, (sg - 1) & 1, s_abort));
-                if (!ok) break;
-                issue_sg(g & 1);
-                if (n_st == 1) { umma_commit(bar_q_free); ++nq; }
-                for (int s = 0; s < n_st; ++s) {
-                    const int gs = g + s;
-                    if (s + 1 < n_st) {
-                        // S/G of the next stage overlap this stage's softmax
-                        ok = wait_or_abort(bar_full + 8 * ((gs + 1) & 1), ((gs + 1) >> 1) & 1, s_abort) &&
-                             wait_or_abort(bar_sg_free, (sg - 1) & 1, s_abort);
-                        if (!ok) break;
-                        issue_sg((gs + 1) & 1);
-                        if (s + 2 == n_st) { umma_commit(bar_q_free); ++nq; }
-                    }
-                    ok = wait_or_abort(bar_p_full, gs & 1, s_abort);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t vbase = sb + SP::off_slot + (gs & 1) * SP::slot + SP::off_v;
-#pragma unroll
-                    for (int k = 0; k < kBN / 16; ++k)
-                        umma_ts(tmem + kColO, tmem + kColP + 8 * k, sdesc(vbase + 2048 * k), id_o,
-                                (s > 0 || k > 0) ? 1 : 0);
-                    umma_commit(bar_pv_done);
-                    umma_commit(bar_empty + 8 * (gs & 1));
-                    ++npv;
+                decode(itm, start, L, i0, h, kl, kh);
+                return (kh - kl + kBN - 1) / kBN;
+            };
+            bool ok = item < n_items;
+            if (ok) {
+                n_st = item_stages(item);
+                ok = wait_or_abort(bar_q_ready, 0, s_abort) &&
+                     wait_or_abort(bar_full, 0, s_abort);
+                if (ok) {
+                    issue_sg(0);
+                    if (n_st == 1) { umma_commit(bar_q_free); ++nq; }
                 }
-                g += n_st;
+            }
+            while (ok) {
+                // the stage after g: this item's next one, or the next item's first
+                const bool last = s + 1 == n_st;
+                const long long next_item = last ? item + gridDim.x : item;
+                if (next_item < n_items) {
+                    const int next_n = last ? item_stages(next_item) : n_st;
+                    const int next_s = last ? 0 : s + 1;
+                    ok = (!last || wait_or_abort(bar_q_ready, (it + 1) & 1, s_abort)) &&
+                         wait_or_abort(bar_full + 8 * ((g + 1) & 1), ((g + 1) >> 1) & 1, s_abort) &&
+                         wait_or_abort(bar_sg_free, (sg - 1) & 1, s_abort);
+                    if (!ok) break;
+                    issue_sg((g + 1) & 1);
+                    if (next_s + 1 == next_n) { umma_commit(bar_q_free); ++nq; }
+                }
+                // P.V of stage g
+                ok = wait_or_abort(bar_p_full, g & 1, s_abort);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t vbase = sb + SP::off_slot + (g & 1) * SP::slot + SP::off_v;
+#pragma unroll
+                for (int k = 0; k < kBN / 16; ++k)
+                    umma_ts(tmem + kColO, tmem + kColP + 8 * k, sdesc(vbase + 2048 * k), id_o,
+                            (s > 0 || k > 0) ? 1 : 0);
+                umma_commit(bar_pv_done);
+                umma_commit(bar_empty + 8 * (g & 1));
+                ++npv;
+                ++g;
+                if (!last) {
+                    ++s;
+                } else {
+                    item = next_item;
+                    ++it;
+                    if (item >= n_items) break;
+                    n_st = item_stages(item);
+                    s = 0;
+                }
             }
             // drain: every MMA issued has finished and every arrival it owes has landed
             umma_commit(bar_drain);
@@ -445,42 +467,49 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             ++nx;
             return true;
         };
+        // bf16(q+u) and bf16(q+v) of item number itq (head hq): this thread's half row, from
+        // the q rows the TMA warp staged; the caller has made sure the MMAs of the previous
+        // item no longer read the Qu/Qv tiles
+        auto prep_q = [&](int itq, int hq) {
+            if (!warp_wait(bar_qb_full, itq & 1)) return false;
+            const uint4* up = reinterpret_cast<const uint4*>(a.pos_bias_u + hq * kHeadDim);
+            const uint4* vp = reinterpret_cast<const uint4*>(a.pos_bias_v + hq * kHeadDim);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int c = 4 * hf + cc;
+                const uint32_t offs = static_cast<uint32_t>(r * kRowBytes + ((c ^ (r & 7)) << 4));
+                const uint4 qc = *reinterpret_cast<const uint4*>(sm + SP::off_qbuf + offs);
+                const uint4 uc = __ldg(up + c), vc = __ldg(vp + c);
+                const uint32_t w[4] = {qc.x, qc.y, qc.z, qc.w};
+                const uint32_t wu[4] = {uc.x, uc.y, uc.z, uc.w};
+                const uint32_t wv[4] = {vc.x, vc.y, vc.z, vc.w};
+                uint32_t ou[4], ov[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+                    ou[e] = pack_bf16(lo + __uint_as_float(wu[e] << 16), hi + __uint_as_float(wu[e] & 0xffff0000u));
+                    ov[e] = pack_bf16(lo + __uint_as_float(wv[e] << 16), hi + __uint_as_float(wv[e] & 0xffff0000u));
+                }
+                *reinterpret_cast<uint4*>(sm + SP::off_qu + offs) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+                *reinterpret_cast<uint4*>(sm + SP::off_qv + offs) = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_qb_free);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_q_ready);
+            return true;
+        };
         int g = 0, it = 0, sg = 0;
-        for (long long item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+        if (static_cast<long long>(blockIdx.x) < n_items) {
+            int st0, L0, i00, h0, kl0, kh0;
+            decode(blockIdx.x, st0, L0, i00, h0, kl0, kh0);
+            if (!prep_q(0, h0)) *s_abort = 1;
+        }
+        for (long long item = blockIdx.x; item < n_items && !*s_abort; item += gridDim.x, ++it) {
             int start, L, i0, h, kl, kh;
             decode(item, start, L, i0, h, kl, kh);
             const int n_st = (kh - kl + kBN - 1) / kBN;
-            // bf16(q+u) and bf16(q+v): this thread's half row, once the previous item's S/G are done
-            if (it > 0 && !warp_wait(bar_q_free, (it - 1) & 1)) break;
-            if (!warp_wait(bar_qb_full, it & 1)) break;
-            {
-                const uint4* up = reinterpret_cast<const uint4*>(a.pos_bias_u + h * kHeadDim);
-                const uint4* vp = reinterpret_cast<const uint4*>(a.pos_bias_v + h * kHeadDim);
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int c = 4 * hf + cc;
-                    const uint32_t offs = static_cast<uint32_t>(r * kRowBytes + ((c ^ (r & 7)) << 4));
-                    const uint4 qc = *reinterpret_cast<const uint4*>(sm + SP::off_qbuf + offs);
-                    const uint4 uc = __ldg(up + c), vc = __ldg(vp + c);
-                    const uint32_t w[4] = {qc.x, qc.y, qc.z, qc.w};
-                    const uint32_t wu[4] = {uc.x, uc.y, uc.z, uc.w};
-                    const uint32_t wv[4] = {vc.x, vc.y, vc.z, vc.w};
-                    uint32_t ou[4], ov[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
-                        ou[e] = pack_bf16(lo + __uint_as_float(wu[e] << 16), hi + __uint_as_float(wu[e] & 0xffff0000u));
-                        ov[e] = pack_bf16(lo + __uint_as_float(wv[e] << 16), hi + __uint_as_float(wv[e] & 0xffff0000u));
-                    }
-                    *reinterpret_cast<uint4*>(sm + SP::off_qu + offs) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
-                    *reinterpret_cast<uint4*>(sm + SP::off_qv + offs) = make_uint4(ov[0], ov[1], ov[2], ov[3]);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_qb_free);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_q_ready);
-            }
             float m_used = -INFINITY, l_sum = 0.f;
             bool ok = true;
             for (int s = 0; s < n_st; ++s, ++g) {
@@ -536,6 +565,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_sg_free);
+                // last stage of the item: the next item's Qu/Qv, so that its first S/G can be
+                // issued while this stage's softmax and the epilogue run
+                if (s + 1 == n_st && item + gridDim.x < n_items) {
+                    int ns1, nL, ni0, nh, nkl, nkh;
+                    decode(item + gridDim.x, ns1, nL, ni0, nh, nkl, nkh);
+                    if (!warp_wait(bar_q_free, it & 1) || !prep_q(it + 1, nh)) { ok = false; break; }
+                }
                 // scale (log2 domain), mask keys this row does not see, this half's max:
                 // the half holds keys jh .. jh+63; row r sees [ka, kb) of them
                 const int jh = kl + s * kBN + 64 * hf;
