@@ -144,48 +144,45 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         return left < kStageKeys ? left : kStageKeys;
     };
 
-    // Stage s into slot s % NS (producer lane only).
+    // Stage s into slot s % NS, by the whole producer warp: lane q issues the K and V boxes
+    // of the stage's q-th page (or 16-row piece of the chunk), lane 0 the band box, so a
+    // stage's boxes go out in one instruction rather than one after another.
     auto issue = [&](int s) {
         const int slot = s % NS;
         const uint32_t bar = bar_full + 8 * slot;
         const uint32_t base = sb + SP::off_slots + slot * SP::kSlot;
         const int j0 = stage_j0(s);
-        if (direct && s == 0) {
-            // the chunk's own rows: boxes of 16 rows of k_new / v_new (rows past T are masked)
-            const int nb = (T + 15) / 16;
-            mbar_arrive_expect_tx(bar, static_cast<uint32_t>((2 * nb * 16 + TL::RB) * kRowBytes));
-            for (int q = 0; q < nb; ++q) {
-                tma_load_3d(base + q * 16 * kRowBytes, &tm_kn, bar, 0, h, b * T + 16 * q);
-                tma_load_3d(base + (kStageKeys + 16 * q) * kRowBytes, &tm_vn, bar, 0, h, b * T + 16 * q);
-            }
-            tma_load_3d(base + 2 * kStageKeys * kRowBytes, &tm_r, bar, 0, h, off + j0 - (TL::Tp - 1));
-            return;
-        }
-        const int box = a.box_rows;
-        int rows[kStageKeys / 8];
-        int nbox = 0;
-        for (int q = 0; q < kStageKeys / box; ++q) {
-            const int j = j0 + q * box;
-            if (j >= kc) break;
-            const int lb = j / a.block_size;
-            const int slot_in_block = j - lb * a.block_size;
-            const int blk = s_bt[lb];
-            if (blk < 0 || blk >= a.num_blocks) {
-                err |= kErrBounds;
-                rows[nbox++] = -2 * box;   // outside the pool: the box reads zeros
+        const bool chunk = direct && s == 0;
+        const int box = chunk ? 16 : a.box_rows;
+        const int nbox = chunk ? (T + 15) / 16
+                               : min(kStageKeys / box, (kc - j0 + box - 1) / box);
+        if (lane == 0)
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>((2 * nbox * box + TL::RB) * kRowBytes));
+        __syncwarp();
+        if (lane < nbox) {
+            const uint32_t dk = base + lane * box * kRowBytes;
+            const uint32_t dv = dk + kStageKeys * kRowBytes;
+            if (chunk) {
+                tma_load_3d(dk, &tm_kn, bar, 0, h, b * T + 16 * lane);
+                tma_load_3d(dv, &tm_vn, bar, 0, h, b * T + 16 * lane);
             } else {
-                rows[nbox++] = blk * a.block_size + slot_in_block;
+                const int j = j0 + lane * box;
+                const int lb = j / a.block_size;
+                const int blk = s_bt[lb];
+                int row;
+                if (blk < 0 || blk >= a.num_blocks) {
+                    err |= kErrBounds;
+                    row = -2 * box;   // outside the pool: the box reads zeros
+                } else {
+                    row = blk * a.block_size + (j - lb * a.block_size);
+                }
+                const uint64_t pol = policy_evict_first();
+                tma_load_3d_hint(dk, &tm_k, bar, 0, h, row, pol);
+                tma_load_3d_hint(dv, &tm_v, bar, 0, h, row, pol);
             }
         }
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>((2 * nbox * box + TL::RB) * kRowBytes));
-        const uint64_t pol = policy_evict_first();
-        for (int q = 0; q < nbox; ++q) {
-            tma_load_3d_hint(base + q * box * kRowBytes, &tm_k, bar, 0, h, rows[q], pol);
-            tma_load_3d_hint(base + kStageKeys * kRowBytes + q * box * kRowBytes, &tm_v, bar, 0,
-                             h, rows[q], pol);
-        }
-        tma_load_3d(base + 2 * kStageKeys * kRowBytes, &tm_r, bar, 0, h,
-                    off + j0 - (TL::Tp - 1));
+        if (lane == 0)
+            tma_load_3d(base + 2 * kStageKeys * kRowBytes, &tm_r, bar, 0, h, off + j0 - (TL::Tp - 1));
     };
 
     const bool producer = warp == kConsumerWarps;
@@ -201,20 +198,18 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
             }
             mbar_arrive_expect_tx(bar_q, TL::Tp * kRowBytes);
             tma_load_3d(sb + SP::off_q, &tm_q, bar_q, 0, h, b * T);
-            // without the direct chunk stage, stages from this one on hold chunk rows
-            const int first_chunk_stage = (FUSED && !direct) ? C / kStageKeys : n_stages;
-            for (int issued = 0; issued < n_stages; ++issued) {
-                const int slot = issued % NS;
-                if (issued >= NS && !mbar_wait(bar_empty + 8 * slot, ((issued / NS) - 1) & 1)) {
-                    err |= kErrTimeout;
-                    break;
-                }
-                if (issued == first_chunk_stage && !mbar_wait(bar_written, 0)) {
-                    err |= kErrTimeout;
-                    break;
-                }
-                issue(issued);
+        }
+        // without the direct chunk stage, stages from this one on hold chunk rows
+        const int first_chunk_stage = (FUSED && !direct) ? C / kStageKeys : n_stages;
+        for (int issued = 0; issued < n_stages; ++issued) {
+            const int slot = issued % NS;
+            bool ok = issued < NS || mbar_wait(bar_empty + 8 * slot, ((issued / NS) - 1) & 1);
+            if (ok && issued == first_chunk_stage) ok = mbar_wait(bar_written, 0);
+            if (!__all_sync(0xffffffffu, ok)) {
+                err |= kErrTimeout;
+                break;
             }
+            issue(issued);
         }
         if (err) atomicOr(a.status, err);
         return;
