@@ -209,6 +209,41 @@ def test_invalid_block_id_is_flagged_and_contained():
         check_close(got[b], ref[b], "bf16", f"stream {b}")
 
 
+@pytest.mark.parametrize("C,T,bad_page", [(40, 8, 2), (44, 8, 3), (44, 8, 2), (0, 16, 0)],
+                         ids=lambda v: str(v))
+def test_fused_step_with_an_invalid_chunk_page(C, T, bad_page):
+    """A chunk page that names no valid block: the fused step falls back to writing the
+    chunk, fencing it and reading it from the pool; the rows of that page read as zeros
+    (and are not written), everything else is exact."""
+    cfg = syn.StreamingConfig("badchunk", B=3, H=2, D=64, T=T, C=C, block_size=16, dtype="bf16",
+                              seed=12)
+    x = stream_case(cfg)
+    bt = x["block_table"].copy()
+    bt[1, bad_page] = cfg.pool_blocks + 7
+    d = gpu_stream_inputs(x, "bf16")
+    d["block_table"] = torch.from_numpy(bt).cuda()
+    out = capi.oasr_chunk_step_paged(d["q"], d["k_new"], d["v_new"], d["k_pool"], d["v_pool"],
+                                     d["block_table"], d["cache_seqlens"], d["pos_bias_u"],
+                                     d["pos_bias_v"], d["rel"])
+    torch.cuda.synchronize()
+    assert capi.oasr_device_status() & capi.STATUS_BOUNDS_BIT
+    got = to_np(out)
+    ref = oracle_chunk(x)
+    for b in (0, 2):
+        check_close(got[b], ref[b], "bf16", f"stream {b}")
+    # stream 1: every key in the bad page (cached or chunk) is a zero key and value
+    x1 = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in x.items()}
+    for p in range(C + T):
+        if p // cfg.block_size == bad_page:
+            if p < C:
+                x1["cache_k"][1, p] = 0
+                x1["cache_v"][1, p] = 0
+            else:
+                x1["k_new"][1, p - C] = 0
+                x1["v_new"][1, p - C] = 0
+    check_close(got[1], oracle_chunk(x1)[1], "bf16", "stream 1 (bad chunk page)")
+
+
 # ----------------------------------------------------------------------- packed
 
 
