@@ -41,6 +41,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+from paged_kv_chunk_gb300 import dist as pdist  # noqa: E402
 from paged_kv_chunk_gb300 import synthetic as syn  # noqa: E402
 
 METRIC = "encoder frames/s per attention layer and achieved HBM GB/s vs GB300 peak"
@@ -213,31 +214,15 @@ class ClockSampler:
 
 
 def dist_setup():
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    elif torch.cuda.is_available():
-        torch.cuda.set_device(0)
-    return rank, world, local
+    return pdist.setup()
 
 
 def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    pdist.barrier()
 
 
 def max_over_ranks(x, world):
-    if world == 1:
-        return x
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    return pdist.max_over_ranks(x)
 
 
 # ------------------------------------------------------------------ CPU oracle legs
