@@ -22,6 +22,10 @@ Sources (OASR documentation pages):
     commits the cache length after the step.
   * ASR Engine page, section 4.1: packed micro-batches are one gapless
     varlen-attention row.
+  * ASR Engine page, KV-pool sizing paragraphs: an encoder with a trained attention
+    window pages by chunk and retains ceil(window / chunk) + 1 pages per stream; with
+    history eviction the cached length is held at the window (window_commit below,
+    plain Python index bookkeeping).
 
 Parity pins (what ties this oracle to something other than itself) live in
 ``tests/test_oracle_pins.py``; every function here is pinned.
@@ -248,3 +252,36 @@ def packed_relattn_chunked(q, k, v, cu_seqlens, pos_bias_u, pos_bias_v, rel, chu
     if bad:
         raise ValueError(f"{bad} rows need rel rows outside [0, {R}) or lie in no segment")
     return out
+
+
+def window_pages(window_frames: int, chunk_frames: int) -> int:
+    """Pages a stream retains with a trained window when it pages by chunk:
+    ceil(window / chunk) + 1 (the history plus the chunk being appended)."""
+    if window_frames < 0 or chunk_frames < 1:
+        raise ValueError("window_frames >= 0 and chunk_frames >= 1 required")
+    return -(-window_frames // chunk_frames) + 1
+
+
+def window_commit(block_table, cache_seqlens, T: int, block_size: int, window_frames: int):
+    """Commit a step's chunk with history eviction, per stream (the caller-side commit of the
+    ASR Engine page, section 4.3, plus the eviction that holds a trained window).
+
+    After the chunk the stream holds n = cache_seqlens[b] + T frames in its first
+    P = ceil(n / block_size) pages.  If n exceeds window_frames, the oldest
+    d = ceil((n - window_frames) / block_size) pages are dropped: the first P entries of the
+    row are rotated left by d, so the dropped blocks become the next pages to be written, and
+    the cached length becomes n - d * block_size.  Otherwise the cached length becomes n.
+    Entries past the first P are left alone.  Returns new (block_table, cache_seqlens).
+    """
+    bt = np.array(block_table, dtype=np.int32, copy=True)
+    cs = np.array(cache_seqlens, dtype=np.int32, copy=True)
+    for b in range(bt.shape[0]):
+        n = int(cs[b]) + T
+        P = -(-n // block_size)
+        d = 0
+        if n > window_frames:
+            d = -(-(n - window_frames) // block_size)
+        row = list(bt[b, :P])
+        bt[b, :P] = row[d:] + row[:d]
+        cs[b] = n - d * block_size
+    return bt, cs

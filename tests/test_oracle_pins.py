@@ -490,3 +490,55 @@ def test_chunked_rows_equal_a_streaming_step(cs, left):
                                     c["k"][None, i0:i1], c["v"][None, i0:i1], c["pos_bias_u"],
                                     c["pos_bias_v"], rel_s)
         np.testing.assert_allclose(out[i0:i1], step[0], rtol=0, atol=1e-13)
+
+
+# --------------------------------------------------------- fixed-window ring (eviction)
+
+
+def test_window_pages_matches_the_pages_sizing():
+    # "ceil(window / chunk_size) + 1 pages"; the pages' 32-stream pool of 160 pages is 5 per
+    # stream, which a 4-chunk window gives
+    assert oracle.window_pages(64, 16) == 5
+    assert oracle.window_pages(56, 8) == 8
+    assert oracle.window_pages(50, 16) == 5
+    assert oracle.window_pages(0, 16) == 1
+
+
+def test_window_commit_hand_worked():
+    # block_size 4, window 8 frames, chunk T = 4
+    bt = np.array([[10, 11, 12, 13],     # C = 8: n = 12 > 8 -> drop 1 page, C = 8
+                   [20, 21, 22, 23],     # C = 4: n = 8 <= 8 -> C = 8, no rotation
+                   [30, 31, 32, 33],     # C = 0: n = 4 -> C = 4
+                   [40, 41, 42, 43]], np.int32)
+    cs = np.array([8, 4, 0, 6], np.int32)  # C = 6: n = 10 > 8 -> d = 1 (P = 3), C = 6
+    bt2, cs2 = oracle.window_commit(bt, cs, T=4, block_size=4, window_frames=8)
+    np.testing.assert_array_equal(cs2, [8, 8, 4, 6])
+    np.testing.assert_array_equal(bt2, [[11, 12, 10, 13],
+                                        [20, 21, 22, 23],
+                                        [30, 31, 32, 33],
+                                        [41, 42, 40, 43]])
+
+
+@pytest.mark.parametrize("bs,T,window", [(16, 16, 64), (8, 16, 40), (16, 8, 48), (4, 12, 20)])
+def test_window_commit_keeps_the_latest_frames_in_order(bs, T, window):
+    """Track frame numbers through the paging for many steps: after every commit the cached
+    frames are exactly the most recent ones, oldest first, and no block is lost."""
+    B, steps = 3, 12
+    pages = -(-(window + T) // bs) + 1
+    bt = np.arange(B * pages, dtype=np.int32).reshape(B, pages)
+    cs = np.zeros(B, np.int32)
+    slots = {}           # (block, slot) -> frame number
+    frame = np.zeros(B, np.int64)
+    for _ in range(steps):
+        for b in range(B):
+            for t in range(T):
+                p = cs[b] + t
+                slots[(int(bt[b, p // bs]), p % bs)] = frame[b] + t
+            frame[b] += T
+        bt2, cs2 = oracle.window_commit(bt, cs, T, bs, window)
+        for b in range(B):
+            assert sorted(bt2[b]) == sorted(bt[b])
+            assert cs2[b] <= window and cs2[b] >= min(frame[b], window) - bs + 1
+            seen = [slots[(int(bt2[b, p // bs]), p % bs)] for p in range(cs2[b])]
+            assert seen == list(range(frame[b] - cs2[b], frame[b]))
+        bt, cs = bt2, cs2
