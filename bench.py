@@ -335,6 +335,9 @@ def run_ours(args, cfg, rank, world, local):
             else:
                 capi.oasr_chunk_step_paged(x[l, 0], x[l, 1], x[l, 2], kp, vp, bt, cs, u, vb, rel,
                                            out=out[l])
+        if cfg.window:
+            # the step's commit: the block table is shared by the layers, so once per step
+            capi.oasr_window_commit(bt, cs, T, bs, cfg.window)
 
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
@@ -420,6 +423,8 @@ def run_ours(args, cfg, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
         "config": {"workload": f"{cfg.name}_streaming", "B": B, "H": H, "D": D, "T": T,
+                   **({"window_frames": cfg.window, "commit": "oasr_window_commit once per step"}
+                      if cfg.window else {}),
                    "cache": cfg.C, "block_size": bs, "pool_blocks": nb, "rel_rows": cfg.R,
                    "layers": layers, "global_batch": B * world, "seq_len": cfg.K,
                    "parallelism": f"dp{world}",
@@ -433,7 +438,7 @@ def run_ours(args, cfg, rank, world, local):
                                 else "chunk_attn_bf16_kernel (fused append + attention)"),
                      "algorithmic_bytes_per_launch": touched,
                      "avg_launch_us": launch_us, "peak_kind": peak_kind},
-        "gpu_launches": args.steps * layers * (2 if args.two_call else 1),
+        "gpu_launches": args.steps * (layers * (2 if args.two_call else 1) + (1 if cfg.window else 0)),
         "clocks": clocks,
     }
     if e2e:

@@ -165,6 +165,28 @@ oasr_status oasr_packed_relattn_chunked(const void* q, const void* k, const void
                                         int H, int D, float scale, int chunk_size,
                                         int left_chunks, oasr_dtype dt, cudaStream_t stream);
 
+/*
+ * Commit a streaming step with fixed-window history eviction (ASR Engine page, KV-pool sizing
+ * paragraphs: an encoder with a trained attention window pages by chunk and retains
+ * ceil(window / chunk) + 1 pages per stream; with eviction the cached length is held at the
+ * window; section 4.3: the caller commits the cache length after the step).
+ *
+ * For every stream b, after a chunk of T frames was appended at cache_seqlens[b], the stream
+ * holds n = cache_seqlens[b] + T frames in its first P = ceil(n / block_size) pages.  If
+ * n > window_frames, the oldest d = ceil((n - window_frames) / block_size) pages are dropped:
+ * block_table[b][0 .. P) is rotated left by d, so the dropped blocks become the next pages to
+ * be written, and cache_seqlens[b] becomes n - d * block_size; otherwise cache_seqlens[b]
+ * becomes n.  Entries past the first P are untouched.  Both arrays are device memory and are
+ * updated in place on `stream`, so a captured step stays replayable.
+ *
+ * Requirements: B >= 1; 1 <= max_blocks_per_seq <= 512 (else OASR_ERR_UNSUPPORTED);
+ * block_size >= 1; T >= 0; window_frames >= 0.  A negative cache length or a row that would
+ * run past the table raises OASR_ERR_BOUNDS in the device status word and is clamped.
+ */
+oasr_status oasr_window_commit(int32_t* block_table, int32_t* cache_seqlens, int B,
+                               int max_blocks_per_seq, int block_size, int T, int window_frames,
+                               cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* oasr_status_string(oasr_status status);
 

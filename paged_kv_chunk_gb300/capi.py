@@ -53,8 +53,10 @@ def load() -> ctypes.CDLL:
         L.oasr_packed_relattn_varlen.argtypes = [P, P, P, P, I, I, I, P, P, P, I, P, I, I, F, I, S]
         L.oasr_packed_relattn_chunked.argtypes = [P, P, P, P, I, I, I, P, P, P, I, P, I, I, F, I, I,
                                                   I, S]
+        L.oasr_window_commit.argtypes = [P, P, I, I, I, I, I, S]
         for fn in ("oasr_paged_append", "oasr_chunk_relattn_paged", "oasr_chunk_step_paged",
-                   "oasr_packed_relattn_varlen", "oasr_packed_relattn_chunked"):
+                   "oasr_packed_relattn_varlen", "oasr_packed_relattn_chunked",
+                   "oasr_window_commit"):
             getattr(L, fn).restype = I
         L.oasr_status_string.argtypes = [I]
         L.oasr_status_string.restype = ctypes.c_char_p
@@ -227,6 +229,18 @@ def oasr_packed_relattn_chunked(q, k, v, cu_seqlens, max_seqlen, pos_bias_u, pos
         _dev(rel, "rel", q.dtype), rel.shape[0], _dev(out, "out", q.dtype), H, D, scale,
         int(chunk_size), int(left_chunks), dt, _stream(stream)))
     return out
+
+
+def oasr_window_commit(block_table, cache_seqlens, T, block_size, window_frames, stream=None):
+    """Commit a step's chunk with fixed-window history eviction, in place on the device:
+    rotates each full stream's block-table row and advances cache_seqlens."""
+    L = load()
+    if block_table.dim() != 2 or cache_seqlens.dim() != 1 or cache_seqlens.shape[0] != block_table.shape[0]:
+        raise ValueError("block_table must be [B, max_blocks_per_seq] and cache_seqlens [B]")
+    B, mbps = block_table.shape
+    _check("oasr_window_commit", L.oasr_window_commit(
+        _dev(block_table, "block_table", torch.int32, 2), _dev(cache_seqlens, "cache_seqlens", torch.int32, 1),
+        B, mbps, int(block_size), int(T), int(window_frames), _stream(stream)))
 
 
 def oasr_device_status(clear: bool = True) -> int:

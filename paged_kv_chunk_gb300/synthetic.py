@@ -35,6 +35,7 @@ class StreamingConfig:
     seed: int
     num_blocks: int | None = None          # default: twice the demand
     max_blocks_per_seq: int | None = None  # default: pages needed for C + T keys
+    window: int = 0                        # > 0: trained window (frames); steps commit with eviction
 
     @property
     def K(self) -> int:
@@ -87,7 +88,13 @@ SWEEP = tuple(StreamingConfig(f"sweep_T{T}", B=128, H=8, D=64, T=T, C=16 * T, bl
 PACKED = PackedConfig("packed_varlen", num_seqs=256, min_len=50, max_len=1500, H=8, D=64,
                       dtype="bf16", seed=1004)
 
-STREAMING_CONFIGS = {c.name: c for c in (TINY, SMALL, LARGE) + SWEEP}
+# A trained-window cohort paged by chunk (the pages' Nemotron sizing: 32 streams, 5 pages of
+# one 16-frame chunk each, i.e. a 64-frame window plus the chunk being appended); every step
+# commits with eviction, so the cache length stays at the window.
+WINDOW_RING = StreamingConfig("window_ring", B=32, H=8, D=64, T=16, C=64, block_size=16,
+                              dtype="bf16", seed=1010, window=64)
+
+STREAMING_CONFIGS = {c.name: c for c in (TINY, SMALL, LARGE, WINDOW_RING) + SWEEP}
 
 
 def round_to(x: np.ndarray, dtype: str) -> np.ndarray:

@@ -16,7 +16,8 @@ def lib():
 def test_exports_every_header_symbol(lib):
     names = capi.header_symbols()
     assert {"oasr_paged_append", "oasr_chunk_relattn_paged", "oasr_chunk_step_paged",
-            "oasr_packed_relattn_varlen", "oasr_packed_relattn_chunked", "oasr_status_string",
+            "oasr_packed_relattn_varlen", "oasr_packed_relattn_chunked", "oasr_window_commit",
+            "oasr_status_string",
             "oasr_device_status",
             "oasr_version"} <= set(names)
     for n in names:
@@ -118,6 +119,22 @@ def test_chunked_rejects_bad_arguments(lib, args, expect):
                                         a["total"], a["u"], a["vb"], a["rel"], a["R"], a["out"],
                                         a["H"], a["D"], 0.125, a["cs"], a["left"], a["dt"], None)
     assert r == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    (dict(bt=None), capi.OASR_ERR_INVALID_ARG),
+    (dict(cs=None), capi.OASR_ERR_INVALID_ARG),
+    (dict(B=0), capi.OASR_ERR_INVALID_ARG),
+    (dict(bs=0), capi.OASR_ERR_INVALID_ARG),
+    (dict(T=-1), capi.OASR_ERR_INVALID_ARG),
+    (dict(window=-1), capi.OASR_ERR_INVALID_ARG),
+    (dict(mbps=513), capi.OASR_ERR_UNSUPPORTED),
+])
+def test_window_commit_rejects_bad_arguments(lib, args, expect):
+    a = dict(bt=FAKE, cs=FAKE, B=4, mbps=8, bs=16, T=16, window=64)
+    a.update(args)
+    assert lib.oasr_window_commit(a["bt"], a["cs"], a["B"], a["mbps"], a["bs"], a["T"], a["window"],
+                                  None) == expect
 
 
 def test_device_status_needs_pointer(lib):

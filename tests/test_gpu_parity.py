@@ -494,3 +494,61 @@ def test_chunked_full_size_sampled():
     got = to_np(out)
     check_close(got[rows[:, 0], rows[:, 1]], ref[rows[:, 0], rows[:, 1]], cfg.dtype, "chunked full")
     assert capi.oasr_device_status() == 0
+
+
+# --------------------------------------------------------- fixed-window ring (eviction)
+
+
+@pytest.mark.parametrize("bs,T,window,mbps", [(16, 16, 64, 12), (8, 16, 40, 20), (4, 12, 20, 40)],
+                         ids=str)
+def test_window_commit_matches_oracle(bs, T, window, mbps):
+    rng = np.random.default_rng(bs * 100 + T)
+    B = 37
+    bt = np.stack([rng.permutation(1000)[:mbps] for _ in range(B)]).astype(np.int32)
+    cs = rng.integers(0, mbps * bs - T + 1, size=B).astype(np.int32)
+    cs[:3] = [0, window, window - T]
+    d_bt = torch.from_numpy(bt).cuda()
+    d_cs = torch.from_numpy(cs).cuda()
+    capi.oasr_window_commit(d_bt, d_cs, T, bs, window)
+    torch.cuda.synchronize()
+    ref_bt, ref_cs = oracle.window_commit(bt, cs, T, bs, window)
+    np.testing.assert_array_equal(d_bt.cpu().numpy(), ref_bt)
+    np.testing.assert_array_equal(d_cs.cpu().numpy(), ref_cs)
+    assert capi.oasr_device_status() == 0
+
+
+@pytest.mark.parametrize("bs,T,window", [(16, 16, 48), (8, 16, 40), (16, 8, 40)], ids=str)
+def test_window_session_matches_the_sliding_history(bs, T, window):
+    """A stream session under a trained window: every step is one fused append + attention
+    launch followed by the commit with eviction; each step's output equals the oracle over
+    the last cache_seqlens frames of the stream's own history, and the tables follow the
+    oracle's bookkeeping exactly."""
+    B, H, steps = 4, 2, 9
+    rng = np.random.default_rng(bs + T + window)
+    mbps = -(-(window + T) // bs) + 1
+    nblk = B * mbps + 5
+    bt = rng.permutation(nblk)[: B * mbps].reshape(B, mbps).astype(np.int32)
+    cs = np.zeros(B, np.int32)
+    R = window + 2 * T - 1
+    u, vb, rel = (syn.normal(rng, shp, "bf16") for shp in ((H, 64), (H, 64), (R, H, 64)))
+    d = {"u": dev(u, "bf16"), "vb": dev(vb, "bf16"), "rel": dev(rel, "bf16")}
+    kp = dev_pool(syn.canary_pool(nblk, bs, H, 64, "bf16"), "bf16")
+    vp = dev_pool(syn.canary_pool(nblk, bs, H, 64, "bf16"), "bf16")
+    d_bt, d_cs = torch.from_numpy(bt).cuda(), torch.from_numpy(cs).cuda()
+    hk = np.zeros((B, 0, H, 64), np.float32)
+    hv = np.zeros((B, 0, H, 64), np.float32)
+    for _ in range(steps):
+        q, kn, vn = (syn.normal(rng, (B, T, H, 64), "bf16") for _ in range(3))
+        out = capi.oasr_chunk_step_paged(dev(q, "bf16"), dev(kn, "bf16"), dev(vn, "bf16"), kp, vp,
+                                         d_bt, d_cs, d["u"], d["vb"], d["rel"])
+        C = int(cs[0])
+        ref = oracle.chunk_relattn(q, hk[:, hk.shape[1] - C:], hv[:, hv.shape[1] - C:], kn, vn, u, vb, rel)
+        check_close(to_np(out), ref, "bf16", f"window step C={C}")
+        capi.oasr_window_commit(d_bt, d_cs, T, bs, window)
+        bt, cs = oracle.window_commit(bt, cs, T, bs, window)
+        np.testing.assert_array_equal(d_bt.cpu().numpy(), bt)
+        np.testing.assert_array_equal(d_cs.cpu().numpy(), cs)
+        hk = np.concatenate([hk, kn], 1)
+        hv = np.concatenate([hv, vn], 1)
+    assert int(cs[0]) <= window
+    assert capi.oasr_device_status() == 0
