@@ -285,3 +285,28 @@ def window_commit(block_table, cache_seqlens, T: int, block_size: int, window_fr
         bt[b, :P] = row[d:] + row[:d]
         cs[b] = n - d * block_size
     return bt, cs
+
+
+def project_qkv_pos(x, w_qkv, b_qkv, pos_emb, w_pos, H: int):
+    """The projections that feed the path, in float64 (Model Layer page, fixed_attention_window
+    row: one positional projection per step serves the cohort; the Conformer rel-pos attention's
+    linear_q / linear_k / linear_v with bias and linear_pos without, WeNet's layout).
+
+    x: [M, d_model] (M = B*T frames); w_qkv: [3*d_model, d_model] (q rows, then k, then v);
+    b_qkv: [3*d_model]; pos_emb: [R, d_model]; w_pos: [d_model, d_model].
+    Returns q, k, v: [M, H, d_model/H] and rel: [R, H, d_model/H].
+    """
+    x = np.asarray(x, dtype=np.float64)
+    pos_emb = np.asarray(pos_emb, dtype=np.float64)
+    w_qkv = np.asarray(w_qkv, dtype=np.float64)
+    w_pos = np.asarray(w_pos, dtype=np.float64)
+    b_qkv = np.asarray(b_qkv, dtype=np.float64)
+    M, dm = x.shape
+    if w_qkv.shape != (3 * dm, dm) or b_qkv.shape != (3 * dm,) or w_pos.shape != (dm, dm) \
+            or pos_emb.ndim != 2 or pos_emb.shape[1] != dm or dm % H:
+        raise ValueError("shapes: x [M,d], w_qkv [3d,d], b_qkv [3d], pos_emb [R,d], w_pos [d,d]")
+    y = x @ w_qkv.T + b_qkv
+    D = dm // H
+    q, k, v = (y[:, i * dm:(i + 1) * dm].reshape(M, H, D) for i in range(3))
+    rel = (pos_emb @ w_pos.T).reshape(pos_emb.shape[0], H, D)
+    return q, k, v, rel

@@ -542,3 +542,54 @@ def test_window_commit_keeps_the_latest_frames_in_order(bs, T, window):
             seen = [slots[(int(bt2[b, p // bs]), p % bs)] for p in range(cs2[b])]
             assert seen == list(range(frame[b] - cs2[b], frame[b]))
         bt, cs = bt2, cs2
+
+
+# -------------------------------------------------- projections feeding the path
+
+
+def test_projection_hand_worked():
+    # d_model 2, H 1: q/k/v rows of w_qkv and the biases by hand
+    x = np.array([[1.0, 2.0], [0.5, -1.0]])
+    w_qkv = np.array([[1, 0], [0, 1],      # q = x
+                      [1, 1], [1, -1],     # k = (x0 + x1, x0 - x1)
+                      [2, 0], [0, 0]])     # v = (2 x0, 0)
+    b = np.array([0, 0, 1, 0, 0, 3])
+    pos = np.array([[3.0, 4.0]])
+    w_pos = np.array([[0, 1], [1, 0]])     # swaps the two dims
+    q, k, v, rel = oracle.project_qkv_pos(x, w_qkv, b, pos, w_pos, H=1)
+    np.testing.assert_array_equal(q[:, 0], [[1, 2], [0.5, -1]])
+    np.testing.assert_array_equal(k[:, 0], [[4, -1], [0.5, 1.5]])
+    np.testing.assert_array_equal(v[:, 0], [[2, 3], [1, 3]])
+    np.testing.assert_array_equal(rel[:, 0], [[4, 3]])
+
+
+def test_projection_identity_weights_and_head_split():
+    rng = np.random.default_rng(50)
+    M, H, D, R = 5, 3, 4, 7
+    dm = H * D
+    x, pos = rng.standard_normal((M, dm)), rng.standard_normal((R, dm))
+    b = rng.standard_normal(3 * dm)
+    eye = np.eye(dm)
+    q, k, v, rel = oracle.project_qkv_pos(x, np.concatenate([eye, 2 * eye, -eye]), b, pos, eye, H)
+    np.testing.assert_allclose(q.reshape(M, dm), x + b[:dm], atol=1e-15)
+    np.testing.assert_allclose(k.reshape(M, dm), 2 * x + b[dm:2 * dm], atol=1e-15)
+    np.testing.assert_allclose(v.reshape(M, dm), -x + b[2 * dm:], atol=1e-15)
+    np.testing.assert_allclose(rel.reshape(R, dm), pos, atol=1e-15)
+    # head h holds dims [h*D, (h+1)*D)
+    np.testing.assert_array_equal(q[:, 1], (x + b[:dm])[:, D:2 * D])
+
+
+def test_projection_is_affine():
+    rng = np.random.default_rng(51)
+    M, H, D, R = 4, 2, 8, 3
+    dm = H * D
+    w_qkv, w_pos = rng.standard_normal((3 * dm, dm)), rng.standard_normal((dm, dm))
+    b = rng.standard_normal(3 * dm)
+    x1, x2 = rng.standard_normal((M, dm)), rng.standard_normal((M, dm))
+    p1, p2 = rng.standard_normal((R, dm)), rng.standard_normal((R, dm))
+    z = np.zeros(3 * dm)
+    a = oracle.project_qkv_pos(x1 + x2, w_qkv, b, p1 + p2, w_pos, H)
+    s1 = oracle.project_qkv_pos(x1, w_qkv, b, p1, w_pos, H)
+    s2 = oracle.project_qkv_pos(x2, w_qkv, z, p2, w_pos, H)
+    for t, u, w in zip(a, s1, s2):
+        np.testing.assert_allclose(t, u + w, atol=1e-12)
