@@ -59,7 +59,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="conformer_small",
-                    choices=sorted(syn.STREAMING_CONFIGS) + [syn.PACKED.name, NEMOTRON])
+                    choices=sorted(syn.STREAMING_CONFIGS) + [syn.PACKED.name, NEMOTRON]
+                    + sorted(PROJECTIONS))
     ap.add_argument("--two-call", action="store_true",
                     help="time oasr_paged_append + oasr_chunk_relattn_paged instead of the fused step")
     ap.add_argument("--layers", type=int, default=0,
@@ -448,6 +449,97 @@ def run_ours(args, cfg, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+# The projections that feed the path, at the Conformer cohorts' shapes: q/k/v with bias for
+# the B*T frames of a step and the positional projection of the R-row table.
+PROJECTIONS = {"projection_small": dict(B=64, T=16, H=4, R=287, seed=1020),
+               "projection_large": dict(B=256, T=16, H=8, R=543, seed=1021)}
+
+
+def run_projection(args, rank, world, local, name):
+    """One step = the projections of `layers` distinct layers (inputs and weights larger than
+    L2 between steps), one oasr_project_qkv_pos launch per layer, replayed as a CUDA graph."""
+    from paged_kv_chunk_gb300 import build as pkg_build
+    from paged_kv_chunk_gb300 import capi
+    pkg_build.build()
+    capi.load()
+    p = PROJECTIONS[name]
+    B, T, H, R = p["B"], p["T"], p["H"], p["R"]
+    M, d = B * T, 64 * H
+    dev = torch.device("cuda", torch.cuda.current_device())
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(p["seed"] + 7919 * rank)
+    per_layer = 2 * (M * d + 3 * d * d + 3 * d + R * d + d * d + 3 * M * d + R * d)
+    layers = args.layers or max(1, math.ceil(4 * L2_BYTES / per_layer))
+
+    def rnd(shape, sigma):
+        return (torch.randn(shape, generator=gen, device=dev) * sigma).to(torch.bfloat16)
+
+    ins = [(rnd((M, d), syn.SIGMA), rnd((3 * d, d), d ** -0.5), rnd((3 * d,), syn.SIGMA),
+            rnd((R, d), syn.SIGMA), rnd((d, d), d ** -0.5)) for _ in range(layers)]
+    outs = [(torch.empty((M, H, 64), dtype=torch.bfloat16, device=dev),
+             torch.empty((M, H, 64), dtype=torch.bfloat16, device=dev),
+             torch.empty((M, H, 64), dtype=torch.bfloat16, device=dev),
+             torch.empty((R, H, 64), dtype=torch.bfloat16, device=dev)) for _ in range(layers)]
+
+    def step():
+        for l in range(layers):
+            x, wq, bq, pe, wp = ins[l]
+            q, k, v, rel = outs[l]
+            capi.oasr_project_qkv_pos(x, wq, bq, pe, wp, H, q=q, k=k, v=v, rel=rel)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        t_end = time.perf_counter() + args.soak_seconds
+        while time.perf_counter() < t_end:
+            graph.replay()
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    if rank != 0:
+        return
+    per_launch_s = ms / 1e3 / (args.steps * layers)
+    flops = 2.0 * M * 3 * d * d + 2.0 * R * d * d
+    peak, kind = measured_tensor_peak()
+    achieved = flops / per_launch_s / 1e12
+    line = {
+        "metric": METRIC, "value": M * layers * args.steps * world / (ms / 1e3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{name}_qkv_pos", "frames": M, "d_model": d, "H": H, "rel_rows": R,
+                   "layers": layers,
+                   "l2": f"inputs larger than L2: {layers} distinct layers, {layers * per_layer / 1e6:.0f} MB per step",
+                   "timing": "CUDA events around graph replays on the launching stream"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "project_tc_kernel",
+                     "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": per_layer,
+                     "achieved_gbs": per_layer / per_launch_s / 1e9,
+                     "avg_launch_us": per_launch_s * 1e6, "peak_kind": kind},
+        "gpu_launches": args.steps * layers, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_packed(args, rank, world, local, window=None):
     """The offline packed row: one call = one attention layer over all utterances
     (window = (chunk, left) for the chunked-limited Nemotron mask)."""
@@ -527,6 +619,10 @@ def run_packed(args, rank, world, local, window=None):
 
 def main():
     args = parse_args()
+    if args.config in PROJECTIONS:
+        rank, world, local = dist_setup()
+        run_projection(args, rank, world, local, args.config)
+        return
     if args.config in (syn.PACKED.name, NEMOTRON):
         rank, world, local = dist_setup()
         run_packed(args, rank, world, local,

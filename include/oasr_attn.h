@@ -187,6 +187,26 @@ oasr_status oasr_window_commit(int32_t* block_table, int32_t* cache_seqlens, int
                                int max_blocks_per_seq, int block_size, int T, int window_frames,
                                cudaStream_t stream);
 
+/*
+ * The projections that feed the path, in one launch (Model Layer page, fixed_attention_window
+ * row: one positional projection per step serves the cohort; the Conformer rel-pos attention's
+ * linear_q / linear_k / linear_v carry a bias, linear_pos does not):
+ *
+ *   q | k | v = x . w_qkv^T + b_qkv     x [M, d_model], w_qkv [3 d_model, d_model] (q rows,
+ *                                       then k, then v), b_qkv [3 d_model]; q, k, v written as
+ *                                       [M, H, 64] (M = B * T frames: the [B, T, H, 64] inputs of
+ *                                       the attention calls)
+ *   rel       = pos_emb . w_pos^T        pos_emb [R, d_model], w_pos [d_model, d_model]; rel
+ *                                       written as [R, H, 64]
+ *
+ * bf16 in and out, fp32 accumulation, one rounding per output.  Requirements: d_model = 64 H
+ * and a multiple of 128 (else OASR_ERR_UNSUPPORTED); every pointer 16-byte aligned.
+ */
+oasr_status oasr_project_qkv_pos(const void* x, const void* w_qkv, const void* b_qkv,
+                                 const void* pos_emb, const void* w_pos, void* q, void* k, void* v,
+                                 void* rel, int M, int R, int d_model, int H, oasr_dtype dt,
+                                 cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* oasr_status_string(oasr_status status);
 

@@ -54,9 +54,10 @@ def load() -> ctypes.CDLL:
         L.oasr_packed_relattn_chunked.argtypes = [P, P, P, P, I, I, I, P, P, P, I, P, I, I, F, I, I,
                                                   I, S]
         L.oasr_window_commit.argtypes = [P, P, I, I, I, I, I, S]
+        L.oasr_project_qkv_pos.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, S]
         for fn in ("oasr_paged_append", "oasr_chunk_relattn_paged", "oasr_chunk_step_paged",
                    "oasr_packed_relattn_varlen", "oasr_packed_relattn_chunked",
-                   "oasr_window_commit"):
+                   "oasr_window_commit", "oasr_project_qkv_pos"):
             getattr(L, fn).restype = I
         L.oasr_status_string.argtypes = [I]
         L.oasr_status_string.restype = ctypes.c_char_p
@@ -241,6 +242,29 @@ def oasr_window_commit(block_table, cache_seqlens, T, block_size, window_frames,
     _check("oasr_window_commit", L.oasr_window_commit(
         _dev(block_table, "block_table", torch.int32, 2), _dev(cache_seqlens, "cache_seqlens", torch.int32, 1),
         B, mbps, int(block_size), int(T), int(window_frames), _stream(stream)))
+
+
+def oasr_project_qkv_pos(x, w_qkv, b_qkv, pos_emb, w_pos, H, q=None, k=None, v=None, rel=None,
+                         stream=None):
+    """q, k, v = x . w_qkv^T + b_qkv (split in three, [M, H, 64] each) and
+    rel = pos_emb . w_pos^T ([R, H, 64]), bf16, one launch; returns (q, k, v, rel)."""
+    L = load()
+    M, d = x.shape
+    R = pos_emb.shape[0]
+    if tuple(w_qkv.shape) != (3 * d, d) or tuple(b_qkv.shape) != (3 * d,) or \
+            tuple(w_pos.shape) != (d, d) or pos_emb.dim() != 2 or pos_emb.shape[1] != d or d % H:
+        raise ValueError("shapes: x [M,d], w_qkv [3d,d], b_qkv [3d], pos_emb [R,d], w_pos [d,d]")
+    D = d // H
+    q = torch.empty((M, H, D), dtype=x.dtype, device=x.device) if q is None else q
+    k = torch.empty((M, H, D), dtype=x.dtype, device=x.device) if k is None else k
+    v = torch.empty((M, H, D), dtype=x.dtype, device=x.device) if v is None else v
+    rel = torch.empty((R, H, D), dtype=x.dtype, device=x.device) if rel is None else rel
+    _check("oasr_project_qkv_pos", L.oasr_project_qkv_pos(
+        _dev(x, "x", x.dtype, 2), _dev(w_qkv, "w_qkv", x.dtype, 2), _dev(b_qkv, "b_qkv", x.dtype, 1),
+        _dev(pos_emb, "pos_emb", x.dtype, 2), _dev(w_pos, "w_pos", x.dtype, 2),
+        _dev(q, "q", x.dtype), _dev(k, "k", x.dtype), _dev(v, "v", x.dtype), _dev(rel, "rel", x.dtype),
+        M, R, d, H, _dtype_code(x), _stream(stream)))
+    return q, k, v, rel
 
 
 def oasr_device_status(clear: bool = True) -> int:

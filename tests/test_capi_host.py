@@ -17,7 +17,7 @@ def test_exports_every_header_symbol(lib):
     names = capi.header_symbols()
     assert {"oasr_paged_append", "oasr_chunk_relattn_paged", "oasr_chunk_step_paged",
             "oasr_packed_relattn_varlen", "oasr_packed_relattn_chunked", "oasr_window_commit",
-            "oasr_status_string",
+            "oasr_project_qkv_pos", "oasr_status_string",
             "oasr_device_status",
             "oasr_version"} <= set(names)
     for n in names:
@@ -135,6 +135,22 @@ def test_window_commit_rejects_bad_arguments(lib, args, expect):
     a.update(args)
     assert lib.oasr_window_commit(a["bt"], a["cs"], a["B"], a["mbps"], a["bs"], a["T"], a["window"],
                                   None) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    (dict(x=None), capi.OASR_ERR_INVALID_ARG),
+    (dict(M=0), capi.OASR_ERR_INVALID_ARG),
+    (dict(dm=192, H=3), capi.OASR_ERR_UNSUPPORTED),     # not a multiple of 128
+    (dict(dm=256, H=2), capi.OASR_ERR_UNSUPPORTED),     # d_model != 64 H
+    (dict(dt=capi.OASR_F32), capi.OASR_ERR_UNSUPPORTED),
+    (dict(q=FAKE + 4), capi.OASR_ERR_INVALID_ARG),
+])
+def test_projection_rejects_bad_arguments(lib, args, expect):
+    a = dict(x=FAKE, q=FAKE, M=1024, R=287, dm=256, H=4, dt=capi.OASR_BF16)
+    a.update(args)
+    r = lib.oasr_project_qkv_pos(a["x"], FAKE, FAKE, FAKE, FAKE, a["q"], FAKE, FAKE, FAKE, a["M"],
+                                 a["R"], a["dm"], a["H"], a["dt"], None)
+    assert r == expect
 
 
 def test_device_status_needs_pointer(lib):
