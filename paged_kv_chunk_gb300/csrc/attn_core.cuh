@@ -162,8 +162,8 @@ __device__ __forceinline__ void warp_stage(WarpAcc& acc, const uint32_t (&qu)[4]
     const float base0 = (mx0 == -INFINITY) ? 0.f : mx0;
     const float base1 = (mx1 == -INFINITY) ? 0.f : mx1;
     if (mx0 != acc.m[0] || mx1 != acc.m[1]) {
-        const float alpha0 = exp2f(acc.m[0] - base0);
-        const float alpha1 = exp2f(acc.m[1] - base1);
+        const float alpha0 = ex2_approx(acc.m[0] - base0);
+        const float alpha1 = ex2_approx(acc.m[1] - base1);
         acc.l[0] *= alpha0;
         acc.l[1] *= alpha1;
 #pragma unroll
@@ -178,10 +178,10 @@ __device__ __forceinline__ void warp_stage(WarpAcc& acc, const uint32_t (&qu)[4]
     }
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
-        s[nt][0] = exp2f(s[nt][0] - base0);
-        s[nt][1] = exp2f(s[nt][1] - base0);
-        s[nt][2] = exp2f(s[nt][2] - base1);
-        s[nt][3] = exp2f(s[nt][3] - base1);
+        s[nt][0] = ex2_approx(s[nt][0] - base0);
+        s[nt][1] = ex2_approx(s[nt][1] - base0);
+        s[nt][2] = ex2_approx(s[nt][2] - base1);
+        s[nt][3] = ex2_approx(s[nt][3] - base1);
         acc.l[0] += s[nt][0] + s[nt][1];
         acc.l[1] += s[nt][2] + s[nt][3];
     }
@@ -228,6 +228,7 @@ __device__ __forceinline__ void warp_slice16(WarpAcc& acc, const uint32_t (&qu)[
                                              int lane)
 {
     const int g4 = lane >> 2, t4 = lane & 3, mi = lane >> 3;
+    uint32_t vf[4][4];   // V fragments of the slice
     float s[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -258,6 +259,12 @@ __device__ __forceinline__ void warp_slice16(WarpAcc& acc, const uint32_t (&qu)[
             }
         }
         __syncwarp();   // every lane's K reads are done before the scratch (aliasing them) is written
+        // the slice's V fragments now, so their shared-memory latency hides behind the skew
+        // and the softmax
+        const int vrow = ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+        for (int dp = 0; dp < 4; ++dp)
+            ldsm_x4_t(v_s + swz128(vrow, 2 * dp + (mi >> 1)), vf[dp][0], vf[dp][1], vf[dp][2], vf[dp][3]);
         const int sw0 = 8 * (g4 & 3);   // rows g4 and g4 + 8 share the swizzle
 #pragma unroll
         for (int nb = 0; nb < 4; ++nb) {
@@ -291,8 +298,8 @@ __device__ __forceinline__ void warp_slice16(WarpAcc& acc, const uint32_t (&qu)[
     const float base0 = (mx0 == -INFINITY) ? 0.f : mx0;
     const float base1 = (mx1 == -INFINITY) ? 0.f : mx1;
     if (mx0 != acc.m[0] || mx1 != acc.m[1]) {
-        const float alpha0 = exp2f(acc.m[0] - base0);
-        const float alpha1 = exp2f(acc.m[1] - base1);
+        const float alpha0 = ex2_approx(acc.m[0] - base0);
+        const float alpha1 = ex2_approx(acc.m[1] - base1);
         acc.l[0] *= alpha0;
         acc.l[1] *= alpha1;
 #pragma unroll
@@ -307,24 +314,22 @@ __device__ __forceinline__ void warp_slice16(WarpAcc& acc, const uint32_t (&qu)[
     }
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-        s[nt][0] = exp2f(s[nt][0] - base0);
-        s[nt][1] = exp2f(s[nt][1] - base0);
-        s[nt][2] = exp2f(s[nt][2] - base1);
-        s[nt][3] = exp2f(s[nt][3] - base1);
+        s[nt][0] = ex2_approx(s[nt][0] - base0);
+        s[nt][1] = ex2_approx(s[nt][1] - base0);
+        s[nt][2] = ex2_approx(s[nt][2] - base1);
+        s[nt][3] = ex2_approx(s[nt][3] - base1);
         acc.l[0] += s[nt][0] + s[nt][1];
         acc.l[1] += s[nt][2] + s[nt][3];
     }
     const uint32_t pa[4] = {pack_bf16(s[0][0], s[0][1]), pack_bf16(s[0][2], s[0][3]),
                             pack_bf16(s[1][0], s[1][1]), pack_bf16(s[1][2], s[1][3])};
-    const int row = ((mi & 1) << 3) + (lane & 7);
     const int k0 = 2 * t4;   // keys of this lane's B fragments: b0,b2 -> 2t(+1), b1,b3 -> 8+2t(+1)
     const bool tail = kvalid < 16;
     const uint32_t m0 = (k0 < kvalid ? 0xffffu : 0u) | (k0 + 1 < kvalid ? 0xffff0000u : 0u);
     const uint32_t m1 = (k0 + 8 < kvalid ? 0xffffu : 0u) | (k0 + 9 < kvalid ? 0xffff0000u : 0u);
 #pragma unroll
     for (int dp = 0; dp < 4; ++dp) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(v_s + swz128(row, 2 * dp + (mi >> 1)), b0, b1, b2, b3);
+        uint32_t b0 = vf[dp][0], b1 = vf[dp][1], b2 = vf[dp][2], b3 = vf[dp][3];
         if (tail) {   // V rows past the last key may hold anything (0 * NaN is NaN)
             b0 &= m0;
             b2 &= m0;
@@ -379,7 +384,7 @@ __device__ __forceinline__ uint4 combine_row8(const float* comb_o, const float* 
     float L = 0.f;
     for (int k = 0; k < nparts; ++k) {
         const float mk = comb_m[k * pstride + row];
-        const float w = (mk == -INFINITY) ? 0.f : exp2f(mk - mstar);
+        const float w = (mk == -INFINITY) ? 0.f : ex2_approx(mk - mstar);
         L += w * comb_l[k * pstride + row];
         const float* src = comb_o + (k * pstride + row) * kOW + d0;
 #pragma unroll

@@ -30,6 +30,14 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+// 2^x by the hardware approximation (flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
