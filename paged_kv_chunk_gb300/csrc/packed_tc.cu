@@ -418,8 +418,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 ++sg;
                 tc_fence_after();
                 uint8_t* slot_p = sm + SP::off_slot + (g & 1) * SP::slot;
+                // the half holds keys jh .. jh+63; row r sees [ka, kb) of them.  Under the
+                // chunked-limited window a warp whose rows see none of them skips the half (it
+                // still releases S/G, exchanges -inf and writes P = 0)
+                const int jh = kl + s * kBN + 64 * hf;
+                int ka = 0, kb = kh - jh;
+                if (MASKED) {
+                    const int ci = (i0 + r) / a.cs;
+                    const int lo = (ci - a.left) * a.cs - jh, hi = (ci + 1) * a.cs - jh;
+                    ka = lo > 0 ? lo : 0;
+                    kb = hi < kb ? hi : kb;
+                }
+                const bool live = !MASKED || __any_sync(0xffffffffu, ka < kb && ka < 64 && kb > 0);
                 float sc[64];
-                {
+                if (live) {
                     uint32_t sr[64], rr[32];
                     const uint32_t colg = kColG + static_cast<uint32_t>(96 - 32 * quad + 64 * hf);
                     OASR_TMEM_LD32(tl + kColS + 64 * hf, sr);
@@ -473,18 +485,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     decode(item + gridDim.x, ns1, nL, ni0, nh, nkl, nkh);
                     if (!warp_wait(bar_q_free, it & 1) || !prep_q(it + 1, nh)) { ok = false; break; }
                 }
-                // scale (log2 domain), mask keys this row does not see, this half's max:
-                // the half holds keys jh .. jh+63; row r sees [ka, kb) of them
-                const int jh = kl + s * kBN + 64 * hf;
-                int ka = 0, kb = kh - jh;
-                if (MASKED) {
-                    const int ci = (i0 + r) / a.cs;
-                    const int lo = (ci - a.left) * a.cs - jh, hi = (ci + 1) * a.cs - jh;
-                    ka = lo > 0 ? lo : 0;
-                    kb = hi < kb ? hi : kb;
-                }
+                // scale (log2 domain), mask keys this row does not see, this half's max
                 float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-                if (ka <= 0 && kb >= 64) {
+                if (!live) {
+                } else if (ka <= 0 && kb >= 64) {
 #pragma unroll
                     for (int j = 0; j < 64; j += 4) {
                         sc[j] *= a.scale_log2; sc[j + 1] *= a.scale_log2;
@@ -524,7 +528,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 m_used = m_new;
                 // a row that has seen no key yet has max -inf: its P is 0, not NaN
                 const float mref = m_used == -INFINITY ? 0.f : m_used;
-                {
+                if (!live) {
+                    uint32_t zero[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) zero[j] = 0u;
+                    OASR_TMEM_ST16(tl + kColP + 32 * hf, zero);
+                    OASR_TMEM_ST16(tl + kColP + 32 * hf + 16, zero);
+                } else {
                     float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
                     for (int q2 = 0; q2 < 2; ++q2) {
