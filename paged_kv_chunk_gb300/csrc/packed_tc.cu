@@ -81,7 +81,8 @@ struct TcArgs {
     unsigned* status;
     int num_seqs, total, H, z;
     int cs, left;            // chunked-limited window (MASKED kernel): chunk frames, earlier chunks
-    float scale_log2;
+    uint32_t sign;           // 0x80008000 when the scale is negative (q+u, q+v are negated)
+    float scale_log2;        // |scale| * log2(e)
 };
 
 // ------------------------------------------------------------------------ kernel
@@ -390,6 +391,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
                     ou[e] = pack_bf16(lo + __uint_as_float(wu[e] << 16), hi + __uint_as_float(wu[e] & 0xffff0000u));
                     ov[e] = pack_bf16(lo + __uint_as_float(wv[e] << 16), hi + __uint_as_float(wv[e] & 0xffff0000u));
+                    ou[e] ^= a.sign;   // a negative scale: negate q+u and q+v (exact in bf16)
+                    ov[e] ^= a.sign;
                 }
                 *reinterpret_cast<uint4*>(sm + SP::off_qu + offs) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
                 *reinterpret_cast<uint4*>(sm + SP::off_qv + offs) = make_uint4(ov[0], ov[1], ov[2], ov[3]);
@@ -486,13 +489,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     if (!warp_wait(bar_q_free, it & 1) || !prep_q(it + 1, nh)) { ok = false; break; }
                 }
                 // scale (log2 domain), mask keys this row does not see, this half's max
+                // scores stay unscaled here: the scale (> 0, its sign is folded into q+u and
+                // q+v) is applied to the row max and inside the exponent's FFMA
                 float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
                 if (!live) {
                 } else if (ka <= 0 && kb >= 64) {
 #pragma unroll
                     for (int j = 0; j < 64; j += 4) {
-                        sc[j] *= a.scale_log2; sc[j + 1] *= a.scale_log2;
-                        sc[j + 2] *= a.scale_log2; sc[j + 3] *= a.scale_log2;
                         mx0 = fmaxf(mx0, sc[j]); mx1 = fmaxf(mx1, sc[j + 1]);
                         mx2 = fmaxf(mx2, sc[j + 2]); mx3 = fmaxf(mx3, sc[j + 3]);
                     }
@@ -501,12 +504,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     for (int j = 0; j < 64; j += 4) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            sc[j + e] = (j + e >= ka && j + e < kb) ? sc[j + e] * a.scale_log2 : -INFINITY;
+                            sc[j + e] = (j + e >= ka && j + e < kb) ? sc[j + e] : -INFINITY;
                         mx0 = fmaxf(mx0, sc[j]); mx1 = fmaxf(mx1, sc[j + 1]);
                         mx2 = fmaxf(mx2, sc[j + 2]); mx3 = fmaxf(mx3, sc[j + 3]);
                     }
                 }
-                float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)), mx_other;
+                float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2, mx_other;
                 pair_post(mx);
                 // P.V of the previous stage must be done before P and O are touched
                 if (s > 0 && !warp_wait(bar_pv_done, (g - 1) & 1)) { ok = false; break; }
@@ -541,8 +544,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                         uint32_t pk[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const float p0 = ex2_approx(sc[32 * q2 + 2 * j] - mref);
-                            const float p1 = ex2_approx(sc[32 * q2 + 2 * j + 1] - mref);
+                            const float p0 = ex2_approx(fmaf(sc[32 * q2 + 2 * j], a.scale_log2, -mref));
+                            const float p1 = ex2_approx(fmaf(sc[32 * q2 + 2 * j + 1], a.scale_log2, -mref));
                             ps0 += p0;
                             ps1 += p1;
                             pk[j] = pack_bf16(p0, p1);
@@ -647,7 +650,10 @@ oasr_status launch_packed_tc(const void* q, const void* k, const void* v, const 
     a.z = (R - 1) / 2;
     a.cs = masked ? cs : 1;
     a.left = masked ? left : 0;
-    a.scale_log2 = scale * 1.4426950408889634f;
+    a.sign = scale < 0.f ? 0x80008000u : 0u;
+    // > 0 even for a zero scale, so that a masked score (-inf) times it stays -inf; at 1e-30
+    // every finite score's contribution to ex2 rounds away in fp32, as with a zero scale
+    a.scale_log2 = fmaxf(fabsf(scale) * 1.4426950408889634f, 1e-30f);
     const long long items_bound = ((static_cast<long long>(total) + kBM - 1) / kBM + num_seqs) * H;
     const int grid = static_cast<int>(items_bound < sms ? items_bound : sms);
     kern<<<grid, kTcThreads, smem, stream>>>(tm_q, tm_k, tm_v, tm_r, a);

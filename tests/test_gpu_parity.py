@@ -283,6 +283,20 @@ def test_packed_full(lengths, dtype):
     assert capi.oasr_device_status() == 0
 
 
+@pytest.mark.parametrize("scale", [0.3, -0.2, 0.0], ids=str)
+def test_packed_scale_argument(scale):
+    """Any scale, including a negative one (folded into the sign of q+u and q+v) and zero."""
+    _, x = _packed_case([200, 1, 77], seed=14)
+    d = {k: dev(x[k], "bf16") for k in ("q", "k", "v", "pos_bias_u", "pos_bias_v", "rel")}
+    cu = torch.from_numpy(x["cu_seqlens"]).cuda()
+    out = capi.oasr_packed_relattn_varlen(d["q"], d["k"], d["v"], cu, x["max_seqlen"], d["pos_bias_u"],
+                                          d["pos_bias_v"], d["rel"], scale=scale)
+    torch.cuda.synchronize()
+    ref = oracle.packed_relattn(x["q"], x["k"], x["v"], x["cu_seqlens"], x["pos_bias_u"],
+                                x["pos_bias_v"], x["rel"], scale=scale)
+    check_close(to_np(out), ref, "bf16", f"packed scale {scale}")
+
+
 def test_packed_longer_table():
     _, x = _packed_case([90, 33], R_extra=10)
     out = _run_packed(x, "bf16")
