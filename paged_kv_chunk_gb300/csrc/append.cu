@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(256) paged_append_kernel(
     const int32_t* __restrict__ block_table, int mbps, const int32_t* __restrict__ cache_seqlens,
     int T, int H, int vpr, long long n_vec, unsigned* status)
 {
+    grid_dep_wait();     // the previous grid on the stream has finished (programmatic launch)
     unsigned err = 0;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -45,6 +46,8 @@ __global__ void __launch_bounds__(256) paged_append_kernel(
         else
             k_pool[dst] = __ldg(k_new + e);
     }
+    // this thread's copies are issued: the next grid may schedule (it waits for this one)
+    grid_dep_trigger();
     if (err) atomicOr(status, err);
 }
 
@@ -75,9 +78,9 @@ extern "C" oasr_status oasr_paged_append(const void* k_new, const void* v_new, v
     const long long n_vec = static_cast<long long>(B) * T * H * vpr;
     long long blocks = (2 * n_vec + 255) / 256;
     if (blocks > 16LL * sms) blocks = 16LL * sms;
-    paged_append_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
-        static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), num_blocks, block_size,
-        block_table, max_blocks_per_seq, cache_seqlens, T, H, vpr, n_vec, status);
-    return launch_status();
+    return launch_pdl(paged_append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+                      static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), num_blocks,
+                      block_size, block_table, max_blocks_per_seq, cache_seqlens, T, H, vpr, n_vec,
+                      status);
 }

@@ -93,6 +93,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     const int T = a.T;
     unsigned err = 0;
 
+    // Launched with programmatic stream serialization: everything the previous grid on the
+    // stream wrote is visible once this returns, and nothing global is read before it.
+    grid_dep_wait();
     int C = __ldg(a.cache_seqlens + b);
     if (C < 0) { C = 0; err |= kErrBounds; }
     int K = C + T;
@@ -290,6 +293,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         }
     }
     if (failed) s_failed = 1;
+    // the stage loop is done: the next grid on the stream may start launching its CTAs (they
+    // wait for this grid to finish before reading anything)
+    grid_dep_trigger();
     named_bar_sync(1, 32 * kConsumerWarps);
     if (s_failed) {
         if (tid == 0) atomicOr(a.status, err | kErrTimeout);
@@ -477,8 +483,8 @@ oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, voi
     a.R = R;
     a.box_rows = box;
     a.scale_log2 = scale * 1.4426950408889634f;
-    kern<<<static_cast<unsigned>(B) * H, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, tm_r, tm_kn, tm_vn, a);
-    return launch_status();
+    return launch_pdl(kern, dim3(static_cast<unsigned>(B) * H), dim3(kThreads), smem, stream, tm_q,
+                      tm_k, tm_v, tm_r, tm_kn, tm_vn, a);
 }
 
 template <bool FUSED>

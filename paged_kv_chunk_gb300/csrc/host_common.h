@@ -28,6 +28,29 @@ inline oasr_status launch_status()
     return cudaGetLastError() == cudaSuccess ? OASR_OK : OASR_ERR_CUDA;
 }
 
+// Launch with programmatic stream serialization: the grid's CTAs may be scheduled while the
+// previous grid on the stream drains.  Every kernel launched this way executes
+// griddepcontrol.wait before its first global access, so it still sees all of the previous
+// grid's writes.
+template <typename... KArgs, typename... Args>
+oasr_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, int smem,
+                       cudaStream_t stream, Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...) != cudaSuccess)
+        return OASR_ERR_CUDA;
+    return launch_status();
+}
+
 // Raise the dynamic shared-memory limit of `func` once per device.
 template <typename F>
 bool ensure_smem(F* func, int bytes, int (&done)[64])

@@ -88,6 +88,9 @@ __global__ void __launch_bounds__(kPThreads, 1) project_tc_kernel(
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
+    // the setup above overlaps the previous grid on the stream; inputs and outputs are
+    // touched only after it has finished
+    grid_dep_wait();
 
     // tile t -> problem, row tile, column tile
     auto decode = [&](int t, int& g, int& mt, int& nt) {
@@ -230,6 +233,7 @@ __global__ void __launch_bounds__(kPThreads, 1) project_tc_kernel(
             if (lane == 0) mbar_arrive(bar_acc_free + 8 * buf);
         }
     }
+    grid_dep_trigger();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -283,6 +287,6 @@ extern "C" oasr_status oasr_project_qkv_pos(const void* x, const void* w_qkv, co
     a.tiles = a.tiles0 + ((R + kPM - 1) / kPM) * a.nt1;
     a.status = status;
     const int grid = a.tiles < sms ? a.tiles : sms;
-    project_tc_kernel<<<grid, kPThreads, smem, stream>>>(tm_x, tm_wqkv, tm_pos, tm_wpos, a);
-    return launch_status();
+    return launch_pdl(project_tc_kernel, dim3(grid), dim3(kPThreads), smem, stream, tm_x, tm_wqkv,
+                      tm_pos, tm_wpos, a);
 }

@@ -38,6 +38,12 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
+// Programmatic dependent launch: wait until the previous grid on the stream has finished and
+// its writes are visible (a no-op when launched without the attribute), and let the next
+// grid start scheduling its CTAs.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)

@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(128) window_commit_kernel(int32_t* __restrict_
                                                             int mbps, int bs, int T, int window,
                                                             unsigned* status)
 {
+    grid_dep_wait();     // the previous grid on the stream has finished (programmatic launch)
+    grid_dep_trigger();
     const int b = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (b >= B) return;
     unsigned err = 0;
@@ -76,8 +78,6 @@ extern "C" oasr_status oasr_window_commit(int32_t* block_table, int32_t* cache_s
     if (max_blocks_per_seq > kWinMaxPages) return OASR_ERR_UNSUPPORTED;
     unsigned* status = status_word();
     if (!status) return OASR_ERR_CUDA;
-    window_commit_kernel<<<(B + 3) / 4, 128, 0, stream>>>(block_table, cache_seqlens, B,
-                                                          max_blocks_per_seq, block_size, T,
-                                                          window_frames, status);
-    return launch_status();
+    return launch_pdl(window_commit_kernel, dim3((B + 3) / 4), dim3(128), 0, stream, block_table,
+                      cache_seqlens, B, max_blocks_per_seq, block_size, T, window_frames, status);
 }
