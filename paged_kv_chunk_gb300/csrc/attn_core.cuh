@@ -214,6 +214,63 @@ __device__ __forceinline__ void warp_stage(WarpAcc& acc, const uint32_t (&qu)[4]
     }
 }
 
+// The rest of a 16-key slice once its scaled scores s (log2 units, masked keys -inf) and the
+// running maxima folded with this thread's scores (mx0, mx1) are known: quad max, online
+// softmax update, P rounded to bf16, O += P . V (vf: the slice's V fragments).
+__device__ __forceinline__ void softmax_pv16(WarpAcc& acc, float (&s)[2][4], const uint32_t (&vf)[4][4],
+                                             float mx0, float mx1, int kvalid, int lane)
+{
+    const int t4 = lane & 3;
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float base0 = (mx0 == -INFINITY) ? 0.f : mx0;
+    const float base1 = (mx1 == -INFINITY) ? 0.f : mx1;
+    if (mx0 != acc.m[0] || mx1 != acc.m[1]) {
+        const float alpha0 = ex2_approx(acc.m[0] - base0);
+        const float alpha1 = ex2_approx(acc.m[1] - base1);
+        acc.l[0] *= alpha0;
+        acc.l[1] *= alpha1;
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt) {
+            acc.o[dt][0] *= alpha0;
+            acc.o[dt][1] *= alpha0;
+            acc.o[dt][2] *= alpha1;
+            acc.o[dt][3] *= alpha1;
+        }
+        acc.m[0] = mx0;
+        acc.m[1] = mx1;
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        s[nt][0] = ex2_approx(s[nt][0] - base0);
+        s[nt][1] = ex2_approx(s[nt][1] - base0);
+        s[nt][2] = ex2_approx(s[nt][2] - base1);
+        s[nt][3] = ex2_approx(s[nt][3] - base1);
+        acc.l[0] += s[nt][0] + s[nt][1];
+        acc.l[1] += s[nt][2] + s[nt][3];
+    }
+    const uint32_t pa[4] = {pack_bf16(s[0][0], s[0][1]), pack_bf16(s[0][2], s[0][3]),
+                            pack_bf16(s[1][0], s[1][1]), pack_bf16(s[1][2], s[1][3])};
+    const int k0 = 2 * t4;   // keys of this lane's B fragments: b0,b2 -> 2t(+1), b1,b3 -> 8+2t(+1)
+    const bool tail = kvalid < 16;
+    const uint32_t m0 = (k0 < kvalid ? 0xffffu : 0u) | (k0 + 1 < kvalid ? 0xffff0000u : 0u);
+    const uint32_t m1 = (k0 + 8 < kvalid ? 0xffffu : 0u) | (k0 + 9 < kvalid ? 0xffff0000u : 0u);
+#pragma unroll
+    for (int dp = 0; dp < 4; ++dp) {
+        uint32_t b0 = vf[dp][0], b1 = vf[dp][1], b2 = vf[dp][2], b3 = vf[dp][3];
+        if (tail) {   // V rows past the last key may hold anything (0 * NaN is NaN)
+            b0 &= m0;
+            b2 &= m0;
+            b1 &= m1;
+            b3 &= m1;
+        }
+        mma_bf16_16816(acc.o[2 * dp], pa, b0, b1);
+        mma_bf16_16816(acc.o[2 * dp + 1], pa, b2, b3);
+    }
+}
+
 // One warp, 16 query rows, one 16-key slice of a stage (the four consumer warps of a
 // one-m-tile CTA split every stage this way, so a stage is consumed in a quarter of the
 // latency).  k_s, v_s: shared addresses of the slice's first K and V rows; band_s: the
@@ -291,54 +348,151 @@ __device__ __forceinline__ void warp_slice16(WarpAcc& acc, const uint32_t (&qu)[
         mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
         mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
     }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float base0 = (mx0 == -INFINITY) ? 0.f : mx0;
-    const float base1 = (mx1 == -INFINITY) ? 0.f : mx1;
-    if (mx0 != acc.m[0] || mx1 != acc.m[1]) {
-        const float alpha0 = ex2_approx(acc.m[0] - base0);
-        const float alpha1 = ex2_approx(acc.m[1] - base1);
-        acc.l[0] *= alpha0;
-        acc.l[1] *= alpha1;
+    softmax_pv16(acc, s, vf, mx0, mx1, kvalid, lane);
+}
+
+// Position table of one CTA (16 query rows of one head), built once before the key loop:
+// G[i][c] = bf16(q_i + v) . rel[rho0 + c] for c in [0, ncols), rel rows outside [0, R) taken
+// as zero.  It is stored pre-skewed, G[i][c] at gs[i*W + c + i + 1], so that query i and key j
+// (c = j + 15 - i) read gs[i*W + j + 16]: one row of a slice's scores is one contiguous run.
+// Warp `warp` of `nw` computes column tiles warp, warp + nw, ...  The head dimension is
+// contracted in a permuted order: lane quad position t4 holds dims [16 t4, 16 t4 + 16) of
+// both operands, so a lane's B fragments for one rel row are two 16-byte loads (rel is read
+// from global memory; the table is the same for every stream and stays in L2).
+// The rel rows of the first kPosBatch tiles are requested by load() as early as the caller
+// can (they need only the cache length), the rest by build() itself.
+constexpr int kPosBatch = 10;   // column tiles of one warp whose rel rows are in flight together
+
+struct PosTable {
+    const uint16_t* rel_h;   // rel + h * 64
+    long long stride;        // elements between rel rows
+    int R, rho0, ncols, warp, nw, lane;
+    uint4 bl[kPosBatch], bh[kPosBatch];
+
+    __device__ __forceinline__ int ntiles() const { return (ncols + 7) >> 3; }
+
+    __device__ __forceinline__ void load(int nb0)
+    {
+        const int g4 = lane >> 2, t4 = lane & 3;
 #pragma unroll
-        for (int dt = 0; dt < 8; ++dt) {
-            acc.o[dt][0] *= alpha0;
-            acc.o[dt][1] *= alpha0;
-            acc.o[dt][2] *= alpha1;
-            acc.o[dt][3] *= alpha1;
+        for (int u = 0; u < kPosBatch; ++u) {
+            const int rho = rho0 + 8 * (nb0 + u * nw) + g4;
+            bl[u] = bh[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (nb0 + u * nw < ntiles() && rho >= 0 && rho < R) {
+                const uint4* src = reinterpret_cast<const uint4*>(rel_h + rho * stride + 16 * t4);
+                bl[u] = __ldg(src);
+                bh[u] = __ldg(src + 1);
+            }
         }
-        acc.m[0] = mx0;
-        acc.m[1] = mx1;
     }
+
+    // q_tile: the 128-byte-swizzled Q tile; v: the bias v in fp32 (smem).  load(warp) must
+    // have been called.
+    __device__ __forceinline__ void build(float* gs, int W, const uint8_t* q_tile, const float* v)
+    {
+        const int g4 = lane >> 2, t4 = lane & 3;
+        uint32_t qa[4][4];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int row = g4 + 8 * half;
+            const uint4 c0 = *reinterpret_cast<const uint4*>(q_tile + swz128(row, 2 * t4));
+            const uint4 c1 = *reinterpret_cast<const uint4*>(q_tile + swz128(row, 2 * t4 + 1));
+            const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int d = 16 * t4 + 2 * m;
+                // word m holds dims d, d+1: k-step m/2, k pair m%2 (a0/a1 pair 0, a2/a3 pair 1)
+                qa[m >> 1][half + 2 * (m & 1)] =
+                    pack_bf16(bf16_lo(w[m]) + v[d], bf16_hi(w[m]) + v[d + 1]);
+            }
+        }
+        for (int nb0 = warp;;) {
+#pragma unroll
+            for (int u = 0; u < kPosBatch; ++u) {
+                const int nb = nb0 + u * nw;
+                if (nb >= ntiles()) break;
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_bf16_16816(c, qa[0], bl[u].x, bl[u].y);
+                mma_bf16_16816(c, qa[1], bl[u].z, bl[u].w);
+                mma_bf16_16816(c, qa[2], bh[u].x, bh[u].y);
+                mma_bf16_16816(c, qa[3], bh[u].z, bh[u].w);
+                const int col = 8 * nb + 2 * t4;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    if (col + e < ncols) {
+                        gs[g4 * W + col + e + g4 + 1] = c[e];
+                        gs[(g4 + 8) * W + col + e + g4 + 9] = c[2 + e];
+                    }
+                }
+            }
+            nb0 += kPosBatch * nw;
+            if (nb0 >= ntiles()) break;
+            load(nb0);
+        }
+    }
+};
+
+// One warp, one 16-key slice, with the position term read from the CTA's pre-skewed table:
+// gq points at gs + js + 16 for the slice's first key js, so key jl of query row i uses
+// gq[i*W + jl].  k_s, v_s: the slice's 16 K and V rows (128-byte swizzled); keys
+// [0, kvalid) of the slice exist.
+__device__ __forceinline__ void warp_slice16_gt(WarpAcc& acc, const uint32_t (&qu)[4][4],
+                                                uint32_t k_s, uint32_t v_s, const float* gq,
+                                                int W, bool even, int kvalid, float scale_log2,
+                                                int lane)
+{
+    const int g4 = lane >> 2, t4 = lane & 3, mi = lane >> 3;
+    float gb[2][4];   // [nt][row g4 cols 2t4, 2t4+1 | row g4+8 cols 2t4, 2t4+1]
+    {
+        const float* r0 = gq + g4 * W + 2 * t4;
+        const float* r1 = r0 + 8 * W;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            if (even) {
+                const float2 x = *reinterpret_cast<const float2*>(r0 + 8 * nt);
+                const float2 y = *reinterpret_cast<const float2*>(r1 + 8 * nt);
+                gb[nt][0] = x.x;
+                gb[nt][1] = x.y;
+                gb[nt][2] = y.x;
+                gb[nt][3] = y.y;
+            } else {
+                gb[nt][0] = r0[8 * nt];
+                gb[nt][1] = r0[8 * nt + 1];
+                gb[nt][2] = r1[8 * nt];
+                gb[nt][3] = r1[8 * nt + 1];
+            }
+        }
+    }
+    float s[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(k_s + swz128(((mi >> 1) << 3) + (lane & 7), 2 * ks + (mi & 1)), b0, b1, b2, b3);
+        mma_bf16_16816(s[0], qu[ks], b0, b1);
+        mma_bf16_16816(s[1], qu[ks], b2, b3);
+    }
+    uint32_t vf[4][4];
+    const int vrow = ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+    for (int dp = 0; dp < 4; ++dp)
+        ldsm_x4_t(v_s + swz128(vrow, 2 * dp + (mi >> 1)), vf[dp][0], vf[dp][1], vf[dp][2], vf[dp][3]);
+    float mx0 = acc.m[0], mx1 = acc.m[1];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-        s[nt][0] = ex2_approx(s[nt][0] - base0);
-        s[nt][1] = ex2_approx(s[nt][1] - base0);
-        s[nt][2] = ex2_approx(s[nt][2] - base1);
-        s[nt][3] = ex2_approx(s[nt][3] - base1);
-        acc.l[0] += s[nt][0] + s[nt][1];
-        acc.l[1] += s[nt][2] + s[nt][3];
-    }
-    const uint32_t pa[4] = {pack_bf16(s[0][0], s[0][1]), pack_bf16(s[0][2], s[0][3]),
-                            pack_bf16(s[1][0], s[1][1]), pack_bf16(s[1][2], s[1][3])};
-    const int k0 = 2 * t4;   // keys of this lane's B fragments: b0,b2 -> 2t(+1), b1,b3 -> 8+2t(+1)
-    const bool tail = kvalid < 16;
-    const uint32_t m0 = (k0 < kvalid ? 0xffffu : 0u) | (k0 + 1 < kvalid ? 0xffff0000u : 0u);
-    const uint32_t m1 = (k0 + 8 < kvalid ? 0xffffu : 0u) | (k0 + 9 < kvalid ? 0xffff0000u : 0u);
 #pragma unroll
-    for (int dp = 0; dp < 4; ++dp) {
-        uint32_t b0 = vf[dp][0], b1 = vf[dp][1], b2 = vf[dp][2], b3 = vf[dp][3];
-        if (tail) {   // V rows past the last key may hold anything (0 * NaN is NaN)
-            b0 &= m0;
-            b2 &= m0;
-            b1 &= m1;
-            b3 &= m1;
+        for (int e = 0; e < 2; ++e) {
+            const bool ok = 8 * nt + 2 * t4 + e < kvalid;
+            s[nt][e] = ok ? (s[nt][e] + gb[nt][e]) * scale_log2 : -INFINITY;
+            s[nt][2 + e] = ok ? (s[nt][2 + e] + gb[nt][2 + e]) * scale_log2 : -INFINITY;
         }
-        mma_bf16_16816(acc.o[2 * dp], pa, b0, b1);
-        mma_bf16_16816(acc.o[2 * dp + 1], pa, b2, b3);
+        mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+        mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
     }
+    softmax_pv16(acc, s, vf, mx0, mx1, kvalid, lane);
 }
 
 // Quad-reduce the row sums (each thread held its own columns' share).

@@ -37,10 +37,12 @@ struct ChunkArgs {
     const int32_t* cache_seqlens;
     const uint16_t* pos_bias_u;
     const uint16_t* pos_bias_v;
+    const uint16_t* rel;     // position-table variant: rel rows [R][H][64]
     uint16_t* out;
     unsigned* status;
     int num_blocks, block_size, mbps, T, H, R;
     int box_rows;            // rows of one K/V TMA box = min(block_size, 64)
+    int gt_w;                // position-table variant: row stride of the table (floats)
     float scale_log2;        // scale * log2(e)
 };
 
@@ -49,23 +51,27 @@ struct ChunkArgs {
 // 128-byte swizzled by TMA.  With one m-tile the skew scratch of the consuming warp reuses
 // the slot's band tile; otherwise each consumer warp has its own scratch.  After the key
 // loop the slots hold the cross-warp combine.
+// Position-table variant (GT, one m-tile): no band in the slots; the CTA's whole position
+// term, 16 rows of gt_w floats, follows the barriers (its size is set at launch).
 // Block-table entries a CTA caches in shared memory.
 constexpr int kMaxPages = 512;
 
-template <int MT, int NS>
+template <int MT, int NS, bool GT>
 struct ChunkSmem {
     using TL = Tile<MT>;
-    static constexpr bool kGInBand = MT == 1;
-    static constexpr int kBand = TL::RB * kRowBytes;
+    static_assert(!GT || MT == 1, "the position table serves one m-tile");
+    static constexpr bool kGInBand = MT == 1 && !GT;
+    static constexpr int kBand = GT ? 0 : TL::RB * kRowBytes;
     static constexpr int kSlot = 2 * kStageKeys * kRowBytes + kBand;
     static constexpr int off_slots = 0;
     static constexpr int off_q = NS * kSlot;
     static constexpr int off_g = off_q + TL::Tp * kRowBytes;
-    static constexpr int off_u = off_g + (kGInBand ? 0 : kConsumerWarps * kGBytes);
+    static constexpr int off_u = off_g + (MT == 1 ? 0 : kConsumerWarps * kGBytes);
     static constexpr int off_vb = off_u + kHeadDim * 4;
     static constexpr int off_bt = off_vb + kHeadDim * 4;    // the stream's block-table row
     static constexpr int off_bar = off_bt + kMaxPages * 4;  // full[NS], empty[NS], q, written
-    static constexpr int bytes = off_bar + (2 * NS + 2) * 8 + 1024;
+    static constexpr int off_gt = (off_bar + (2 * NS + 2) * 8 + 15) & ~15;
+    static constexpr int bytes = off_gt + 1024;   // + 16 * gt_w * 4 with GT
     static constexpr int comb_o = 0;
     static constexpr int comb_m = comb_o + TL::KG * TL::Tp * kOW * 4;
     static constexpr int comb_l = comb_m + TL::KG * TL::Tp * 4;
@@ -74,7 +80,7 @@ struct ChunkSmem {
     static_assert(comb_l + TL::KG * TL::Tp * 4 <= NS * kSlot, "combine area");
 };
 
-template <int MT, int NS, bool FUSED>
+template <int MT, int NS, bool FUSED, bool GT>
 __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
@@ -82,7 +88,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     const ChunkArgs a)
 {
     using TL = Tile<MT>;
-    using SP = ChunkSmem<MT, NS>;
+    using SP = ChunkSmem<MT, NS, GT>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, derived from the __shared__ array itself so that every access
     // through it stays a shared-space access
@@ -121,10 +127,24 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         mbar_init(bar_written, 32 * kConsumerWarps);
         fence_mbar_init();
         s_failed = 0;
+        // the Q tile needs no block-table entry: it is requested before the table row is read
+        mbar_arrive_expect_tx(bar_q, TL::Tp * kRowBytes);
+        tma_load_3d(sb + SP::off_q, &tm_q, bar_q, 0, h, b * T);
+    }
+    // Position-table variant: u, v go out beside the block-table row (the producer warp
+    // alone loads the row, and the table's rel rows are requested only once the row is in:
+    // issued earlier they delay it and the first stages behind them).
+    if (GT && warp < kConsumerWarps) {
+        if (tid < kHeadDim)
+            s_u[tid] = bf16_lo(__ldg(a.pos_bias_u + h * kHeadDim + tid));
+        else
+            s_vb[tid - kHeadDim] = bf16_lo(__ldg(a.pos_bias_v + h * kHeadDim + tid - kHeadDim));
     }
     const int n_pages = (K + a.block_size - 1) / a.block_size;   // <= kMaxPages (host check)
-    for (int i = tid; i < n_pages; i += kThreads)
-        s_bt[i] = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + i);
+    if (!GT || warp == kConsumerWarps) {   // GT: the producer warp alone, so no rel load delays it
+        for (int i = GT ? lane : tid; i < n_pages; i += GT ? 32 : kThreads)
+            s_bt[i] = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + i);
+    }
     __syncthreads();
 
     // Stage plan (every thread derives the same one from the cached table row).
@@ -160,7 +180,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         const int nbox = chunk ? (T + 15) / 16
                                : min(kStageKeys / box, (kc - j0 + box - 1) / box);
         if (lane == 0)
-            mbar_arrive_expect_tx(bar, static_cast<uint32_t>((2 * nbox * box + TL::RB) * kRowBytes));
+            mbar_arrive_expect_tx(
+                bar, static_cast<uint32_t>((2 * nbox * box + (GT ? 0 : TL::RB)) * kRowBytes));
         __syncwarp();
         if (lane < nbox) {
             const uint32_t dk = base + lane * box * kRowBytes;
@@ -184,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
                 tma_load_3d_hint(dv, &tm_v, bar, 0, h, row, pol);
             }
         }
-        if (lane == 0)
+        if (!GT && lane == 0)
             tma_load_3d(base + 2 * kStageKeys * kRowBytes, &tm_r, bar, 0, h, off + j0 - (TL::Tp - 1));
     };
 
@@ -194,13 +215,11 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         if (lane == 0) {
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
-            prefetch_tensormap(&tm_r);
+            if (!GT) prefetch_tensormap(&tm_r);
             if (direct) {
                 prefetch_tensormap(&tm_kn);
                 prefetch_tensormap(&tm_vn);
             }
-            mbar_arrive_expect_tx(bar_q, TL::Tp * kRowBytes);
-            tma_load_3d(sb + SP::off_q, &tm_q, bar_q, 0, h, b * T);
         }
         // without the direct chunk stage, stages from this one on hold chunk rows
         const int first_chunk_stage = (FUSED && !direct) ? C / kStageKeys : n_stages;
@@ -219,12 +238,14 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     }
 
     // ---- consumers: u, v; the chunk into the pool (fused); then the stages
-    if (tid < kHeadDim)
-        s_u[tid] = bf16_lo(__ldg(a.pos_bias_u + h * kHeadDim + tid));
-    else
-        s_vb[tid - kHeadDim] = bf16_lo(__ldg(a.pos_bias_v + h * kHeadDim + tid - kHeadDim));
-    if constexpr (FUSED) {
-        // This head's slice of the chunk: T rows x 8 vectors of 16 B, for K and for V.
+    const int mt = warp % MT, kg = warp / MT;
+    bool failed = false;
+    uint32_t qu[4][4], qv[4][4];
+    WarpAcc acc;
+    acc_init(acc);
+    // fused, without the direct chunk stage: this head's slice of the chunk into the pool
+    // (T rows x 8 vectors of 16 B, for K and for V), fenced for the stages that read it back
+    auto copy_chunk_global = [&]() {
         for (int idx = tid; idx < 2 * T * 8; idx += 32 * kConsumerWarps) {
             const int kv = idx >= T * 8;
             const int rem = idx - kv * T * 8;
@@ -244,19 +265,73 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         }
         fence_proxy_async_global();
         mbar_arrive(bar_written);
+    };
+    if constexpr (GT) {
+        PosTable pt;
+        pt.rel_h = a.rel + h * kHeadDim;
+        pt.stride = static_cast<long long>(a.H) * kHeadDim;
+        pt.R = a.R;
+        pt.rho0 = off - 15;
+        pt.ncols = K + 15;
+        pt.warp = warp;
+        pt.nw = kConsumerWarps;
+        pt.lane = lane;
+        pt.load(warp);
+        if (FUSED && !direct) copy_chunk_global();
+        // the whole position term of the CTA (its rel rows are in flight or in), while the
+        // first pages land
+        failed = !mbar_wait(bar_q, 0);
+        if (!failed)
+            pt.build(reinterpret_cast<float*>(sm + SP::off_gt), a.gt_w, sm + SP::off_q, s_vb);
+        named_bar_sync(1, 32 * kConsumerWarps);   // the table is complete
+        if (!failed) make_q_frags(sb + SP::off_q, s_u, s_vb, mt, lane, qu, qv);
+    } else {
+        if (tid < kHeadDim)
+            s_u[tid] = bf16_lo(__ldg(a.pos_bias_u + h * kHeadDim + tid));
+        else
+            s_vb[tid - kHeadDim] = bf16_lo(__ldg(a.pos_bias_v + h * kHeadDim + tid - kHeadDim));
+        if constexpr (FUSED) copy_chunk_global();
+        named_bar_sync(1, 32 * kConsumerWarps);
+        failed = !mbar_wait(bar_q, 0);
+        if (!failed) make_q_frags(sb + SP::off_q, s_u, s_vb, mt, lane, qu, qv);
     }
-    named_bar_sync(1, 32 * kConsumerWarps);
-
-    // ---- consumers
-    const int mt = warp % MT, kg = warp / MT;
-    bool failed = !mbar_wait(bar_q, 0);
-    uint32_t qu[4][4], qv[4][4];
-    WarpAcc acc;
-    acc_init(acc);
     if (!failed) {
-        make_q_frags(sb + SP::off_q, s_u, s_vb, mt, lane, qu, qv);
         float* gw = reinterpret_cast<float*>(sm + SP::off_g) + warp * (kGBytes / 4);
-        if constexpr (MT == 1) {
+        if constexpr (GT) {
+            const float* gs = reinterpret_cast<const float*>(sm + SP::off_gt);
+            for (int s = 0; s < n_stages; ++s) {
+                const int slot = s % NS;
+                if (!mbar_wait(bar_full + 8 * slot, (s / NS) & 1)) { failed = true; break; }
+                const uint32_t base = sb + SP::off_slots + slot * SP::kSlot;
+                if (FUSED && direct && s == 0) {
+                    // the chunk stage: its rows (staged from k_new / v_new) go into the pool;
+                    // every chunk page is a valid block (that is what selected the direct stage)
+                    for (int idx = tid; idx < 2 * T * 8; idx += 32 * kConsumerWarps) {
+                        const int kv = idx >= T * 8;
+                        const int rem = idx - kv * T * 8;
+                        const int t = rem >> 3, c = rem & 7;
+                        const int p = C + t;
+                        const int lb = p / a.block_size;
+                        const uint4 val = *reinterpret_cast<const uint4*>(
+                            sm + SP::off_slots + slot * SP::kSlot + kv * kStageKeys * kRowBytes +
+                            swz128(t, c));
+                        *reinterpret_cast<uint4*>(
+                            (kv ? a.v_pool : a.k_pool) +
+                            ((static_cast<long long>(s_bt[lb]) * a.block_size + (p - lb * a.block_size)) *
+                                 a.H + h) * kHeadDim + c * 8) = val;
+                    }
+                }
+                const int kv = stage_valid(s) - 16 * warp;
+                if (kv > 0) {
+                    const int x0 = stage_j0(s) + 16 * warp + 16;   // table column of the slice
+                    warp_slice16_gt(acc, qu, base + 16 * warp * kRowBytes,
+                                    base + (kStageKeys + 16 * warp) * kRowBytes, gs + x0, a.gt_w,
+                                    (x0 & 1) == 0, kv, a.scale_log2, lane);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+            }
+        } else if constexpr (MT == 1) {
             // every stage: this warp's 16-key slice; its skew scratch overlays its K rows
             for (int s = 0; s < n_stages; ++s) {
                 const int slot = s % NS;
@@ -436,7 +511,14 @@ __global__ void __launch_bounds__(128) chunk_attn_f32_kernel(
 
 int g_smem_done[16][64];
 
-template <int MT, int NS, bool FUSED>
+// Dynamic shared memory of one CTA that still lets two CTAs share an SM.
+constexpr int kTwoCtaSmem = 112 * 1024;
+
+// Row stride (floats) of the position table for keys up to `cap`: every read and write stays
+// below cap + 32, and a stride of 8 mod 32 keeps the 8-byte reads of a slice conflict-free.
+inline int pos_table_stride(int cap) { return ((cap + 32 + 31) & ~31) + 8; }
+
+template <int MT, int NS, bool FUSED, bool GT>
 oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, void* k_pool,
                         void* v_pool, int num_blocks, int block_size, const int32_t* bt,
                         int mbps, const int32_t* cs, const void* u, const void* vb,
@@ -447,8 +529,11 @@ oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, voi
     const int box = block_size < kStageKeys ? block_size : kStageKeys;
     if (!encode_rows_bf16(&tm_q, q, static_cast<long long>(B) * T, H, Tile<MT>::Tp) ||
         !encode_rows_bf16(&tm_k, k_pool, static_cast<long long>(num_blocks) * block_size, H, box) ||
-        !encode_rows_bf16(&tm_v, v_pool, static_cast<long long>(num_blocks) * block_size, H, box) ||
-        !encode_rows_bf16(&tm_r, rel, R, H, Tile<MT>::RB))
+        !encode_rows_bf16(&tm_v, v_pool, static_cast<long long>(num_blocks) * block_size, H, box))
+        return OASR_ERR_INVALID_ARG;
+    if (GT)
+        tm_r = tm_k;   // unused: the table reads rel directly
+    else if (!encode_rows_bf16(&tm_r, rel, R, H, Tile<MT>::RB))
         return OASR_ERR_INVALID_ARG;
     if (FUSED) {
         // the chunk's rows as TMA sources for the direct chunk stage
@@ -461,8 +546,9 @@ oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, voi
     }
     unsigned* status = status_word();
     if (!status) return OASR_ERR_CUDA;
-    auto kern = chunk_attn_bf16_kernel<MT, NS, FUSED>;
-    constexpr int smem = ChunkSmem<MT, NS>::bytes;
+    auto kern = chunk_attn_bf16_kernel<MT, NS, FUSED, GT>;
+    const int gt_w = GT ? pos_table_stride(mbps * block_size) : 0;
+    const int smem = ChunkSmem<MT, NS, GT>::bytes + 16 * gt_w * 4;
     if (!ensure_smem(kern, smem, g_smem_done[slot])) return OASR_ERR_CUDA;
     ChunkArgs a;
     a.k_new = static_cast<const uint16_t*>(k_new);
@@ -473,6 +559,7 @@ oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, voi
     a.cache_seqlens = cs;
     a.pos_bias_u = static_cast<const uint16_t*>(u);
     a.pos_bias_v = static_cast<const uint16_t*>(vb);
+    a.rel = static_cast<const uint16_t*>(rel);
     a.out = static_cast<uint16_t*>(out);
     a.status = status;
     a.num_blocks = num_blocks;
@@ -482,6 +569,7 @@ oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, voi
     a.H = H;
     a.R = R;
     a.box_rows = box;
+    a.gt_w = gt_w;
     a.scale_log2 = scale * 1.4426950408889634f;
     return launch_pdl(kern, dim3(static_cast<unsigned>(B) * H), dim3(kThreads), smem, stream, tm_q,
                       tm_k, tm_v, tm_r, tm_kn, tm_vn, a);
@@ -522,15 +610,25 @@ oasr_status dispatch(const void* q, const void* k_new, const void* v_new, void* 
         return launch_status();
     }
     const int f = FUSED ? 8 : 0;
+    // one m-tile: the position table when each consumer warp's share of it comes from one
+    // batch of rel loads (a second batch would wait a further L2 round trip before the first
+    // stage can be consumed; measured slower than the band on 528-key histories), else the
+    // per-stage band
+    const long long cap = static_cast<long long>(mbps) * block_size;
+    if (T <= 16 && cap + 15 <= 8LL * kConsumerWarps * kPosBatch &&
+        ChunkSmem<1, 4, true>::bytes + 64 * pos_table_stride(static_cast<int>(cap)) <= kTwoCtaSmem)
+        return launch_bf16<1, 4, FUSED, true>(q, k_new, v_new, k_pool, v_pool, num_blocks,
+                                              block_size, bt, mbps, cs, u, vb, rel, R, out, B, T,
+                                              H, scale, stream, f + 3);
     if (T <= 16)
-        return launch_bf16<1, 4, FUSED>(q, k_new, v_new, k_pool, v_pool, num_blocks, block_size,
-                                        bt, mbps, cs, u, vb, rel, R, out, B, T, H, scale, stream,
-                                        f + 0);
+        return launch_bf16<1, 4, FUSED, false>(q, k_new, v_new, k_pool, v_pool, num_blocks,
+                                               block_size, bt, mbps, cs, u, vb, rel, R, out, B, T,
+                                               H, scale, stream, f + 0);
     if (T <= 32)
-        return launch_bf16<2, 3, FUSED>(q, k_new, v_new, k_pool, v_pool, num_blocks, block_size,
+        return launch_bf16<2, 3, FUSED, false>(q, k_new, v_new, k_pool, v_pool, num_blocks, block_size,
                                         bt, mbps, cs, u, vb, rel, R, out, B, T, H, scale, stream,
                                         f + 1);
-    return launch_bf16<4, 2, FUSED>(q, k_new, v_new, k_pool, v_pool, num_blocks, block_size, bt,
+    return launch_bf16<4, 2, FUSED, false>(q, k_new, v_new, k_pool, v_pool, num_blocks, block_size, bt,
                                     mbps, cs, u, vb, rel, R, out, B, T, H, scale, stream, f + 2);
 }
 
