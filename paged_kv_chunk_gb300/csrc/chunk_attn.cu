@@ -99,10 +99,29 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     const int T = a.T;
     unsigned err = 0;
 
+    // The tensor maps are launch parameters no grid writes: their descriptors are fetched
+    // while the previous grid on the stream drains.
+    if (tid == 0) prefetch_tensormap(&tm_q);
+    if (warp == kConsumerWarps && lane == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        if (!GT) prefetch_tensormap(&tm_r);
+        if (FUSED) {
+            prefetch_tensormap(&tm_kn);
+            prefetch_tensormap(&tm_vn);
+        }
+    }
     // Launched with programmatic stream serialization: everything the previous grid on the
     // stream wrote is visible once this returns, and nothing global is read before it.
     grid_dep_wait();
     int C = __ldg(a.cache_seqlens + b);
+    // The whole block-table row (mbps <= kMaxPages, host check), not just the pages of the
+    // K keys: its loads go out beside the cache length's instead of after it.
+    int* s_bt = reinterpret_cast<int*>(sm + SP::off_bt);
+    if (!GT || warp == kConsumerWarps) {   // GT: the producer warp alone, so no rel load delays it
+        for (int i = GT ? lane : tid; i < a.mbps; i += GT ? 32 : kThreads)
+            s_bt[i] = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + i);
+    }
     if (C < 0) { C = 0; err |= kErrBounds; }
     int K = C + T;
     const int cap = a.mbps * a.block_size;
@@ -116,7 +135,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     float* s_vb = reinterpret_cast<float*>(sm + SP::off_vb);
     __shared__ int s_failed;
 
-    int* s_bt = reinterpret_cast<int*>(sm + SP::off_bt);
     if (tid == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(bar_full + 8 * i, 1);
@@ -139,11 +157,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
             s_u[tid] = bf16_lo(__ldg(a.pos_bias_u + h * kHeadDim + tid));
         else
             s_vb[tid - kHeadDim] = bf16_lo(__ldg(a.pos_bias_v + h * kHeadDim + tid - kHeadDim));
-    }
-    const int n_pages = (K + a.block_size - 1) / a.block_size;   // <= kMaxPages (host check)
-    if (!GT || warp == kConsumerWarps) {   // GT: the producer warp alone, so no rel load delays it
-        for (int i = GT ? lane : tid; i < n_pages; i += GT ? 32 : kThreads)
-            s_bt[i] = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + i);
     }
     __syncthreads();
 
@@ -212,15 +225,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     const bool producer = warp == kConsumerWarps;
     if (producer) {
         // The producer warp only issues copies: no other work shares its warp.
-        if (lane == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-            if (!GT) prefetch_tensormap(&tm_r);
-            if (direct) {
-                prefetch_tensormap(&tm_kn);
-                prefetch_tensormap(&tm_vn);
-            }
-        }
         // without the direct chunk stage, stages from this one on hold chunk rows
         const int first_chunk_stage = (FUSED && !direct) ? C / kStageKeys : n_stages;
         for (int issued = 0; issued < n_stages; ++issued) {

@@ -65,6 +65,12 @@ __global__ void __launch_bounds__(kPThreads, 1) project_tc_kernel(
     const uint32_t bar_drain = bar_acc_free + 16;                // issuer's MMAs all finished
     const int ksteps = a.d / kPK;
 
+    if (warp == 5 && lane == 0) {   // launch parameters: fetched before the previous grid ends
+        prefetch_tensormap(&tm_x);
+        prefetch_tensormap(&tm_wqkv);
+        prefetch_tensormap(&tm_pos);
+        prefetch_tensormap(&tm_wpos);
+    }
     if (tid == 0) {
         for (int i = 0; i < kPStages; ++i) {
             mbar_init(bar_full + 8 * i, 1);
@@ -109,10 +115,6 @@ __global__ void __launch_bounds__(kPThreads, 1) project_tc_kernel(
     if (warp == 5) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            prefetch_tensormap(&tm_x);
-            prefetch_tensormap(&tm_wqkv);
-            prefetch_tensormap(&tm_pos);
-            prefetch_tensormap(&tm_wpos);
             int i = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < a.tiles && ok; t += gridDim.x) {
