@@ -65,17 +65,19 @@ struct ChunkSmem {
     static constexpr int kSlot = 2 * kStageKeys * kRowBytes + kBand;
     static constexpr int off_slots = 0;
     static constexpr int off_q = NS * kSlot;
-    static constexpr int off_g = off_q + TL::Tp * kRowBytes;
+    static constexpr int off_ck = off_q + TL::Tp * kRowBytes;   // GT: the chunk's K|V rows
+    static constexpr int off_g = off_ck + (GT ? 2 * 16 * kRowBytes : 0);
     static constexpr int off_u = off_g + (MT == 1 ? 0 : kConsumerWarps * kGBytes);
     static constexpr int off_vb = off_u + kHeadDim * 4;
     static constexpr int off_bt = off_vb + kHeadDim * 4;    // the stream's block-table row
-    static constexpr int off_bar = off_bt + kMaxPages * 4;  // full[NS], empty[NS], q, written
-    static constexpr int off_gt = (off_bar + (2 * NS + 2) * 8 + 15) & ~15;
+    static constexpr int off_bar = off_bt + kMaxPages * 4;  // full[NS], empty[NS], q, written, chunk
+    static constexpr int off_gt = (off_bar + (2 * NS + 3) * 8 + 15) & ~15;
     static constexpr int bytes = off_gt + 1024;   // + 16 * gt_w * 4 with GT
     static constexpr int comb_o = 0;
     static constexpr int comb_m = comb_o + TL::KG * TL::Tp * kOW * 4;
     static constexpr int comb_l = comb_m + TL::KG * TL::Tp * 4;
-    static_assert(kSlot % 1024 == 0 && off_q % 1024 == 0, "TMA tiles need 1024-byte alignment");
+    static_assert(kSlot % 1024 == 0 && off_q % 1024 == 0 && off_ck % 1024 == 0,
+                  "TMA tiles need 1024-byte alignment");
     static_assert(!kGInBand || kGBytes <= kBand, "skew scratch must fit the band tile");
     static_assert(comb_l + TL::KG * TL::Tp * 4 <= NS * kSlot, "combine area");
 };
@@ -131,6 +133,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     const uint32_t bar_empty = bar_full + NS * 8;
     const uint32_t bar_q = bar_empty + NS * 8;
     const uint32_t bar_written = bar_q + 8;   // fused: the chunk is in the pool and fenced
+    const uint32_t bar_chunk = bar_written + 8;   // GT, fused: the chunk rows have landed
     float* s_u = reinterpret_cast<float*>(sm + SP::off_u);
     float* s_vb = reinterpret_cast<float*>(sm + SP::off_vb);
     __shared__ int s_failed;
@@ -143,11 +146,18 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         }
         mbar_init(bar_q, 1);
         mbar_init(bar_written, 32 * kConsumerWarps);
+        mbar_init(bar_chunk, 1);
         fence_mbar_init();
         s_failed = 0;
         // the Q tile needs no block-table entry: it is requested before the table row is read
         mbar_arrive_expect_tx(bar_q, TL::Tp * kRowBytes);
         tma_load_3d(sb + SP::off_q, &tm_q, bar_q, 0, h, b * T);
+        if (GT && FUSED) {
+            // nor do the chunk's rows (T <= 16: one 16-row box each for K and V)
+            mbar_arrive_expect_tx(bar_chunk, 2 * 16 * kRowBytes);
+            tma_load_3d(sb + SP::off_ck, &tm_kn, bar_chunk, 0, h, b * T);
+            tma_load_3d(sb + SP::off_ck + 16 * kRowBytes, &tm_vn, bar_chunk, 0, h, b * T);
+        }
     }
     // Position-table variant: u, v go out beside the block-table row (the producer warp
     // alone loads the row, and the table's rel rows are requested only once the row is in:
@@ -171,11 +181,15 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     }
     const int kc = direct ? C : K;                        // keys served from the pool
     const int n_pool = (kc + kStageKeys - 1) / kStageKeys;
-    const int n_stages = n_pool + (direct ? 1 : 0);
+    // direct: the chunk is stage 0 of the ring, or (GT) a region of its own loaded at the start
+    const bool chunk_stage = direct && !GT;
+    const int n_stages = n_pool + (chunk_stage ? 1 : 0);
     // stage s: first key and number of valid keys
-    auto stage_j0 = [&](int s) { return direct ? (s == 0 ? C : kStageKeys * (s - 1)) : kStageKeys * s; };
+    auto stage_j0 = [&](int s) {
+        return chunk_stage ? (s == 0 ? C : kStageKeys * (s - 1)) : kStageKeys * s;
+    };
     auto stage_valid = [&](int s) {
-        if (direct && s == 0) return T;
+        if (chunk_stage && s == 0) return T;
         const int left = kc - stage_j0(s);
         return left < kStageKeys ? left : kStageKeys;
     };
@@ -188,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         const uint32_t bar = bar_full + 8 * slot;
         const uint32_t base = sb + SP::off_slots + slot * SP::kSlot;
         const int j0 = stage_j0(s);
-        const bool chunk = direct && s == 0;
+        const bool chunk = chunk_stage && s == 0;
         const int box = chunk ? 16 : a.box_rows;
         const int nbox = chunk ? (T + 15) / 16
                                : min(kStageKeys / box, (kc - j0 + box - 1) / box);
@@ -287,6 +301,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         failed = !mbar_wait(bar_q, 0);
         if (!failed)
             pt.build(reinterpret_cast<float*>(sm + SP::off_gt), a.gt_w, sm + SP::off_q, s_vb);
+        // fused: the chunk's rows (requested at the start; they must land before the CTA
+        // ends even when the stages do not use them)
+        if (FUSED && !mbar_wait(bar_chunk, 0)) failed = true;
         named_bar_sync(1, 32 * kConsumerWarps);   // the table is complete
         if (!failed) make_q_frags(sb + SP::off_q, s_u, s_vb, mt, lane, qu, qv);
     } else {
@@ -303,28 +320,31 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         float* gw = reinterpret_cast<float*>(sm + SP::off_g) + warp * (kGBytes / 4);
         if constexpr (GT) {
             const float* gs = reinterpret_cast<const float*>(sm + SP::off_gt);
+            if (FUSED && direct) {
+                // the chunk, landed long before the first pool stage: its rows go into the pool
+                // (every chunk page is a valid block: that is what selected direct mode) and its
+                // keys are warp 0's first slice
+                for (int idx = tid; idx < 2 * T * 8; idx += 32 * kConsumerWarps) {
+                    const int kv = idx >= T * 8;
+                    const int rem = idx - kv * T * 8;
+                    const int t = rem >> 3, c = rem & 7;
+                    const int p = C + t;
+                    const int lb = p / a.block_size;
+                    const uint4 val = *reinterpret_cast<const uint4*>(
+                        sm + SP::off_ck + kv * 16 * kRowBytes + swz128(t, c));
+                    *reinterpret_cast<uint4*>(
+                        (kv ? a.v_pool : a.k_pool) +
+                        ((static_cast<long long>(s_bt[lb]) * a.block_size + (p - lb * a.block_size)) *
+                             a.H + h) * kHeadDim + c * 8) = val;
+                }
+                if (warp == 0)
+                    warp_slice16_gt(acc, qu, sb + SP::off_ck, sb + SP::off_ck + 16 * kRowBytes,
+                                    gs + C + 16, a.gt_w, ((C + 16) & 1) == 0, T, a.scale_log2, lane);
+            }
             for (int s = 0; s < n_stages; ++s) {
                 const int slot = s % NS;
                 if (!mbar_wait(bar_full + 8 * slot, (s / NS) & 1)) { failed = true; break; }
                 const uint32_t base = sb + SP::off_slots + slot * SP::kSlot;
-                if (FUSED && direct && s == 0) {
-                    // the chunk stage: its rows (staged from k_new / v_new) go into the pool;
-                    // every chunk page is a valid block (that is what selected the direct stage)
-                    for (int idx = tid; idx < 2 * T * 8; idx += 32 * kConsumerWarps) {
-                        const int kv = idx >= T * 8;
-                        const int rem = idx - kv * T * 8;
-                        const int t = rem >> 3, c = rem & 7;
-                        const int p = C + t;
-                        const int lb = p / a.block_size;
-                        const uint4 val = *reinterpret_cast<const uint4*>(
-                            sm + SP::off_slots + slot * SP::kSlot + kv * kStageKeys * kRowBytes +
-                            swz128(t, c));
-                        *reinterpret_cast<uint4*>(
-                            (kv ? a.v_pool : a.k_pool) +
-                            ((static_cast<long long>(s_bt[lb]) * a.block_size + (p - lb * a.block_size)) *
-                                 a.H + h) * kHeadDim + c * 8) = val;
-                    }
-                }
                 const int kv = stage_valid(s) - 16 * warp;
                 if (kv > 0) {
                     const int x0 = stage_j0(s) + 16 * warp + 16;   // table column of the slice
