@@ -407,27 +407,44 @@ struct PosTable {
             }
         }
         for (int nb0 = warp;;) {
-#pragma unroll
-            for (int u = 0; u < kPosBatch; ++u) {
-                const int nb = nb0 + u * nw;
-                if (nb >= ntiles()) break;
-                float c[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_bf16_16816(c, qa[0], bl[u].x, bl[u].y);
-                mma_bf16_16816(c, qa[1], bl[u].z, bl[u].w);
-                mma_bf16_16816(c, qa[2], bh[u].x, bh[u].y);
-                mma_bf16_16816(c, qa[3], bh[u].z, bh[u].w);
-                const int col = 8 * nb + 2 * t4;
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    if (col + e < ncols) {
-                        gs[g4 * W + col + e + g4 + 1] = c[e];
-                        gs[(g4 + 8) * W + col + e + g4 + 9] = c[2 + e];
-                    }
-                }
-            }
+            // the batch's tiles as independent MMA chains (tiles past the table have zero rel
+            // rows and store nothing); a short batch runs the half-size version
+            if (nb0 + (kPosBatch / 2) * nw < ntiles())
+                tiles<kPosBatch>(gs, W, qa, nb0);
+            else
+                tiles<kPosBatch / 2>(gs, W, qa, nb0);
             nb0 += kPosBatch * nw;
             if (nb0 >= ntiles()) break;
             load(nb0);
+        }
+    }
+
+    template <int N>
+    __device__ __forceinline__ void tiles(float* gs, int W, const uint32_t (&qa)[4][4], int nb0)
+    {
+        const int g4 = lane >> 2, t4 = lane & 3;
+        float c[N][4];
+#pragma unroll
+        for (int u = 0; u < N; ++u) {
+            c[u][0] = c[u][1] = c[u][2] = c[u][3] = 0.f;
+            mma_bf16_16816(c[u], qa[0], bl[u].x, bl[u].y);
+        }
+#pragma unroll
+        for (int u = 0; u < N; ++u) mma_bf16_16816(c[u], qa[1], bl[u].z, bl[u].w);
+#pragma unroll
+        for (int u = 0; u < N; ++u) mma_bf16_16816(c[u], qa[2], bh[u].x, bh[u].y);
+#pragma unroll
+        for (int u = 0; u < N; ++u) mma_bf16_16816(c[u], qa[3], bh[u].z, bh[u].w);
+#pragma unroll
+        for (int u = 0; u < N; ++u) {
+            const int col = 8 * (nb0 + u * nw) + 2 * t4;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                if (col + e < ncols) {
+                    gs[g4 * W + col + e + g4 + 1] = c[u][e];
+                    gs[(g4 + 8) * W + col + e + g4 + 9] = c[u][2 + e];
+                }
+            }
         }
     }
 };

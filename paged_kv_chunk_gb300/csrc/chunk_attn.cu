@@ -251,6 +251,27 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
             }
             issue(issued);
         }
+        if (GT && FUSED && direct) {
+            // with every stage out, the chunk's rows (in their own region) go into the pool;
+            // every chunk page is a valid block: that is what selected direct mode
+            if (mbar_wait(bar_chunk, 0)) {
+                for (int idx = lane; idx < 2 * T * 8; idx += 32) {
+                    const int kv = idx >= T * 8;
+                    const int rem = idx - kv * T * 8;
+                    const int t = rem >> 3, c = rem & 7;
+                    const int p = C + t;
+                    const int lb = p / a.block_size;
+                    const uint4 val = *reinterpret_cast<const uint4*>(
+                        sm + SP::off_ck + kv * 16 * kRowBytes + swz128(t, c));
+                    *reinterpret_cast<uint4*>(
+                        (kv ? a.v_pool : a.k_pool) +
+                        ((static_cast<long long>(s_bt[lb]) * a.block_size + (p - lb * a.block_size)) *
+                             a.H + h) * kHeadDim + c * 8) = val;
+                }
+            } else {
+                err |= kErrTimeout;
+            }
+        }
         if (err) atomicOr(a.status, err);
         return;
     }
@@ -321,22 +342,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         if constexpr (GT) {
             const float* gs = reinterpret_cast<const float*>(sm + SP::off_gt);
             if (FUSED && direct) {
-                // the chunk, landed long before the first pool stage: its rows go into the pool
-                // (every chunk page is a valid block: that is what selected direct mode) and its
-                // keys are warp 0's first slice
-                for (int idx = tid; idx < 2 * T * 8; idx += 32 * kConsumerWarps) {
-                    const int kv = idx >= T * 8;
-                    const int rem = idx - kv * T * 8;
-                    const int t = rem >> 3, c = rem & 7;
-                    const int p = C + t;
-                    const int lb = p / a.block_size;
-                    const uint4 val = *reinterpret_cast<const uint4*>(
-                        sm + SP::off_ck + kv * 16 * kRowBytes + swz128(t, c));
-                    *reinterpret_cast<uint4*>(
-                        (kv ? a.v_pool : a.k_pool) +
-                        ((static_cast<long long>(s_bt[lb]) * a.block_size + (p - lb * a.block_size)) *
-                             a.H + h) * kHeadDim + c * 8) = val;
-                }
+                // the chunk, landed long before the first pool stage: its keys are warp 0's
+                // first slice (the producer warp writes its rows into the pool)
                 if (warp == 0)
                     warp_slice16_gt(acc, qu, sb + SP::off_ck, sb + SP::off_ck + 16 * kRowBytes,
                                     gs + C + 16, a.gt_w, ((C + 16) & 1) == 0, T, a.scale_log2, lane);
