@@ -256,11 +256,26 @@ def cpu_baseline(cfg, seconds):
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return {"value": cfg.B * cfg.T * n / el, "unit": UNIT, "cores": oracle.num_threads(),
+    cores = oracle.num_threads()
+    # the same on one thread, on a shorter sample
+    oracle.set_num_threads(1)
+    n1, t1 = 0, time.perf_counter()
+    try:
+        while True:
+            oracle_layer_step(oracle, cfg, x, kp, vp)
+            n1 += 1
+            el1 = time.perf_counter() - t1
+            if el1 >= seconds / 2:
+                break
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": cfg.B * cfg.T * n / el, "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": f"{n} layer steps (append + chunk attention of all {cfg.B} streams x "
                       f"{cfg.H} heads, one layer) of the {cfg.name} cohort, {el:.1f} s, "
-                      "fp64 C oracle with OpenMP"}
+                      "fp64 C oracle with OpenMP",
+            "single_thread": {"value": cfg.B * cfg.T * n1 / el1, "unit": UNIT, "cores": 1,
+                              "sample": f"{n1} layer steps, {el1:.1f} s"}}
 
 
 def run_reference(args, cfg, rank, world):
@@ -377,6 +392,35 @@ def run_ours(args, cfg, rank, world, local):
     value = frames / (ms_max / 1e3)
     launch_us = 1e3 * ms / (args.steps * layers)
 
+    # ---- one cold-L2 launch: layer 0's step alone, L2 overwritten (2x its size) before each
+    cold = None
+    if rank == 0:
+        flush = torch.empty(int(2 * L2_BYTES), dtype=torch.uint8, device=dev)
+        n_cold = 20
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_cold)]
+        kp, vp = pools[0]
+        u, vb, rel = params[0]
+        with torch.cuda.stream(stream):
+            for i in range(n_cold):
+                flush.fill_(i & 0xFF)
+                evs[i][0].record(stream)
+                if args.two_call:
+                    capi.oasr_paged_append(x_d[0, 1], x_d[0, 2], kp, vp, bt, cs)
+                    capi.oasr_chunk_relattn_paged(x_d[0, 0], kp, vp, bt, cs, u, vb, rel,
+                                                  out=out_d[0])
+                else:
+                    capi.oasr_chunk_step_paged(x_d[0, 0], x_d[0, 1], x_d[0, 2], kp, vp, bt, cs, u,
+                                               vb, rel, out=out_d[0])
+                evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        del flush
+        cold_us = float(np.median([1e3 * a.elapsed_time(b) for a, b in evs[3:]]))
+        cold = {"launch_us": cold_us, "achieved_gbs": touched / (cold_us * 1e-6) / 1e9,
+                "launches": n_cold - 3,
+                "how": "median of single eager launches of one layer's step, each after a "
+                       "write of 2x L2 on the same stream, CUDA events around the launch"}
+
     # ---- end to end: pinned host inputs -> device, the step, outputs -> pinned host
     e2e = None
     if not args.no_e2e:
@@ -438,7 +482,8 @@ def run_ours(args, cfg, rank, world, local):
                      "kernel": ("paged_append_kernel + chunk_attn_bf16_kernel" if args.two_call
                                 else "chunk_attn_bf16_kernel (fused append + attention)"),
                      "algorithmic_bytes_per_launch": touched,
-                     "avg_launch_us": launch_us, "peak_kind": peak_kind},
+                     "avg_launch_us": launch_us, "peak_kind": peak_kind,
+                     **({"cold_l2": {**cold, "frac": cold["achieved_gbs"] / peak}} if cold else {})},
         "gpu_launches": args.steps * (layers * (2 if args.two_call else 1) + (1 if cfg.window else 0)),
         "clocks": clocks,
     }

@@ -92,6 +92,8 @@ def _load():
                                                       I, I, P, L, P]
         lib.oracle_num_threads.restype = I
         lib.oracle_num_threads.argtypes = []
+        lib.oracle_set_num_threads.restype = None
+        lib.oracle_set_num_threads.argtypes = [I]
         _lib = lib
         return lib
 
@@ -108,6 +110,11 @@ def _ptr(a: np.ndarray):
 def num_threads() -> int:
     """Threads the compiled oracle uses (OpenMP max threads, or 1)."""
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads for the oracle's later calls (for timing; the results do not depend on it)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def paged_append(k_new, v_new, k_pool, v_pool, block_table, cache_seqlens) -> int:

@@ -271,6 +271,17 @@ int oracle_num_threads(void)
 #endif
 }
 
+/* Threads for the oracle's later parallel regions (timing only; results do not depend on
+ * it: every output element is computed by one thread in a fixed order). */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* Chunked-limited packed attention: the packed attention restricted, per query, to the
  * keys of its own chunk and the `left` chunks before it (chunk = cs frames of the
  * segment).  Every key of the segment is tested against that condition. */
