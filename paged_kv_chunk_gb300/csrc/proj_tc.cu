@@ -32,7 +32,8 @@ struct ProjSmem {
     static constexpr int stage = 2 * tile;                  // A | W
     static constexpr int off_ring = 0;
     static constexpr int off_misc = kPStages * stage;       // tmem base, abort flag
-    static constexpr int off_bar = off_misc + 64;
+    static constexpr int off_bias = off_misc + 64;          // [4 warps][128] fp32 tile bias
+    static constexpr int off_bar = off_bias + 4 * kPN * 4;
     static constexpr int n_bars = 2 * kPStages + 2 + 2 + 1;
     static constexpr int bytes = off_bar + n_bars * 8 + 1024;
 };
@@ -179,11 +180,23 @@ __global__ void __launch_bounds__(kPThreads, 1) project_tc_kernel(
     } else {
         // --------------------------------------------------------------- epilogue
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+        float* s_bias = reinterpret_cast<float*>(sm + SP::off_bias) + warp * kPN;   // this warp's
         int lt = 0;
         for (int t = blockIdx.x; t < a.tiles; t += gridDim.x, ++lt) {
             int g, mt, nt;
             decode(t, g, mt, nt);
             const int buf = lt & 1;
+            // the tile's 128 bias values, four per lane, requested before the accumulator is
+            // waited for (the previous tile's reads of them are this warp's own, done)
+            {
+                float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (g == 0) {
+                    const uint2 w = __ldg(reinterpret_cast<const uint2*>(a.bias + nt * kPN) + lane);
+                    b4 = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+                }
+                *reinterpret_cast<float4*>(s_bias + 4 * lane) = b4;
+                __syncwarp();
+            }
             const bool ok = __all_sync(0xffffffffu, wait_or_abort(bar_acc_full + 8 * buf, (lt >> 1) & 1, s_abort));
             if (!ok) break;
             tc_fence_after();
@@ -196,28 +209,23 @@ __global__ void __launch_bounds__(kPThreads, 1) project_tc_kernel(
                 tmem_wait_ld();
                 const int col = nt * kPN + 32 * c;    // column of the problem's output
                 float bias[32];
-                if (g == 0) {
-                    const uint4* bp = reinterpret_cast<const uint4*>(a.bias + col);
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const uint4 w = __ldg(bp + q4);
-                        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            bias[8 * q4 + 2 * e] = bf16_lo(ww[e]);
-                            bias[8 * q4 + 2 * e + 1] = bf16_hi(ww[e]);
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) bias[j] = 0.f;
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 b4 = *reinterpret_cast<const float4*>(s_bias + 32 * c + j);
+                    bias[j] = b4.x;
+                    bias[j + 1] = b4.y;
+                    bias[j + 2] = b4.z;
+                    bias[j + 3] = b4.w;
                 }
                 if (row < M) {
                     // q, k or v by the column's third (d is a multiple of 128, so a tile
                     // never straddles two of them); rel for the positional problem
                     const int which = g ? 3 : col / a.d;
                     const int cw = g ? col : col - which * a.d;
-                    uint4* dst = reinterpret_cast<uint4*>(a.out[which] + static_cast<long long>(row) * a.d + cw);
+                    // a select rather than an indexed read keeps the parameter array out of
+                    // local memory
+                    uint16_t* ob = which == 0 ? a.out[0] : which == 1 ? a.out[1] : which == 2 ? a.out[2] : a.out[3];
+                    uint4* dst = reinterpret_cast<uint4*>(ob + static_cast<long long>(row) * a.d + cw);
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint32_t p[4];
