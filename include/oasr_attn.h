@@ -218,6 +218,16 @@ const char* oasr_status_string(oasr_status status);
  */
 oasr_status oasr_device_status(unsigned* flags, int clear);
 
+/*
+ * Diagnostic (the pages have no counterpart): run the library's bounded pipeline wait on a
+ * barrier that nothing ever signals, with a limit of limit_us microseconds (1 .. 2000000),
+ * on `stream`.  One CTA of one warp; when the wait runs out it raises the timeout bit of the
+ * device status word and returns, as a kernel of the library does when a copy it waits for
+ * never lands.  The context stays usable.  Returns OASR_ERR_INVALID_ARG for a limit outside
+ * the range (nothing is launched), OASR_ERR_CUDA if the launch fails.
+ */
+oasr_status oasr_selftest_wait(unsigned limit_us, cudaStream_t stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int oasr_version(void);
 

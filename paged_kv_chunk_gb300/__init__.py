@@ -9,8 +9,9 @@ build raises.
 """
 from .capi import (OasrError, oasr_chunk_relattn_paged, oasr_chunk_step_paged,  # noqa: F401
                    oasr_device_status, oasr_packed_relattn_chunked, oasr_packed_relattn_varlen,
-                   oasr_paged_append, oasr_project_qkv_pos, oasr_version, oasr_window_commit)
+                   oasr_paged_append, oasr_project_qkv_pos, oasr_selftest_wait, oasr_version,
+                   oasr_window_commit)
 
 __all__ = ["OasrError", "oasr_paged_append", "oasr_chunk_relattn_paged", "oasr_chunk_step_paged",
            "oasr_packed_relattn_varlen", "oasr_packed_relattn_chunked", "oasr_window_commit",
-           "oasr_project_qkv_pos", "oasr_device_status", "oasr_version"]
+           "oasr_project_qkv_pos", "oasr_device_status", "oasr_selftest_wait", "oasr_version"]

@@ -9,6 +9,7 @@ path, and a missing library raises instead of falling back.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 import re
 import threading
@@ -65,6 +66,8 @@ def load() -> ctypes.CDLL:
         L.oasr_device_status.restype = I
         L.oasr_version.argtypes = []
         L.oasr_version.restype = I
+        L.oasr_selftest_wait.argtypes = [ctypes.c_uint, S]
+        L.oasr_selftest_wait.restype = I
         _lib = L
         return L
 
@@ -277,3 +280,33 @@ def oasr_device_status(clear: bool = True) -> int:
 
 def oasr_version() -> int:
     return int(load().oasr_version())
+
+
+def oasr_selftest_wait(limit_us: int = 20000, stream=None) -> None:
+    """Diagnostic: the library's bounded wait on a barrier that nothing signals.  It runs
+    out after ``limit_us`` microseconds and raises the timeout bit (2) of the device status
+    word, as any of the library's kernels does when a copy it waits for never lands."""
+    _check("oasr_selftest_wait", load().oasr_selftest_wait(int(limit_us), _stream(stream)))
+
+
+# NVTX ranges around every call into the library, for Nsight timelines: set OASR_NVTX=1
+# before the import.
+NVTX = os.environ.get("OASR_NVTX", "") == "1"
+
+
+def _traced(fn):
+    @functools.wraps(fn)
+    def wrapper(*args, **kwargs):
+        torch.cuda.nvtx.range_push(fn.__name__)
+        try:
+            return fn(*args, **kwargs)
+        finally:
+            torch.cuda.nvtx.range_pop()
+    return wrapper
+
+
+if NVTX:
+    for _name in ("oasr_paged_append", "oasr_chunk_relattn_paged", "oasr_chunk_step_paged",
+                  "oasr_packed_relattn_varlen", "oasr_packed_relattn_chunked", "oasr_window_commit",
+                  "oasr_project_qkv_pos", "oasr_selftest_wait"):
+        globals()[_name] = _traced(globals()[_name])

@@ -3,6 +3,7 @@
 #include <mutex>
 
 #include "host_common.h"
+#include "ptx.cuh"
 
 namespace oasr {
 
@@ -78,7 +79,34 @@ bool encode_rows_bf16(CUtensorMap* map, const void* base, long long rows, int H,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
+// A wait on a barrier that no thread or copy ever signals: it runs out after limit_ns and
+// takes the path every pipeline wait of the library takes when it runs out.
+__global__ void __launch_bounds__(32) selftest_wait_kernel(uint64_t limit_ns, unsigned* status)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_addr(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const bool ok = mbar_wait(b, 0, limit_ns);
+    if (threadIdx.x == 0 && !ok) atomicOr(status, kErrTimeout);
+}
+}  // namespace
+
 }  // namespace oasr
+
+extern "C" oasr_status oasr_selftest_wait(unsigned limit_us, cudaStream_t stream)
+{
+    using namespace oasr;
+    if (limit_us < 1 || limit_us > 2000000) return OASR_ERR_INVALID_ARG;
+    unsigned* status = status_word();
+    if (!status) return OASR_ERR_CUDA;
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(static_cast<uint64_t>(limit_us) * 1000ull, status);
+    return launch_status();
+}
 
 extern "C" const char* oasr_status_string(oasr_status s)
 {

@@ -18,7 +18,7 @@ def test_exports_every_header_symbol(lib):
     assert {"oasr_paged_append", "oasr_chunk_relattn_paged", "oasr_chunk_step_paged",
             "oasr_packed_relattn_varlen", "oasr_packed_relattn_chunked", "oasr_window_commit",
             "oasr_project_qkv_pos", "oasr_status_string",
-            "oasr_device_status",
+            "oasr_device_status", "oasr_selftest_wait",
             "oasr_version"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in the header but not exported"
@@ -165,3 +165,27 @@ def test_binding_raises_on_cpu_tensors():
         capi.oasr_paged_append(x, x, torch.zeros(16, 16, 4, 64), torch.zeros(16, 16, 4, 64),
                                torch.zeros(2, 8, dtype=torch.int32),
                                torch.zeros(2, dtype=torch.int32))
+
+
+@pytest.mark.parametrize("limit_us", [0, 2000001])
+def test_selftest_wait_rejects_bad_limits(lib, limit_us):
+    assert lib.oasr_selftest_wait(limit_us, None) == capi.OASR_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("flag", ["1", ""])
+def test_nvtx_ranges_are_opt_in(flag):
+    """With OASR_NVTX=1 every library call of the binding is wrapped in an NVTX range;
+    otherwise the binding's functions are the plain ones."""
+    import os
+    import subprocess
+    import sys
+    code = ("from paged_kv_chunk_gb300 import capi\n"
+            "names = ['oasr_paged_append', 'oasr_chunk_relattn_paged', 'oasr_chunk_step_paged',"
+            " 'oasr_packed_relattn_varlen', 'oasr_packed_relattn_chunked', 'oasr_window_commit',"
+            " 'oasr_project_qkv_pos', 'oasr_selftest_wait']\n"
+            "print(sum(hasattr(getattr(capi, n), '__wrapped__') for n in names))\n")
+    env = dict(os.environ, OASR_NVTX=flag)
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "-c", code], env=env, cwd=root, check=True,
+                         capture_output=True, text=True).stdout.split()
+    assert int(out[-1]) == (8 if flag == "1" else 0)
