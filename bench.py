@@ -77,13 +77,14 @@ def parse_args():
 
 
 def workload_bytes(cfg, fused=True):
-    """Algorithmic HBM bytes of one layer step (one launch of the fused kernel)."""
+    """Algorithmic HBM bytes of one layer step (one launch of the fused kernel); a
+    heterogeneous cohort reads each stream's own cache length."""
     es = 2 if cfg.dtype == "bf16" else 4
     row = cfg.H * cfg.D * es
     chunk = cfg.B * cfg.T * row
     b = 2 * chunk                       # read k_new, v_new
     b += 2 * chunk                      # write them into the pools
-    b += 2 * cfg.B * cfg.C * row        # read the cached K/V
+    b += 2 * int(syn.cache_lengths(cfg).sum()) * row   # read the cached K/V
     if not fused:
         b += 2 * chunk                  # re-read the appended chunk
     b += chunk                          # read q
@@ -231,17 +232,25 @@ def max_over_ranks(x, world):
 
 def oracle_layer_inputs(cfg, seed):
     x = syn.streaming_inputs(cfg, seed)
+    x["cache_seqlens"] = syn.cache_lengths(cfg)   # a heterogeneous cohort's own lengths
     kp = syn.canary_pool(x["num_blocks"], cfg.block_size, cfg.H, cfg.D, cfg.dtype)
     vp = kp.copy()
     return x, kp, vp
 
 
 def oracle_layer_step(oracle, cfg, x, kp, vp):
-    """One layer step on the CPU oracle: append the chunk, then chunk attention."""
+    """One layer step on the CPU oracle: append the chunk, then chunk attention (stream by
+    stream over its own cache length in a heterogeneous cohort)."""
     oracle.paged_append(syn.to_bits(x["k_new"], cfg.dtype), syn.to_bits(x["v_new"], cfg.dtype),
                         kp, vp, x["block_table"], x["cache_seqlens"])
-    oracle.chunk_relattn(x["q"], x["cache_k"], x["cache_v"], x["k_new"], x["v_new"],
-                         x["pos_bias_u"], x["pos_bias_v"], x["rel"])
+    if not cfg.hetero:
+        oracle.chunk_relattn(x["q"], x["cache_k"], x["cache_v"], x["k_new"], x["v_new"],
+                             x["pos_bias_u"], x["pos_bias_v"], x["rel"])
+        return
+    for b, c in enumerate(x["cache_seqlens"]):
+        s = slice(b, b + 1)
+        oracle.chunk_relattn(x["q"][s], x["cache_k"][s, :c], x["cache_v"][s, :c], x["k_new"][s],
+                             x["v_new"][s], x["pos_bias_u"], x["pos_bias_v"], x["rel"])
 
 
 def cpu_baseline(cfg, seconds):
@@ -297,7 +306,8 @@ def run_reference(args, cfg, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": f"{cfg.name}_streaming", "B": cfg.B, "H": cfg.H, "D": cfg.D,
-                   "T": cfg.T, "cache": cfg.C, "block_size": cfg.block_size, "layers": 1},
+                   "T": cfg.T, "cache": (f"U{{0..{cfg.C}}} per stream" if cfg.hetero else cfg.C),
+                   "block_size": cfg.block_size, "layers": 1},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
                          "kind": "oracle",
                          "sample": f"each step: one layer (append + chunk attention) of the "
@@ -333,7 +343,7 @@ def run_ours(args, cfg, rank, world, local):
     params = [(dev_normal((H, D)), dev_normal((H, D)), dev_normal((cfg.R, H, D)))
               for _ in range(layers)]
     bt_h = syn.block_table(rng, B, cfg.mbps, nb)
-    cs_h = np.full((B,), cfg.C, np.int32)
+    cs_h = syn.cache_lengths(cfg)
     bt = torch.from_numpy(bt_h).to(dev)
     cs = torch.from_numpy(cs_h).to(dev)
     # per-step inputs of every layer (q, k_new, v_new) and outputs, device-resident
@@ -525,7 +535,9 @@ def run_ours(args, cfg, rank, world, local):
         "config": {"workload": f"{cfg.name}_streaming", "B": B, "H": H, "D": D, "T": T,
                    **({"window_frames": cfg.window, "commit": "oasr_window_commit once per step"}
                       if cfg.window else {}),
-                   "cache": cfg.C, "block_size": bs, "pool_blocks": nb, "rel_rows": cfg.R,
+                   "cache": (f"U{{0..{cfg.C}}} per stream (mean {cs_h.mean():.1f})" if cfg.hetero
+                             else cfg.C),
+                   "block_size": bs, "pool_blocks": nb, "rel_rows": cfg.R,
                    "layers": layers, "global_batch": B * world, "seq_len": cfg.K,
                    "parallelism": f"dp{world}",
                    "l2": f"inputs larger than L2: {layers} distinct layer pools, "

@@ -36,6 +36,7 @@ class StreamingConfig:
     num_blocks: int | None = None          # default: twice the demand
     max_blocks_per_seq: int | None = None  # default: pages needed for C + T keys
     window: int = 0                        # > 0: trained window (frames); steps commit with eviction
+    hetero: bool = False                   # per-stream cache lengths U{0..C} (cache_lengths)
 
     @property
     def K(self) -> int:
@@ -94,7 +95,20 @@ PACKED = PackedConfig("packed_varlen", num_seqs=256, min_len=50, max_len=1500, H
 WINDOW_RING = StreamingConfig("window_ring", B=32, H=8, D=64, T=16, C=64, block_size=16,
                               dtype="bf16", seed=1010, window=64)
 
-STREAMING_CONFIGS = {c.name: c for c in (TINY, SMALL, LARGE, WINDOW_RING) + SWEEP}
+# The Conformer-small cohort at heterogeneous offsets (streams that joined at different
+# times, one launch): stream b's cache length is drawn from U{0..256}, one table for all.
+HETERO = StreamingConfig("hetero_small", B=64, H=4, D=64, T=16, C=256, block_size=16,
+                         dtype="bf16", seed=1011, hetero=True)
+
+STREAMING_CONFIGS = {c.name: c for c in (TINY, SMALL, LARGE, WINDOW_RING, HETERO) + SWEEP}
+
+
+def cache_lengths(cfg: StreamingConfig) -> np.ndarray:
+    """int32 [B]: every stream's cache length (C, or U{0..C} per stream for a heterogeneous
+    cohort, seeded by the config)."""
+    if not cfg.hetero:
+        return np.full((cfg.B,), cfg.C, np.int32)
+    return np.random.default_rng(cfg.seed + 17).integers(0, cfg.C + 1, cfg.B).astype(np.int32)
 
 
 def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
