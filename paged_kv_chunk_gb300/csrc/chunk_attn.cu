@@ -116,19 +116,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
     // Launched with programmatic stream serialization: everything the previous grid on the
     // stream wrote is visible once this returns, and nothing global is read before it.
     grid_dep_wait();
-    int C = __ldg(a.cache_seqlens + b);
-    // The whole block-table row (mbps <= kMaxPages, host check), not just the pages of the
-    // K keys: its loads go out beside the cache length's instead of after it.
-    int* s_bt = reinterpret_cast<int*>(sm + SP::off_bt);
-    if (!GT || warp == kConsumerWarps) {   // GT: the producer warp alone, so no rel load delays it
-        for (int i = GT ? lane : tid; i < a.mbps; i += GT ? 32 : kThreads)
-            s_bt[i] = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + i);
-    }
-    if (C < 0) { C = 0; err |= kErrBounds; }
-    int K = C + T;
-    const int cap = a.mbps * a.block_size;
-    if (K > cap) { K = cap; err |= kErrBounds; }
-    const int off = a.R - T - C;   // rho = off + j - i
     const uint32_t bar_full = sb + SP::off_bar;
     const uint32_t bar_empty = bar_full + NS * 8;
     const uint32_t bar_q = bar_empty + NS * 8;
@@ -149,7 +136,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         mbar_init(bar_chunk, 1);
         fence_mbar_init();
         s_failed = 0;
-        // the Q tile needs no block-table entry: it is requested before the table row is read
+        // the Q tile needs neither the cache length nor the block table: it is requested
+        // before either is read
         mbar_arrive_expect_tx(bar_q, TL::Tp * kRowBytes);
         tma_load_3d(sb + SP::off_q, &tm_q, bar_q, 0, h, b * T);
         if (GT && FUSED) {
@@ -158,6 +146,14 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
             tma_load_3d(sb + SP::off_ck, &tm_kn, bar_chunk, 0, h, b * T);
             tma_load_3d(sb + SP::off_ck + 16 * kRowBytes, &tm_vn, bar_chunk, 0, h, b * T);
         }
+    }
+    int C = __ldg(a.cache_seqlens + b);
+    // The whole block-table row (mbps <= kMaxPages, host check), not just the pages of the
+    // K keys: its loads go out beside the cache length's instead of after it.
+    int* s_bt = reinterpret_cast<int*>(sm + SP::off_bt);
+    if (!GT || warp == kConsumerWarps) {   // GT: the producer warp alone, so no rel load delays it
+        for (int i = GT ? lane : tid; i < a.mbps; i += GT ? 32 : kThreads)
+            s_bt[i] = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + i);
     }
     // Position-table variant: u, v go out beside the block-table row (the producer warp
     // alone loads the row, and the table's rel rows are requested only once the row is in:
@@ -168,6 +164,11 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         else
             s_vb[tid - kHeadDim] = bf16_lo(__ldg(a.pos_bias_v + h * kHeadDim + tid - kHeadDim));
     }
+    if (C < 0) { C = 0; err |= kErrBounds; }
+    int K = C + T;
+    const int cap = a.mbps * a.block_size;
+    if (K > cap) { K = cap; err |= kErrBounds; }
+    const int off = a.R - T - C;   // rho = off + j - i
     __syncthreads();
 
     // Stage plan (every thread derives the same one from the cached table row).
