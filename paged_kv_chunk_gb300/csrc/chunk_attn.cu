@@ -642,12 +642,11 @@ oasr_status dispatch(const void* q, const void* k_new, const void* v_new, void* 
         return launch_status();
     }
     const int f = FUSED ? 8 : 0;
-    // one m-tile: the position table when each consumer warp's share of it comes from one
-    // batch of rel loads (a second batch would wait a further L2 round trip before the first
-    // stage can be consumed; measured slower than the band on 528-key histories), else the
-    // per-stage band
+    // one m-tile: the position table when it fits beside four stages with two CTAs per SM
+    // (histories up to 544 keys; a table past 320 columns takes each warp a second batch of
+    // rel loads, still faster than the band on 528-key histories), else the per-stage band
     const long long cap = static_cast<long long>(mbps) * block_size;
-    if (T <= 16 && cap + 15 <= 8LL * kConsumerWarps * kPosBatch &&
+    if (T <= 16 && cap <= 4096 &&
         ChunkSmem<1, 4, true>::bytes + 64 * pos_table_stride(static_cast<int>(cap)) <= kTwoCtaSmem)
         return launch_bf16<1, 4, FUSED, true>(q, k_new, v_new, k_pool, v_pool, num_blocks,
                                               block_size, bt, mbps, cs, u, vb, rel, R, out, B, T,

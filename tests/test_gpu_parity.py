@@ -157,8 +157,10 @@ EDGE = [
     (3, 1, 16, 100, 16, 0, "bf16"),    # one head per CTA
     (2, 6, 9, 70, 32, 0, "bf16"),      # two heads per CTA
     (2, 4, 16, 530, 32, 0, "bf16"),    # key range split in two, ragged
-    (2, 2, 16, 288, 8, 0, "bf16"),     # the largest whole-CTA position table (304 keys)
-    (2, 2, 16, 290, 8, 0, "bf16"),     # one page more: the per-stage band
+    (2, 2, 16, 288, 8, 0, "bf16"),     # a whole-CTA position table from one batch of rel loads
+    (2, 2, 16, 290, 8, 0, "bf16"),     # one page more: a second batch
+    (2, 2, 16, 528, 8, 0, "bf16"),     # the largest table that fits (544 keys)
+    (2, 2, 16, 530, 8, 0, "bf16"),     # one page past it: the per-stage band
     (2, 2, 11, 61, 16, 4, "bf16"),     # odd chunk start: unaligned table reads; longer table
     (2, 2, 5, 77, 8, 2, "f32"),
     (2, 3, 40, 33, 16, 0, "f32"),
