@@ -5,50 +5,52 @@
 // cache_seqlens afterwards.  Row t of stream b lands at logical position
 // p = cache_seqlens[b] + t: block block_table[b][p / block_size], slot p % block_size.
 //
-// One thread moves one 16-byte vector; consecutive threads cover consecutive vectors of
-// a head row, so both the chunk reads and the pool writes are coalesced 128-byte (bf16)
-// or 256-byte (fp32) row segments.
+// One warp moves one frame of one tensor: its H heads are contiguous both in the chunk and
+// in the pool row, so the reads and the writes are coalesced H * 128-byte (bf16) or
+// H * 256-byte (fp32) rows.
 #include "host_common.h"
 #include "ptx.cuh"
 
 namespace oasr {
 namespace {
 
+// One warp per (K or V, stream b, frame t): it reads the frame's H heads (H * vpr 16-byte
+// vectors, contiguous in k_new / v_new) and writes them into the pool row of position
+// cache_seqlens[b] + t (also contiguous: a pool row holds all heads of one frame).
 __global__ void __launch_bounds__(256) paged_append_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, uint4* __restrict__ k_pool,
     uint4* __restrict__ v_pool, int num_blocks, int block_size,
     const int32_t* __restrict__ block_table, int mbps, const int32_t* __restrict__ cache_seqlens,
-    int T, int H, int vpr, long long n_vec, unsigned* status)
+    int B, int T, int row_vecs, unsigned* status)
 {
     grid_dep_wait();     // the previous grid on the stream has finished (programmatic launch)
+    const int rows = B * T;   // per tensor (host check: 2 * rows fits an int)
+    const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     unsigned err = 0;
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-         idx < 2 * n_vec; idx += stride) {
-        const bool is_v = idx >= n_vec;
-        const long long e = is_v ? idx - n_vec : idx;       // vector index in [B,T,H,vpr]
-        const long long row = e / vpr;                     // (b*T + t)*H + h
-        const int c = static_cast<int>(e - row * vpr);
-        const int h = static_cast<int>(row % H);
-        const long long bt_ = row / H;
-        const int t = static_cast<int>(bt_ % T);
-        const int b = static_cast<int>(bt_ / T);
+    if (w < 2 * rows) {
+        const bool is_v = w >= rows;
+        const int r = is_v ? w - rows : w;   // b * T + t
+        const int b = r / T, t = r - (r / T) * T;
         const long long p = static_cast<long long>(__ldg(cache_seqlens + b)) + t;
         const long long lb = p / block_size;
-        if (p < 0 || lb >= mbps) { err |= kErrBounds; continue; }
-        const int slot = static_cast<int>(p - lb * block_size);
-        const int blk = __ldg(block_table + static_cast<long long>(b) * mbps + lb);
-        if (blk < 0 || blk >= num_blocks) { err |= kErrBounds; continue; }
-        const long long dst =
-            ((static_cast<long long>(blk) * block_size + slot) * H + h) * vpr + c;
-        if (is_v)
-            v_pool[dst] = __ldg(v_new + e);
-        else
-            k_pool[dst] = __ldg(k_new + e);
+        int blk = -1;
+        if (p < 0 || lb >= mbps) {
+            err = kErrBounds;
+        } else {
+            blk = __ldg(block_table + static_cast<long long>(b) * mbps + lb);
+            if (blk < 0 || blk >= num_blocks) err = kErrBounds;
+        }
+        if (!err) {
+            const long long dst = (static_cast<long long>(blk) * block_size + (p - lb * block_size)) * row_vecs;
+            const long long src = static_cast<long long>(r) * row_vecs;
+            const uint4* in = is_v ? v_new : k_new;
+            uint4* out = is_v ? v_pool : k_pool;
+            for (int c = lane; c < row_vecs; c += 32) out[dst + c] = __ldg(in + src + c);
+        }
     }
     // this thread's copies are issued: the next grid may schedule (it waits for this one)
     grid_dep_trigger();
-    if (err) atomicOr(status, err);
+    if (err && lane == 0) atomicOr(status, err);
 }
 
 }  // namespace
@@ -71,16 +73,14 @@ extern "C" oasr_status oasr_paged_append(const void* k_new, const void* v_new, v
     if ((D * es) % 16 != 0) return OASR_ERR_UNSUPPORTED;
     if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
         return OASR_ERR_INVALID_ARG;
+    if (2LL * B * T > 0x7fffffffLL / 32) return OASR_ERR_UNSUPPORTED;
     unsigned* status = status_word();
-    const int sms = sm_count();
-    if (!status || !sms) return OASR_ERR_CUDA;
-    const int vpr = D * es / 16;
-    const long long n_vec = static_cast<long long>(B) * T * H * vpr;
-    long long blocks = (2 * n_vec + 255) / 256;
-    if (blocks > 16LL * sms) blocks = 16LL * sms;
-    return launch_pdl(paged_append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
-                      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+    if (!status) return OASR_ERR_CUDA;
+    const int row_vecs = H * D * es / 16;   // 16-byte vectors of one frame (all heads)
+    const int warps = 2 * B * T;
+    return launch_pdl(paged_append_kernel, dim3(static_cast<unsigned>((warps + 7) / 8)), dim3(256), 0,
+                      stream, static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
                       static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), num_blocks,
-                      block_size, block_table, max_blocks_per_seq, cache_seqlens, T, H, vpr, n_vec,
+                      block_size, block_table, max_blocks_per_seq, cache_seqlens, B, T, row_vecs,
                       status);
 }
