@@ -454,7 +454,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     // colg + 32c ... colg + 32c + 63, staged as two 32-column blocks
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
-                        if (c == 1) {
+                        // for c = 1, rr still holds block 1 (loaded for chunk 0's upper half);
+                        // the unmasked kernel reloads it rather than keep it live across chunk
+                        // 0's reads (measured faster there, slower in the masked one)
+                        if (c == 1 && !MASKED) {
                             OASR_TMEM_LD32(tl + colg + 32, rr);
                             tmem_wait_ld();
                         }
