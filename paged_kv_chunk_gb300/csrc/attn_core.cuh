@@ -1,13 +1,15 @@
-// Per-warp attention unit shared by the streaming (paged) and packed (varlen) bf16
-// kernels: 16 query rows of one head against one stage of 64 keys.
+// Per-warp attention units of the streaming (paged) bf16 kernel: 16 query rows of one head
+// against one stage of 64 keys, or against a 16-key slice of it.
 //
 // A CTA has kConsumerWarps consumer warps and one producer warp.  The producer streams
-// stages of 64 keys (K rows, V rows and the rel band they need) into a ring of smem
-// slots with TMA, completing a `full` mbarrier per slot; consumers release a slot by
-// arriving on its `empty` mbarrier.  Consumer warp w owns m-tile (w % MT) of the CTA's
-// Tp = 16*MT query rows and the stages s with s % KG == w / MT (KG = 4/MT), so each warp
-// works on whole stages (warp_stage); with one m-tile the four warps instead split every
-// stage into 16-key slices (warp_slice16).  Per unit of work:
+// stages of 64 keys (K rows, V rows and, without the position table, the rel band they
+// need) into a ring of smem slots with TMA, completing a `full` mbarrier per slot;
+// consumers release a slot by arriving on its `empty` mbarrier.  Consumer warp w owns
+// m-tile (w % MT) of the CTA's Tp = 16*MT query rows and the stages s with
+// s % KG == w / MT (KG = 4/MT), so each warp works on whole stages (warp_stage); with one
+// m-tile the four warps instead split every stage into 16-key slices (warp_slice16, or
+// warp_slice16_gt when the CTA has built its whole position term as a pre-skewed table,
+// PosTable).  Per unit of work (the band form; with the table, G is read from it):
 //
 //   S  = bf16(q+u) . K^T                       mma.sync m16n8k16, fp32 accumulators
 //   G  = bf16(q+v) . Rband^T                   80 band columns for the 64 keys

@@ -11,15 +11,21 @@
 // bf16 path (the hot path): one CTA per (stream, head), 4 consumer warps and a TMA
 // producer warp.  Keys are streamed in stages of 64 through a TMA pipeline: each stage is
 // one box per block-table page for K and for V (the page's rows of this head, 128 B each,
-// 128-byte swizzled) plus one box of the rel band; all arrive on one mbarrier.  The
-// per-stage math is in attn_core.cuh.
+// 128-byte swizzled), all arriving on one mbarrier.  The position term comes one of two
+// ways.  Position table (GT; T <= 16 and a history that fits): the consumer warps compute
+// the CTA's whole term once, from rel rows read from L2, into a pre-skewed fp32 table in
+// shared memory while the first pages are in flight, and every 16-key slice reads it back.
+// Band (otherwise): each stage also carries a box of the rel band, and each slice or stage
+// multiplies it and skews the product through shared memory.  The per-slice and per-stage
+// math is in attn_core.cuh.
 // Fused variant (append + attention): when every page the chunk lands in is a valid block
-// of the table, stage 0 is the chunk itself, read by TMA straight from k_new / v_new, and
-// the pool stages cover only the cached keys [0, C); the consumers write the chunk into
-// the pool meanwhile, a side effect no stage of this launch reads.  Otherwise (a chunk past
-// the table or in an invalid block) the stages cover [0, C + T) from the pool and those
-// holding the chunk are issued only after the consumers' 16-byte stores of it are fenced
-// against the async proxy, so the error handling of the append applies unchanged.
+// of the table ("direct" mode) the chunk is read by TMA straight from k_new / v_new (with
+// the position table into a region of its own at kernel start, else as stage 0), the pool
+// stages cover only the cached keys [0, C), and the chunk is written into the pool
+// meanwhile, a side effect no stage of this launch reads.  Otherwise (a chunk past the
+// table or in an invalid block) the stages cover [0, C + T) from the pool and those holding
+// the chunk are issued only after the consumers' 16-byte stores of it are fenced against
+// the async proxy, so the error handling of the append applies unchanged.
 //
 // f32 path: a SIMT kernel (one warp per query row, lanes over keys, fp32 FMA and expf).
 #include "attn_core.cuh"
@@ -47,12 +53,13 @@ struct ChunkArgs {
 };
 
 // Shared-memory plan of the streaming kernel (byte offsets from a 1024-aligned base).
-// Slot i holds one stage: K rows [64][128 B], V rows [64][128 B], rel band [RB][128 B], all
-// 128-byte swizzled by TMA.  With one m-tile the skew scratch of the consuming warp reuses
-// the slot's band tile; otherwise each consumer warp has its own scratch.  After the key
-// loop the slots hold the cross-warp combine.
-// Position-table variant (GT, one m-tile): no band in the slots; the CTA's whole position
-// term, 16 rows of gt_w floats, follows the barriers (its size is set at launch).
+// Slot i holds one stage: K rows [64][128 B], V rows [64][128 B] and, for the band, rel
+// band rows [RB][128 B], all 128-byte swizzled by TMA.  With one m-tile a warp's skew
+// scratch overlays its own K rows of the slot (dead once its scores are formed); with 2 or
+// 4 m-tiles each consumer warp has its own scratch.  After the key loop the slots hold the
+// cross-warp combine.  Position-table variant (GT, one m-tile): no band in the slots, a
+// 4 KB region for the chunk's rows, and the CTA's whole position term, 16 rows of gt_w
+// floats, after the barriers (its size is set at launch).
 // Block-table entries a CTA caches in shared memory.
 constexpr int kMaxPages = 512;
 
@@ -60,7 +67,6 @@ template <int MT, int NS, bool GT>
 struct ChunkSmem {
     using TL = Tile<MT>;
     static_assert(!GT || MT == 1, "the position table serves one m-tile");
-    static constexpr bool kGInBand = MT == 1 && !GT;
     static constexpr int kBand = GT ? 0 : TL::RB * kRowBytes;
     static constexpr int kSlot = 2 * kStageKeys * kRowBytes + kBand;
     static constexpr int off_slots = 0;
@@ -78,7 +84,6 @@ struct ChunkSmem {
     static constexpr int comb_l = comb_m + TL::KG * TL::Tp * 4;
     static_assert(kSlot % 1024 == 0 && off_q % 1024 == 0 && off_ck % 1024 == 0,
                   "TMA tiles need 1024-byte alignment");
-    static_assert(!kGInBand || kGBytes <= kBand, "skew scratch must fit the band tile");
     static_assert(comb_l + TL::KG * TL::Tp * 4 <= NS * kSlot, "combine area");
 };
 
@@ -388,13 +393,8 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
             if (!mbar_wait(bar_full + 8 * slot, (s / NS) & 1)) { failed = true; break; }
             const uint32_t base = sb + SP::off_slots + slot * SP::kSlot;
             const uint32_t band = base + 2 * kStageKeys * kRowBytes;
-            float* g = SP::kGInBand
-                           ? reinterpret_cast<float*>(sm + SP::off_slots + slot * SP::kSlot +
-                                                      2 * kStageKeys * kRowBytes)
-                           : gw;
             warp_stage(acc, qu, qv, base, base + kStageKeys * kRowBytes, band,
-                       TL::Tp - 16 - 16 * mt, g, stage_valid(s), a.scale_log2, lane);
-            if (SP::kGInBand) fence_proxy_async_smem();   // the next TMA into this slot
+                       TL::Tp - 16 - 16 * mt, gw, stage_valid(s), a.scale_log2, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
         }
