@@ -141,10 +141,15 @@ def measured_hbm_peak():
 
 
 def source_digest(sources=None):
+    """Digest of the kernel sources' code: comments and blank space are dropped first, so a
+    comment edit does not void a profile taken on the same code."""
     h = hashlib.sha256()
     for name in (sources or KERNEL_SOURCES):
-        with open(os.path.join(ROOT, "paged_kv_chunk_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "paged_kv_chunk_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
