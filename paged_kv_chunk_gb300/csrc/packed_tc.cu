@@ -477,7 +477,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                                     make_uint4(rr[4 * k], rr[4 * k + 1], rr[4 * k + 2], rr[4 * k + 3]);
                         __syncwarp();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) sc[32 * c + j] += stg[31 - lane + j];
+                        for (int j = 0; j < 32; j += 2) {   // two scores per packed add
+                            const float2 r2 = __fadd2_rn(make_float2(sc[32 * c + j], sc[32 * c + j + 1]),
+                                                         make_float2(stg[31 - lane + j], stg[32 - lane + j]));
+                            sc[32 * c + j] = r2.x;
+                            sc[32 * c + j + 1] = r2.y;
+                        }
                         __syncwarp();
                     }
                 }
@@ -541,21 +546,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     OASR_TMEM_ST16(tl + kColP + 32 * hf, zero);
                     OASR_TMEM_ST16(tl + kColP + 32 * hf + 16, zero);
                 } else {
-                    float ps0 = 0.f, ps1 = 0.f;
+                    float2 ps = make_float2(0.f, 0.f);
+                    const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+                    const float2 nm2 = make_float2(-mref, -mref);
 #pragma unroll
                     for (int q2 = 0; q2 < 2; ++q2) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const float p0 = ex2_approx(fmaf(sc[32 * q2 + 2 * j], a.scale_log2, -mref));
-                            const float p1 = ex2_approx(fmaf(sc[32 * q2 + 2 * j + 1], a.scale_log2, -mref));
-                            ps0 += p0;
-                            ps1 += p1;
-                            pk[j] = pack_bf16(p0, p1);
+                            // the exponents' scale-and-shift and the row sums two at a time
+                            const float2 e2 = __ffma2_rn(
+                                make_float2(sc[32 * q2 + 2 * j], sc[32 * q2 + 2 * j + 1]), sc2, nm2);
+                            const float2 p2 = make_float2(ex2_approx(e2.x), ex2_approx(e2.y));
+                            ps = __fadd2_rn(ps, p2);
+                            pk[j] = pack_bf16(p2.x, p2.y);
                         }
                         OASR_TMEM_ST16(tl + kColP + 32 * hf + 16 * q2, pk);
                     }
-                    l_sum += ps0 + ps1;
+                    l_sum += ps.x + ps.y;
                 }
                 // V rows past the segment belong to the next one: zero them so that P = 0
                 // there never meets a non-finite value
