@@ -499,13 +499,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 // scale (log2 domain), mask keys this row does not see, this half's max
                 // scores stay unscaled here: the scale (> 0, its sign is folded into q+u and
                 // q+v) is applied to the row max and inside the exponent's FFMA
-                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+                // (three-input max: two scores per instruction)
+                float mx0 = -INFINITY, mx1 = -INFINITY;
                 if (!live) {
                 } else if (ka <= 0 && kb >= 64) {
 #pragma unroll
                     for (int j = 0; j < 64; j += 4) {
-                        mx0 = fmaxf(mx0, sc[j]); mx1 = fmaxf(mx1, sc[j + 1]);
-                        mx2 = fmaxf(mx2, sc[j + 2]); mx3 = fmaxf(mx3, sc[j + 3]);
+                        mx0 = fmax3(mx0, sc[j], sc[j + 1]);
+                        mx1 = fmax3(mx1, sc[j + 2], sc[j + 3]);
                     }
                 } else {
 #pragma unroll
@@ -513,11 +514,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             sc[j + e] = (j + e >= ka && j + e < kb) ? sc[j + e] : -INFINITY;
-                        mx0 = fmaxf(mx0, sc[j]); mx1 = fmaxf(mx1, sc[j + 1]);
-                        mx2 = fmaxf(mx2, sc[j + 2]); mx3 = fmaxf(mx3, sc[j + 3]);
+                        mx0 = fmax3(mx0, sc[j], sc[j + 1]);
+                        mx1 = fmax3(mx1, sc[j + 2], sc[j + 3]);
                     }
                 }
-                float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2, mx_other;
+                float mx = fmaxf(mx0, mx1) * a.scale_log2, mx_other;
                 pair_post(mx);
                 // P.V of the previous stage must be done before P and O are touched
                 if (s > 0 && !warp_wait(bar_pv_done, (g - 1) & 1)) { ok = false; break; }

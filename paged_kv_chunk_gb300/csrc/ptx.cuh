@@ -38,6 +38,14 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
+// max(a, b, c) in one instruction (a NaN operand is ignored, as with fmaxf).
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Programmatic dependent launch: wait until the previous grid on the stream has finished and
 // its writes are visible (a no-op when launched without the attribute), and let the next
 // grid start scheduling its CTAs.
