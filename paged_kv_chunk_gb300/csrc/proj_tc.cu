@@ -22,37 +22,41 @@
 namespace oasr {
 namespace {
 
-constexpr int kPM = 128, kPN = 128, kPK = 64;   // output tile, K step
+constexpr int kPM = 128, kPK = 64;   // output tile rows, K step (the tile's width PN is 128 or 64)
 constexpr int kPStages = 4;
-constexpr int kPThreads = 192;                  // warps 0-3 epilogue, 4 MMA, 5 TMA
-constexpr int kPTmemCols = 256;                 // two 128-column accumulators
+constexpr int kPThreads = 192;       // warps 0-3 epilogue, 4 MMA, 5 TMA
 
+template <int PN>
 struct ProjSmem {
-    static constexpr int tile = kPM * kRowBytes;            // 16 KB (128 rows x 64 bf16)
-    static constexpr int stage = 2 * tile;                  // A | W
+    static constexpr int tile = kPM * kRowBytes;            // A: 16 KB (128 rows x 64 bf16)
+    static constexpr int tile_w = PN * kRowBytes;           // W: PN rows x 64 bf16
+    static constexpr int stage = tile + tile_w;
     static constexpr int off_ring = 0;
     static constexpr int off_misc = kPStages * stage;       // tmem base, abort flag
-    static constexpr int off_bias = off_misc + 64;          // [4 warps][128] fp32 tile bias
-    static constexpr int off_bar = off_bias + 4 * kPN * 4;
+    static constexpr int off_bias = off_misc + 64;          // [4 warps][PN] fp32 tile bias
+    static constexpr int off_bar = off_bias + 4 * PN * 4;
     static constexpr int n_bars = 2 * kPStages + 2 + 2 + 1;
     static constexpr int bytes = off_bar + n_bars * 8 + 1024;
+    static constexpr int tmem_cols = 2 * PN;                // two accumulators
+    static_assert(tile % 1024 == 0 && tile_w % 1024 == 0, "TMA tiles need 1024-byte alignment");
 };
 
 struct ProjArgs {
     const uint16_t* bias;   // [3 d] for the q/k/v problem
     uint16_t* out[4];       // q, k, v ([M0, d] each), rel ([M1, d])
     int M0, M1, d;          // rows of x, rows of pos_emb, d_model (the K of both problems)
-    int nt0, nt1;           // n-tiles per row tile: 3 d / 128, d / 128
+    int nt0, nt1;           // n-tiles per row tile: 3 d / PN, d / PN
     int tiles0, tiles;      // tiles of the q/k/v problem, of both
     unsigned* status;
 };
 
+template <int PN>
 __global__ void __launch_bounds__(kPThreads, 1) project_tc_kernel(
     const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wqkv,
     const __grid_constant__ CUtensorMap tm_pos, const __grid_constant__ CUtensorMap tm_wpos,
     const ProjArgs a)
 {
-    using SP = ProjSmem;
+    using SP = ProjSmem<PN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_addr(sm);
@@ -88,7 +92,7 @@ __global__ void __launch_bounds__(kPThreads, 1) project_tc_kernel(
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(s_tmem)),
-                     "r"(kPTmemCols));
+                     "r"(SP::tmem_cols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     tc_fence_before();
@@ -132,7 +136,7 @@ __global__ void __launch_bounds__(kPThreads, 1) project_tc_kernel(
                     const uint32_t bar = bar_full + 8 * slot;
                     mbar_arrive_expect_tx(bar, SP::stage);
                     tma_load_3d(base, g ? &tm_pos : &tm_x, bar, 0, kb, mt * kPM);
-                    tma_load_3d(base + SP::tile, g ? &tm_wpos : &tm_wqkv, bar, 0, kb, nt * kPN);
+                    tma_load_3d(base + SP::tile, g ? &tm_wpos : &tm_wqkv, bar, 0, kb, nt * PN);
                 }
             }
             // no copy may still be landing when the CTA exits
@@ -142,7 +146,7 @@ __global__ void __launch_bounds__(kPThreads, 1) project_tc_kernel(
     } else if (warp == 4) {
         // ------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t id = idesc(kPM, kPN, 0);
+            constexpr uint32_t id = idesc(kPM, PN, 0);
             int i = 0, lt = 0, nacc = 0, nfree = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < a.tiles && ok; t += gridDim.x, ++lt) {
@@ -159,7 +163,7 @@ __global__ void __launch_bounds__(kPThreads, 1) project_tc_kernel(
                     const uint32_t base = sb + SP::off_ring + slot * SP::stage;
 #pragma unroll
                     for (int k = 0; k < kPK / 16; ++k)
-                        umma_ss(tmem + buf * kPN, sdesc(base + 32 * k), sdesc(base + SP::tile + 32 * k), id,
+                        umma_ss(tmem + buf * PN, sdesc(base + 32 * k), sdesc(base + SP::tile + 32 * k), id,
                                 (kb > 0 || k > 0) ? 1 : 0);
                     umma_commit(bar_empty + 8 * slot);
                     ++nfree;
@@ -180,34 +184,41 @@ __global__ void __launch_bounds__(kPThreads, 1) project_tc_kernel(
     } else {
         // --------------------------------------------------------------- epilogue
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
-        float* s_bias = reinterpret_cast<float*>(sm + SP::off_bias) + warp * kPN;   // this warp's
+        float* s_bias = reinterpret_cast<float*>(sm + SP::off_bias) + warp * PN;   // this warp's
         int lt = 0;
         for (int t = blockIdx.x; t < a.tiles; t += gridDim.x, ++lt) {
             int g, mt, nt;
             decode(t, g, mt, nt);
             const int buf = lt & 1;
-            // the tile's 128 bias values, four per lane, requested before the accumulator is
+            // the tile's PN bias values, PN / 32 per lane, requested before the accumulator is
             // waited for (the previous tile's reads of them are this warp's own, done)
-            {
+            if constexpr (PN == 128) {
                 float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (g == 0) {
-                    const uint2 w = __ldg(reinterpret_cast<const uint2*>(a.bias + nt * kPN) + lane);
+                    const uint2 w = __ldg(reinterpret_cast<const uint2*>(a.bias + nt * PN) + lane);
                     b4 = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
                 }
                 *reinterpret_cast<float4*>(s_bias + 4 * lane) = b4;
-                __syncwarp();
+            } else {
+                float2 b2 = make_float2(0.f, 0.f);
+                if (g == 0) {
+                    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(a.bias + nt * PN) + lane);
+                    b2 = make_float2(bf16_lo(w), bf16_hi(w));
+                }
+                *reinterpret_cast<float2*>(s_bias + 2 * lane) = b2;
             }
+            __syncwarp();
             const bool ok = __all_sync(0xffffffffu, wait_or_abort(bar_acc_full + 8 * buf, (lt >> 1) & 1, s_abort));
             if (!ok) break;
             tc_fence_after();
             const int row = mt * kPM + 32 * warp + lane;
             const int M = g ? a.M1 : a.M0;
 #pragma unroll
-            for (int c = 0; c < kPN / 32; ++c) {
+            for (int c = 0; c < PN / 32; ++c) {
                 uint32_t r[32];
-                OASR_TMEM_LD32(tl + buf * kPN + 32 * c, r);
+                OASR_TMEM_LD32(tl + buf * PN + 32 * c, r);
                 tmem_wait_ld();
-                const int col = nt * kPN + 32 * c;    // column of the problem's output
+                const int col = nt * PN + 32 * c;     // column of the problem's output
                 float bias[32];
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
@@ -248,12 +259,43 @@ __global__ void __launch_bounds__(kPThreads, 1) project_tc_kernel(
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kPTmemCols));
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(SP::tmem_cols));
     }
     if (tid == 0 && *s_abort) atomicOr(a.status, kErrTimeout);
 }
 
-int g_smem_done_proj[64];
+int g_smem_done_proj[2][64];
+
+template <int PN>
+oasr_status launch_proj(const void* x, const void* w_qkv, const void* b_qkv, const void* pos_emb,
+                        const void* w_pos, void* q, void* k, void* v, void* rel, int M, int R,
+                        int d_model, int sms, unsigned* status, cudaStream_t stream)
+{
+    CUtensorMap tm_x, tm_wqkv, tm_pos, tm_wpos;
+    const int kb = d_model / kPK;   // the inputs as [rows, d/64, 64]
+    if (!encode_rows_bf16(&tm_x, x, M, kb, kPM) || !encode_rows_bf16(&tm_wqkv, w_qkv, 3LL * d_model, kb, PN) ||
+        !encode_rows_bf16(&tm_pos, pos_emb, R, kb, kPM) || !encode_rows_bf16(&tm_wpos, w_pos, d_model, kb, PN))
+        return OASR_ERR_INVALID_ARG;
+    constexpr int smem = ProjSmem<PN>::bytes;
+    if (!ensure_smem(project_tc_kernel<PN>, smem, g_smem_done_proj[PN == 64])) return OASR_ERR_CUDA;
+    ProjArgs a;
+    a.bias = static_cast<const uint16_t*>(b_qkv);
+    a.out[0] = static_cast<uint16_t*>(q);
+    a.out[1] = static_cast<uint16_t*>(k);
+    a.out[2] = static_cast<uint16_t*>(v);
+    a.out[3] = static_cast<uint16_t*>(rel);
+    a.M0 = M;
+    a.M1 = R;
+    a.d = d_model;
+    a.nt0 = 3 * d_model / PN;
+    a.nt1 = d_model / PN;
+    a.tiles0 = ((M + kPM - 1) / kPM) * a.nt0;
+    a.tiles = a.tiles0 + ((R + kPM - 1) / kPM) * a.nt1;
+    a.status = status;
+    const int grid = a.tiles < sms ? a.tiles : sms;
+    return launch_pdl(project_tc_kernel<PN>, dim3(grid), dim3(kPThreads), smem, stream, tm_x,
+                      tm_wqkv, tm_pos, tm_wpos, a);
+}
 
 }  // namespace
 }  // namespace oasr
@@ -268,35 +310,20 @@ extern "C" oasr_status oasr_project_qkv_pos(const void* x, const void* w_qkv, co
         return OASR_ERR_INVALID_ARG;
     if (M <= 0 || R <= 0 || d_model <= 0 || H <= 0) return OASR_ERR_INVALID_ARG;
     if (dt != OASR_BF16) return OASR_ERR_UNSUPPORTED;
-    if (d_model != H * kHeadDim || d_model % kPN) return OASR_ERR_UNSUPPORTED;
+    if (d_model != H * kHeadDim || d_model % 128) return OASR_ERR_UNSUPPORTED;
     const void* ptrs[] = {x, w_qkv, b_qkv, pos_emb, w_pos, q, k, v, rel};
     for (const void* p : ptrs)
         if (!aligned16(p)) return OASR_ERR_INVALID_ARG;
-    CUtensorMap tm_x, tm_wqkv, tm_pos, tm_wpos;
-    const int kb = d_model / kPK;   // the inputs as [rows, d/64, 64]
-    if (!encode_rows_bf16(&tm_x, x, M, kb, kPM) || !encode_rows_bf16(&tm_wqkv, w_qkv, 3LL * d_model, kb, kPN) ||
-        !encode_rows_bf16(&tm_pos, pos_emb, R, kb, kPM) || !encode_rows_bf16(&tm_wpos, w_pos, d_model, kb, kPN))
-        return OASR_ERR_INVALID_ARG;
     unsigned* status = status_word();
     const int sms = sm_count();
     if (!status || !sms) return OASR_ERR_CUDA;
-    constexpr int smem = ProjSmem::bytes;
-    if (!ensure_smem(project_tc_kernel, smem, g_smem_done_proj)) return OASR_ERR_CUDA;
-    ProjArgs a;
-    a.bias = static_cast<const uint16_t*>(b_qkv);
-    a.out[0] = static_cast<uint16_t*>(q);
-    a.out[1] = static_cast<uint16_t*>(k);
-    a.out[2] = static_cast<uint16_t*>(v);
-    a.out[3] = static_cast<uint16_t*>(rel);
-    a.M0 = M;
-    a.M1 = R;
-    a.d = d_model;
-    a.nt0 = 3 * d_model / kPN;
-    a.nt1 = d_model / kPN;
-    a.tiles0 = ((M + kPM - 1) / kPM) * a.nt0;
-    a.tiles = a.tiles0 + ((R + kPM - 1) / kPM) * a.nt1;
-    a.status = status;
-    const int grid = a.tiles < sms ? a.tiles : sms;
-    return launch_pdl(project_tc_kernel, dim3(grid), dim3(kPThreads), smem, stream, tm_x, tm_wqkv,
-                      tm_pos, tm_wpos, a);
+    // 128 x 128 output tiles, or 128 x 64 when the wide ones would leave most SMs idle (a
+    // small step is latency bound: twice the tiles at half the work each)
+    const long long tiles128 = ((M + kPM - 1LL) / kPM) * (3LL * d_model / 128) +
+                               ((R + kPM - 1LL) / kPM) * (d_model / 128LL);
+    if (2 * tiles128 <= sms)
+        return launch_proj<64>(x, w_qkv, b_qkv, pos_emb, w_pos, q, k, v, rel, M, R, d_model, sms,
+                               status, stream);
+    return launch_proj<128>(x, w_qkv, b_qkv, pos_emb, w_pos, q, k, v, rel, M, R, d_model, sms,
+                            status, stream);
 }
