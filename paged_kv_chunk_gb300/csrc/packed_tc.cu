@@ -49,6 +49,7 @@ constexpr int kColS = 0, kColG = 128, kColO = 384, kColP = 448;
 constexpr int kStgW = 68;                // staging row stride (floats): conflict-free both ways
 constexpr int kStgWarpBytes = 32 * kStgW * 4;
 constexpr int kStgOverlay = 5;           // warps whose staging overlays the stage's K and band tiles
+constexpr int kUvHeads = 32;             // pos_bias_u / v of up to this many heads live in smem
 
 struct TcSmem {
     static constexpr int k_tile = kBN * kRowBytes;               // 16 KB
@@ -66,10 +67,12 @@ struct TcSmem {
     static constexpr int off_xm = off_stg + (kSoftmaxWarps - kStgOverlay) * kStgWarpBytes;
     static constexpr int off_cu = off_xm + 2 * 2 * kBM * 4;      // [exchange parity][half][row]
     static constexpr int off_tile = off_cu + (kTcMaxSeqs + 1) * 4;
-    static constexpr int off_misc = off_tile + (kTcMaxSeqs + 1) * 4;   // wsum[16], tmem, abort
+    static constexpr int off_uv = (off_tile + (kTcMaxSeqs + 1) * 4 + 15) & ~15;   // u | v, bf16
+    static constexpr int off_misc = off_uv + 2 * kUvHeads * kRowBytes;   // wsum[16], tmem, abort
     static constexpr int off_bar = (off_misc + 128 + 7) & ~7;
     static constexpr int n_bars = 2 + 2 + 7 + 4 + 2;
     static constexpr int bytes = off_bar + n_bars * 8 + 1024;
+    static_assert(bytes <= 232448, "dynamic shared memory of one CTA");
 };
 
 struct TcArgs {
@@ -143,6 +146,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                      "r"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
+    // pos_bias_u and pos_bias_v of every head (when they fit), read per item by prep_q
+    const bool uv_smem = a.H <= kUvHeads;
+    uint4* s_uv = reinterpret_cast<uint4*>(sm + SP::off_uv);   // [u | v][head][8 x 16 B]
+    if (uv_smem)
+        for (int i = tid; i < 2 * a.H * 8; i += kTcThreads) {
+            const int which = i >= a.H * 8, rem = i - which * a.H * 8;
+            s_uv[which * kUvHeads * 8 + rem] =
+                __ldg(reinterpret_cast<const uint4*>(which ? a.pos_bias_v : a.pos_bias_u) + rem);
+        }
     // segment starts and the exclusive prefix of per-segment 128-row tile counts
     for (int i = tid; i <= ns; i += kTcThreads) {
         int c = __ldg(a.cu_seqlens + i);
@@ -193,13 +205,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
     // item -> segment start and length, first query of the tile, head, and the keys
     // [kl, kh) the tile's queries can see (the whole segment, or with the chunked-limited
     // window the chunks from the first query's window start to the last query's chunk)
-    auto decode = [&](long long item, int& start, int& L, int& i0, int& h, int& kl, int& kh) {
+    // The unmasked kernel finds the segment by scanning on from the caller's previous one
+    // (`seg`, starting at 0: each role visits its items in increasing order); the masked one,
+    // whose softmax warps have no register to spare for it, by binary search.
+    auto decode = [&](long long item, int& seg, int& start, int& L, int& i0, int& h, int& kl,
+                      int& kh) {
         const int tile = static_cast<int>(item / a.H);
         h = static_cast<int>(item - static_cast<long long>(tile) * a.H);
-        int lo = 0, hi = ns - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (s_tile[mid] <= tile) lo = mid; else hi = mid - 1;
+        int lo = 0;
+        if (!MASKED) {
+            while (seg + 1 < ns && s_tile[seg + 1] <= tile) ++seg;
+            lo = seg;
+        } else {
+            int hi = ns - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_tile[mid] <= tile) lo = mid; else hi = mid - 1;
+            }
         }
         start = s_cu[lo];
         L = s_cu[lo + 1] - start;
@@ -231,9 +253,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             const uint64_t pol = policy_evict_last();   // K/V tiles are re-read by every query tile
             int g = 0, itp = 0;
             bool ok = true;
+            int seg = 0;
             for (long long item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++itp) {
                 int start, L, i0, h, kl, kh;
-                decode(item, start, L, i0, h, kl, kh);
+                decode(item, seg, start, L, i0, h, kl, kh);
                 const int n_st = (kh - kl + kBN - 1) / kBN;
                 // the item's 128 q rows, once the softmax warps have read the previous ones
                 if (itp > 0 && !wait_or_abort(bar_qb_free, (itp - 1) & 1, s_abort)) {
@@ -286,10 +309,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             // so it overlaps this stage's softmax, and across items the next tile's first
             // products overlap the current tile's last stage and epilogue.
             long long item = blockIdx.x;
-            int n_st = 0, s = 0;
+            int n_st = 0, s = 0, seg = 0;
             auto item_stages = [&](long long itm) {
                 int start, L, i0, h, kl, kh;
-                decode(itm, start, L, i0, h, kl, kh);
+                decode(itm, seg, start, L, i0, h, kl, kh);
                 return (kh - kl + kBN - 1) / kBN;
             };
             bool ok = item < n_items;
@@ -376,12 +399,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             if (!warp_wait(bar_qb_full, itq & 1)) return false;
             const uint4* up = reinterpret_cast<const uint4*>(a.pos_bias_u + hq * kHeadDim);
             const uint4* vp = reinterpret_cast<const uint4*>(a.pos_bias_v + hq * kHeadDim);
+            const uint4* sup = s_uv + hq * 8;
+            const uint4* svp = s_uv + (kUvHeads + hq) * 8;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 const int c = 4 * hf + cc;
                 const uint32_t offs = static_cast<uint32_t>(r * kRowBytes + ((c ^ (r & 7)) << 4));
                 const uint4 qc = *reinterpret_cast<const uint4*>(sm + SP::off_qbuf + offs);
-                const uint4 uc = __ldg(up + c), vc = __ldg(vp + c);
+                const uint4 uc = uv_smem ? sup[c] : __ldg(up + c);
+                const uint4 vc = uv_smem ? svp[c] : __ldg(vp + c);
                 const uint32_t w[4] = {qc.x, qc.y, qc.z, qc.w};
                 const uint32_t wu[4] = {uc.x, uc.y, uc.z, uc.w};
                 const uint32_t wv[4] = {vc.x, vc.y, vc.z, vc.w};
@@ -404,15 +430,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             if (lane == 0) mbar_arrive(bar_q_ready);
             return true;
         };
-        int g = 0, it = 0, sg = 0;
+        int g = 0, it = 0, sg = 0, seg = 0;
         if (static_cast<long long>(blockIdx.x) < n_items) {
             int st0, L0, i00, h0, kl0, kh0;
-            decode(blockIdx.x, st0, L0, i00, h0, kl0, kh0);
+            decode(blockIdx.x, seg, st0, L0, i00, h0, kl0, kh0);
             if (!prep_q(0, h0)) *s_abort = 1;
         }
         for (long long item = blockIdx.x; item < n_items && !*s_abort; item += gridDim.x, ++it) {
             int start, L, i0, h, kl, kh;
-            decode(item, start, L, i0, h, kl, kh);
+            decode(item, seg, start, L, i0, h, kl, kh);
             const int n_st = (kh - kl + kBN - 1) / kBN;
             float m_used = -INFINITY, l_sum = 0.f;
             bool ok = true;
@@ -493,7 +519,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 // issued while this stage's softmax and the epilogue run
                 if (s + 1 == n_st && item + gridDim.x < n_items) {
                     int ns1, nL, ni0, nh, nkl, nkh;
-                    decode(item + gridDim.x, ns1, nL, ni0, nh, nkl, nkh);
+                    decode(item + gridDim.x, seg, ns1, nL, ni0, nh, nkl, nkh);
                     if (!warp_wait(bar_q_free, it & 1) || !prep_q(it + 1, nh)) { ok = false; break; }
                 }
                 // scale (log2 domain), mask keys this row does not see, this half's max
@@ -633,6 +659,7 @@ oasr_status launch_packed_tc(const void* q, const void* k, const void* v, const 
                              float scale, int cs, int left, cudaStream_t stream)
 {
     if (num_seqs > kTcMaxSeqs) return OASR_ERR_UNSUPPORTED;
+    if ((static_cast<long long>(total) / kBM + num_seqs) * H >= 0x7fffffffLL) return OASR_ERR_UNSUPPORTED;
     CUtensorMap tm_q, tm_k, tm_v, tm_r;
     if (!encode_rows_bf16(&tm_q, q, total, H, kBM) || !encode_rows_bf16(&tm_k, k, total, H, kBN) ||
         !encode_rows_bf16(&tm_v, v, total, H, kBN) ||
