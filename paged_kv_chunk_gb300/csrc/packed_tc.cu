@@ -436,6 +436,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             decode(blockIdx.x, seg, st0, L0, i00, h0, kl0, kh0);
             if (!prep_q(0, h0)) *s_abort = 1;
         }
+        // O rows of a finished item: wait for its last P.V, combine the pair's sums, store.
+        // It runs inside the next item's first stage, after that stage's S/G have been read,
+        // so the wait for the last P.V overlaps useful work.
+        auto epilogue = [&](int e_start, int e_L, int e_i0, int e_h, float e_l) {
+            if (!warp_wait(bar_pv_done, (g - 1) & 1)) return false;
+            float l_other;
+            pair_post(e_l);
+            if (!pair_collect(l_other)) return false;
+            const float l_row = e_l + l_other;
+            tc_fence_after();
+            uint32_t oo[32];
+            OASR_TMEM_LD32(tl + kColO + 32 * hf, oo);
+            tmem_wait_ld();
+            const int row = e_i0 + r;
+            if (row < e_L) {
+                const float inv = 1.f / l_row;
+                uint4* dst = reinterpret_cast<uint4*>(
+                                 a.out + (static_cast<long long>(e_start + row) * a.H + e_h) * kHeadDim) + 4 * hf;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    dst[c] = make_uint4(
+                        pack_bf16(__uint_as_float(oo[8 * c]) * inv, __uint_as_float(oo[8 * c + 1]) * inv),
+                        pack_bf16(__uint_as_float(oo[8 * c + 2]) * inv, __uint_as_float(oo[8 * c + 3]) * inv),
+                        pack_bf16(__uint_as_float(oo[8 * c + 4]) * inv, __uint_as_float(oo[8 * c + 5]) * inv),
+                        pack_bf16(__uint_as_float(oo[8 * c + 6]) * inv, __uint_as_float(oo[8 * c + 7]) * inv));
+            }
+            tc_fence_before();
+            return true;
+        };
+        int p_start = 0, p_L = 0, p_i0 = 0, p_h = 0;
+        float p_l = 0.f;
+        bool have_prev = false, all_ok = true;
         for (long long item = blockIdx.x; item < n_items && !*s_abort; item += gridDim.x, ++it) {
             int start, L, i0, h, kl, kh;
             decode(item, seg, start, L, i0, h, kl, kh);
@@ -521,6 +553,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     int ns1, nL, ni0, nh, nkl, nkh;
                     decode(item + gridDim.x, seg, ns1, nL, ni0, nh, nkl, nkh);
                     if (!warp_wait(bar_q_free, it & 1) || !prep_q(it + 1, nh)) { ok = false; break; }
+                }
+                // the previous item's O, now that this first stage's S/G are read
+                if (s == 0 && have_prev) {
+                    if (!epilogue(p_start, p_L, p_i0, p_h, p_l)) { ok = false; break; }
+                    have_prev = false;
                 }
                 // scale (log2 domain), mask keys this row does not see, this half's max
                 // scores stay unscaled here: the scale (> 0, its sign is folded into q+u and
@@ -609,32 +646,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_p_full);
             }
-            if (!ok) break;
-            // O half row of this tile: wait for the last P.V, combine the pair's sums, store
-            if (!warp_wait(bar_pv_done, (g - 1) & 1)) break;
-            float l_other;
-            pair_post(l_sum);
-            if (!pair_collect(l_other)) break;
-            const float l_row = l_sum + l_other;
-            tc_fence_after();
-            uint32_t oo[32];
-            OASR_TMEM_LD32(tl + kColO + 32 * hf, oo);
-            tmem_wait_ld();
-            const int row = i0 + r;
-            if (row < L) {
-                const float inv = 1.f / l_row;
-                uint4* dst = reinterpret_cast<uint4*>(
-                                 a.out + (static_cast<long long>(start + row) * a.H + h) * kHeadDim) + 4 * hf;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    dst[c] = make_uint4(
-                        pack_bf16(__uint_as_float(oo[8 * c]) * inv, __uint_as_float(oo[8 * c + 1]) * inv),
-                        pack_bf16(__uint_as_float(oo[8 * c + 2]) * inv, __uint_as_float(oo[8 * c + 3]) * inv),
-                        pack_bf16(__uint_as_float(oo[8 * c + 4]) * inv, __uint_as_float(oo[8 * c + 5]) * inv),
-                        pack_bf16(__uint_as_float(oo[8 * c + 6]) * inv, __uint_as_float(oo[8 * c + 7]) * inv));
-            }
-            tc_fence_before();
+            if (!ok) { all_ok = false; break; }
+            p_start = start;
+            p_L = L;
+            p_i0 = i0;
+            p_h = h;
+            p_l = l_sum;
+            have_prev = true;
         }
+        if (all_ok && have_prev && !*s_abort) epilogue(p_start, p_L, p_i0, p_h, p_l);
     }
     // every role has stopped issuing and the MMA issuer has drained the tensor pipe
     tc_fence_before();
