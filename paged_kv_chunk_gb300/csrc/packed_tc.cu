@@ -309,15 +309,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             // so it overlaps this stage's softmax, and across items the next tile's first
             // products overlap the current tile's last stage and epilogue.
             long long item = blockIdx.x;
-            int n_st = 0, s = 0, seg = 0;
-            auto item_stages = [&](long long itm) {
+            int n_st = 0, s = 0, seg = 0, n_keys = 0;
+            auto item_stages = [&](long long itm, int& keys) {
                 int start, L, i0, h, kl, kh;
                 decode(itm, seg, start, L, i0, h, kl, kh);
+                keys = kh - kl;
                 return (kh - kl + kBN - 1) / kBN;
             };
             bool ok = item < n_items;
             if (ok) {
-                n_st = item_stages(item);
+                n_st = item_stages(item, n_keys);
                 ok = wait_or_abort(bar_q_ready, 0, s_abort) &&
                      wait_or_abort(bar_full, 0, s_abort);
                 if (ok) {
@@ -330,7 +331,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 const bool last = s + 1 == n_st;
                 const long long next_item = last ? item + gridDim.x : item;
                 if (next_item < n_items) {
-                    const int next_n = last ? item_stages(next_item) : n_st;
+                    int next_keys = 0;
+                    const int next_n = last ? item_stages(next_item, next_keys) : n_st;
                     const int next_s = last ? 0 : s + 1;
                     ok = (!last || wait_or_abort(bar_q_ready, (it + 1) & 1, s_abort)) &&
                          wait_or_abort(bar_full + 8 * ((g + 1) & 1), ((g + 1) >> 1) & 1, s_abort) &&
@@ -344,10 +346,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t vbase = sb + SP::off_slot + (g & 1) * SP::slot + SP::off_v;
+                // only the 16-key steps that hold keys of the segment (a partial last stage
+                // stops early, so V rows past them are never read)
+                const int kst = n_keys - s * kBN;
+                const int ksteps = kst < kBN ? (kst + 15) >> 4 : kBN / 16;
 #pragma unroll
                 for (int k = 0; k < kBN / 16; ++k)
-                    umma_ts(tmem + kColO, tmem + kColP + 8 * k, sdesc(vbase + 2048 * k), id_o,
-                            (s > 0 || k > 0) ? 1 : 0);
+                    if (k < ksteps)
+                        umma_ts(tmem + kColO, tmem + kColP + 8 * k, sdesc(vbase + 2048 * k), id_o,
+                                (s > 0 || k > 0) ? 1 : 0);
                 umma_commit(bar_pv_done);
                 umma_commit(bar_empty + 8 * (g & 1));
                 ++npv;
@@ -358,7 +365,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     item = next_item;
                     ++it;
                     if (item >= n_items) break;
-                    n_st = item_stages(item);
+                    n_st = item_stages(item, n_keys);
                     s = 0;
                 }
             }
@@ -629,12 +636,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     }
                     l_sum += ps.x + ps.y;
                 }
-                // V rows past the segment belong to the next one: zero them so that P = 0
-                // there never meets a non-finite value
+                // V rows past the segment belong to the next one.  P.V stops at the 16-key
+                // step holding the segment's last key; that step's rows past it are zeroed so
+                // that P = 0 there never meets a non-finite value (only the warps whose rows
+                // fall there take part)
                 const int kstage = kh - (kl + s * kBN);   // keys of this stage that exist
-                if (kstage < kBN) {
+                const int k16 = (kstage + 15) & ~15;
+                if (kstage < k16 && 32 * quad < k16 && 32 * quad + 32 > kstage) {
                     if (!warp_wait(bar_full + 8 * (g & 1), (g >> 1) & 1)) { ok = false; break; }
-                    if (r >= kstage) {
+                    if (r >= kstage && r < k16) {
                         uint4* vrow = reinterpret_cast<uint4*>(slot_p + SP::off_v + r * kRowBytes) + 4 * hf;
 #pragma unroll
                         for (int c = 0; c < 4; ++c) vrow[c] = make_uint4(0u, 0u, 0u, 0u);
