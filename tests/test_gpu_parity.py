@@ -279,6 +279,7 @@ def _oracle_packed(x, rows=None):
 @pytest.mark.parametrize("lengths", [
     [1], [64], [65], [7, 0, 130, 1, 64, 200, 3], [300, 299, 1, 0, 0, 150],
     [128], [129], [256, 255, 257, 127],
+    [16, 17, 31, 33, 112, 113, 144, 145],   # the last stage's P.V stops at its 16-key step
 ], ids=str)
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_packed_full(lengths, dtype):
@@ -396,11 +397,14 @@ def _hetero_inputs(Cs, T, H, bs, seed, R):
     return x
 
 
+@pytest.mark.parametrize("Cs", [[0, 17, 64, 130, 255, 3], [0, 300, 527, 130, 511, 45]],
+                         ids=["short", "long"])
 @pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
-def test_heterogeneous_cache_lengths_one_launch(fused):
+def test_heterogeneous_cache_lengths_one_launch(fused, Cs):
     """Streams at different offsets in one launch (Scheduler page, section 4.3): each reads
-    its own cache_seqlens and indexes the shared table at distance C_b + i - j."""
-    Cs, T, H, bs = [0, 17, 64, 130, 255, 3], 16, 4, 16
+    its own cache_seqlens and indexes the shared table at distance C_b + i - j (the long
+    cohort's position tables take two batches of rel loads)."""
+    T, H, bs = 16, 4, 16
     R = max(Cs) + 2 * T - 1 + 4
     x = _hetero_inputs(Cs, T, H, bs, seed=123, R=R)
     cfg = syn.StreamingConfig("het", B=len(Cs), H=H, D=64, T=T, C=max(Cs), block_size=bs,
