@@ -80,7 +80,8 @@ typedef enum { OASR_F32 = 0, OASR_BF16 = 1 } oasr_dtype;
  * A pure copy (bit-exact).  cache_seqlens is read, never advanced: the caller commits
  * the chunk afterwards.  Rows whose position lies past max_blocks_per_seq pages, or whose
  * block id is outside [0, num_blocks), are skipped (status bit OASR_ERR_BOUNDS).
- * D * sizeof(dtype) must be a multiple of 16 bytes.
+ * D * sizeof(dtype) must be a multiple of 16 bytes and 2 * B * T at most 2^26 (else
+ * OASR_ERR_UNSUPPORTED).
  */
 oasr_status oasr_paged_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
                               int num_blocks, int block_size, const int32_t* block_table,
@@ -134,8 +135,9 @@ oasr_status oasr_chunk_step_paged(const void* q, const void* k_new, const void* 
  * Segment s owns rows [cu_seqlens[s], cu_seqlens[s+1]); each of its queries attends to
  * every key of the same segment, with distance i - j (local indices) and rel row
  * z - (i - j), z = (R - 1) / 2.  Requirements: D = 64; 1 <= num_seqs <= 1024;
- * max_seqlen >= every segment length; R >= 2 * max_seqlen - 1.  Rows of a segment that
- * would cross `total` are clamped (status bit OASR_ERR_BOUNDS).
+ * max_seqlen >= every segment length; R >= 2 * max_seqlen - 1; bf16: (total / 128 +
+ * num_seqs) * H < 2^31 (else OASR_ERR_UNSUPPORTED).  Rows of a segment that would cross
+ * `total` are clamped (status bit OASR_ERR_BOUNDS).
  */
 oasr_status oasr_packed_relattn_varlen(const void* q, const void* k, const void* v,
                                        const int32_t* cu_seqlens, int num_seqs, int max_seqlen,
