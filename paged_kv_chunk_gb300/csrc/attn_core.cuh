@@ -361,15 +361,15 @@ __device__ __forceinline__ void warp_slice16(WarpAcc& acc, const uint32_t (&qu)[
 // contracted in a permuted order: lane quad position t4 holds dims [16 t4, 16 t4 + 16) of
 // both operands, so a lane's B fragments for one rel row are two 16-byte loads (rel is read
 // from global memory; the table is the same for every stream and stays in L2).
-// The rel rows of the first kPosBatch tiles are requested by load() as early as the caller
-// can (they need only the cache length), the rest by build() itself.
-constexpr int kPosBatch = 10;   // column tiles of one warp whose rel rows are in flight together
-
+// The rel rows of the first BATCH tiles are requested by load() (once the caller has the
+// cache length), the rest by build() itself.  BATCH: column tiles of one warp whose rel
+// rows are in flight together (10; 5 for the lighter three-CTAs-per-SM kernel).
+template <int BATCH>
 struct PosTable {
     const uint16_t* rel_h;   // rel + h * 64
     long long stride;        // elements between rel rows
     int R, rho0, ncols, warp, nw, lane;
-    uint4 bl[kPosBatch], bh[kPosBatch];
+    uint4 bl[BATCH], bh[BATCH];
 
     __device__ __forceinline__ int ntiles() const { return (ncols + 7) >> 3; }
 
@@ -377,7 +377,7 @@ struct PosTable {
     {
         const int g4 = lane >> 2, t4 = lane & 3;
 #pragma unroll
-        for (int u = 0; u < kPosBatch; ++u) {
+        for (int u = 0; u < BATCH; ++u) {
             const int rho = rho0 + 8 * (nb0 + u * nw) + g4;
             bl[u] = bh[u] = make_uint4(0u, 0u, 0u, 0u);
             if (nb0 + u * nw < ntiles() && rho >= 0 && rho < R) {
@@ -411,11 +411,11 @@ struct PosTable {
         for (int nb0 = warp;;) {
             // the batch's tiles as independent MMA chains (tiles past the table have zero rel
             // rows and store nothing); a short batch runs the half-size version
-            if (nb0 + (kPosBatch / 2) * nw < ntiles())
-                tiles<kPosBatch>(gs, W, qa, nb0);
+            if (nb0 + (BATCH / 2) * nw < ntiles())
+                tiles<BATCH>(gs, W, qa, nb0);
             else
-                tiles<kPosBatch / 2>(gs, W, qa, nb0);
-            nb0 += kPosBatch * nw;
+                tiles<BATCH / 2>(gs, W, qa, nb0);
+            nb0 += BATCH * nw;
             if (nb0 >= ntiles()) break;
             load(nb0);
         }

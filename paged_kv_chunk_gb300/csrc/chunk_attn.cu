@@ -87,8 +87,10 @@ struct ChunkSmem {
     static_assert(comb_l + TL::KG * TL::Tp * 4 <= NS * kSlot, "combine area");
 };
 
+// Two CTAs per SM; the position-table kernel with a two-stage ring (short histories on grids
+// of several waves) is built for three, with lighter batches of rel loads.
 template <int MT, int NS, bool FUSED, bool GT>
-__global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
+__global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 3 : 2) chunk_attn_bf16_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
     const __grid_constant__ CUtensorMap tm_kn, const __grid_constant__ CUtensorMap tm_vn,
@@ -312,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_attn_bf16_kernel(
         mbar_arrive(bar_written);
     };
     if constexpr (GT) {
-        PosTable pt;
+        PosTable<NS == 2 ? 5 : 10> pt;
         pt.rel_h = a.rel + h * kHeadDim;
         pt.stride = static_cast<long long>(a.H) * kHeadDim;
         pt.R = a.R;
@@ -543,8 +545,9 @@ __global__ void __launch_bounds__(128) chunk_attn_f32_kernel(
 
 int g_smem_done[16][64];
 
-// Dynamic shared memory of one CTA that still lets two CTAs share an SM.
+// Dynamic shared memory of one CTA that still lets two (three) CTAs share an SM.
 constexpr int kTwoCtaSmem = 112 * 1024;
+constexpr int kThreeCtaSmem = 74 * 1024;
 
 // Row stride (floats) of the position table for keys up to `cap`: every read and write stays
 // below cap + 32, and a stride of 8 mod 32 keeps the 8-byte reads of a slice conflict-free.
@@ -646,6 +649,15 @@ oasr_status dispatch(const void* q, const void* k_new, const void* v_new, void* 
     // (histories up to 544 keys; a table past 320 columns takes each warp a second batch of
     // rel loads, still faster than the band on 528-key histories), else the per-stage band
     const long long cap = static_cast<long long>(mbps) * block_size;
+    // a grid of several waves at two CTAs per SM with a short history: the same kernel with a
+    // two-stage ring, three CTAs per SM (more CTAs resident beats stages in flight there;
+    // measured 18 % faster on the T = 4 sweep, slower on one-wave cohorts)
+    const int sms = sm_count();
+    if (T <= 16 && cap <= 4096 && sms > 0 && static_cast<long long>(B) * H > 2LL * sms &&
+        ChunkSmem<1, 2, true>::bytes + 64 * pos_table_stride(static_cast<int>(cap)) <= kThreeCtaSmem)
+        return launch_bf16<1, 2, FUSED, true>(q, k_new, v_new, k_pool, v_pool, num_blocks,
+                                              block_size, bt, mbps, cs, u, vb, rel, R, out, B, T,
+                                              H, scale, stream, f + 4);
     if (T <= 16 && cap <= 4096 &&
         ChunkSmem<1, 4, true>::bytes + 64 * pos_table_stride(static_cast<int>(cap)) <= kTwoCtaSmem)
         return launch_bf16<1, 4, FUSED, true>(q, k_new, v_new, k_pool, v_pool, num_blocks,
