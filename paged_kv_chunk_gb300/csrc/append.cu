@@ -31,6 +31,14 @@ __global__ void __launch_bounds__(256) paged_append_kernel(
         const bool is_v = w >= rows;
         const int r = is_v ? w - rows : w;   // b * T + t
         const int b = r / T, t = r - (r / T) * T;
+        const long long src = static_cast<long long>(r) * row_vecs;
+        const uint4* in = is_v ? v_new : k_new;
+        // the frame's first 4 * 32 vectors are requested before the cache length and the
+        // table entry (they do not depend on them), so the three loads overlap
+        uint4 pre[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (lane + 32 * u < row_vecs) pre[u] = __ldg(in + src + lane + 32 * u);
         const long long p = static_cast<long long>(__ldg(cache_seqlens + b)) + t;
         const long long lb = p / block_size;
         int blk = -1;
@@ -42,10 +50,11 @@ __global__ void __launch_bounds__(256) paged_append_kernel(
         }
         if (!err) {
             const long long dst = (static_cast<long long>(blk) * block_size + (p - lb * block_size)) * row_vecs;
-            const long long src = static_cast<long long>(r) * row_vecs;
-            const uint4* in = is_v ? v_new : k_new;
             uint4* out = is_v ? v_pool : k_pool;
-            for (int c = lane; c < row_vecs; c += 32) out[dst + c] = __ldg(in + src + c);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (lane + 32 * u < row_vecs) out[dst + lane + 32 * u] = pre[u];
+            for (int c = lane + 128; c < row_vecs; c += 32) out[dst + c] = __ldg(in + src + c);
         }
     }
     // this thread's copies are issued: the next grid may schedule (it waits for this one)
