@@ -154,9 +154,9 @@ EDGE = [
     (2, 2, 32, 96, 16, 0, "bf16"),     # two m-tiles, full
     (2, 2, 33, 20, 16, 0, "bf16"),     # four m-tiles, ragged
     (2, 2, 64, 130, 16, 0, "bf16"),    # four m-tiles, full
-    (3, 1, 16, 100, 16, 0, "bf16"),    # one head per CTA
-    (2, 6, 9, 70, 32, 0, "bf16"),      # two heads per CTA
-    (2, 4, 16, 530, 32, 0, "bf16"),    # key range split in two, ragged
+    (3, 1, 16, 100, 16, 0, "bf16"),    # a single head
+    (2, 6, 9, 70, 32, 0, "bf16"),      # six heads, T not a power of two
+    (2, 4, 16, 530, 32, 0, "bf16"),    # past the largest position table, 32-row pages
     (2, 2, 16, 288, 8, 0, "bf16"),     # a whole-CTA position table from one batch of rel loads
     (2, 2, 16, 290, 8, 0, "bf16"),     # one page more: a second batch
     (2, 2, 16, 528, 8, 0, "bf16"),     # the largest table that fits (544 keys)
