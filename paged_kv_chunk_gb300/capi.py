@@ -96,6 +96,10 @@ def _dtype_code(t: torch.Tensor) -> int:
 def _dev(t: torch.Tensor, name: str, dtype=None, ndim=None) -> int:
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        # the kernels run on the current device: another device's pointer would be a fault
+        raise ValueError(f"{name} is on {t.device}, the current device is "
+                         f"cuda:{torch.cuda.current_device()}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -129,10 +133,13 @@ def oasr_paged_append(k_new, v_new, k_pool, v_pool, block_table, cache_seqlens, 
         _dev(cache_seqlens, "cache_seqlens", torch.int32, 1), B, T, H, D, dt, _stream(stream)))
 
 
-def _chunk_common(q, k_pool, block_table, cache_seqlens, pos_bias_u, pos_bias_v, rel, out):
+def _chunk_common(q, k_pool, v_pool, block_table, cache_seqlens, pos_bias_u, pos_bias_v, rel,
+                  out):
     B, T, H, D = q.shape
     if k_pool.dim() != 4 or tuple(k_pool.shape[2:]) != (H, D):
         raise ValueError("k_pool must be [num_blocks, block_size, H, D]")
+    if v_pool.shape != k_pool.shape:
+        raise ValueError("v_pool must have k_pool's shape")
     if tuple(pos_bias_u.shape) != (H, D) or tuple(pos_bias_v.shape) != (H, D):
         raise ValueError("pos biases must be [H, D]")
     if rel.dim() != 3 or tuple(rel.shape[1:]) != (H, D):
@@ -151,8 +158,8 @@ def oasr_chunk_relattn_paged(q, k_pool, v_pool, block_table, cache_seqlens, pos_
     dt = _dtype_code(q)
     if out is None:
         out = torch.empty_like(q)
-    B, T, H, D = _chunk_common(q, k_pool, block_table, cache_seqlens, pos_bias_u, pos_bias_v,
-                               rel, out)
+    B, T, H, D = _chunk_common(q, k_pool, v_pool, block_table, cache_seqlens, pos_bias_u,
+                               pos_bias_v, rel, out)
     scale = D ** -0.5 if scale is None else float(scale)
     _check("oasr_chunk_relattn_paged", L.oasr_chunk_relattn_paged(
         _dev(q, "q", q.dtype), _dev(k_pool, "k_pool", q.dtype), _dev(v_pool, "v_pool", q.dtype),
@@ -171,8 +178,8 @@ def oasr_chunk_step_paged(q, k_new, v_new, k_pool, v_pool, block_table, cache_se
     dt = _dtype_code(q)
     if out is None:
         out = torch.empty_like(q)
-    B, T, H, D = _chunk_common(q, k_pool, block_table, cache_seqlens, pos_bias_u, pos_bias_v,
-                               rel, out)
+    B, T, H, D = _chunk_common(q, k_pool, v_pool, block_table, cache_seqlens, pos_bias_u,
+                               pos_bias_v, rel, out)
     if tuple(k_new.shape) != (B, T, H, D) or tuple(v_new.shape) != (B, T, H, D):
         raise ValueError("k_new, v_new must be [B, T, H, D]")
     scale = D ** -0.5 if scale is None else float(scale)
@@ -262,6 +269,8 @@ def oasr_project_qkv_pos(x, w_qkv, b_qkv, pos_emb, w_pos, H, q=None, k=None, v=N
     k = torch.empty((M, H, D), dtype=x.dtype, device=x.device) if k is None else k
     v = torch.empty((M, H, D), dtype=x.dtype, device=x.device) if v is None else v
     rel = torch.empty((R, H, D), dtype=x.dtype, device=x.device) if rel is None else rel
+    if any(tuple(t.shape) != (M, H, D) for t in (q, k, v)) or tuple(rel.shape) != (R, H, D):
+        raise ValueError("q, k, v must be [M, H, d/H] and rel [R, H, d/H]")
     _check("oasr_project_qkv_pos", L.oasr_project_qkv_pos(
         _dev(x, "x", x.dtype, 2), _dev(w_qkv, "w_qkv", x.dtype, 2), _dev(b_qkv, "b_qkv", x.dtype, 1),
         _dev(pos_emb, "pos_emb", x.dtype, 2), _dev(w_pos, "w_pos", x.dtype, 2),

@@ -167,6 +167,27 @@ def test_binding_raises_on_cpu_tensors():
                                torch.zeros(2, dtype=torch.int32))
 
 
+def test_binding_checks_shapes_before_any_pointer():
+    """Sizes the kernels derive from one tensor must hold for the others: a V pool or an
+    output smaller than its partner is refused before anything reaches the library."""
+    import torch
+    bf = torch.bfloat16
+    q = torch.zeros(2, 16, 4, 64, dtype=bf)
+    kp, vp_small = torch.zeros(16, 16, 4, 64, dtype=bf), torch.zeros(8, 16, 4, 64, dtype=bf)
+    bt, cs = torch.zeros(2, 8, dtype=torch.int32), torch.zeros(2, dtype=torch.int32)
+    uv, rel = torch.zeros(4, 64, dtype=bf), torch.zeros(47, 4, 64, dtype=bf)
+    for call in (lambda: capi.oasr_chunk_relattn_paged(q, kp, vp_small, bt, cs, uv, uv, rel),
+                 lambda: capi.oasr_chunk_step_paged(q, q, q, kp, vp_small, bt, cs, uv, uv, rel)):
+        with pytest.raises(ValueError, match="v_pool"):
+            call()
+    x, w, bqkv = torch.zeros(32, 256, dtype=bf), torch.zeros(768, 256, dtype=bf), torch.zeros(768, dtype=bf)
+    pe, wp = torch.zeros(47, 256, dtype=bf), torch.zeros(256, 256, dtype=bf)
+    with pytest.raises(ValueError, match="q, k, v must be"):
+        capi.oasr_project_qkv_pos(x, w, bqkv, pe, wp, 4, q=torch.zeros(16, 4, 64, dtype=bf))
+    with pytest.raises(ValueError, match="q, k, v must be"):
+        capi.oasr_project_qkv_pos(x, w, bqkv, pe, wp, 4, rel=torch.zeros(46, 4, 64, dtype=bf))
+
+
 @pytest.mark.parametrize("limit_us", [0, 2000001])
 def test_selftest_wait_rejects_bad_limits(lib, limit_us):
     assert lib.oasr_selftest_wait(limit_us, None) == capi.OASR_ERR_INVALID_ARG
