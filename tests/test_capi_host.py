@@ -56,6 +56,7 @@ def _chunk(lib, **kw):
     (dict(bs=24), capi.OASR_ERR_UNSUPPORTED),
     (dict(bs=4), capi.OASR_ERR_UNSUPPORTED),
     (dict(bs=512), capi.OASR_ERR_UNSUPPORTED),
+    (dict(mbps=513), capi.OASR_ERR_UNSUPPORTED),   # one page past the widest table
     (dict(dt=7), capi.OASR_ERR_UNSUPPORTED),
     (dict(q=FAKE + 2), capi.OASR_ERR_INVALID_ARG),
     (dict(rel=FAKE + 8), capi.OASR_ERR_INVALID_ARG),

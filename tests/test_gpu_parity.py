@@ -626,3 +626,42 @@ def test_projection_feeds_the_step():
     ref = oracle.chunk_relattn(to_np(q).reshape(shp), x["cache_k"], x["cache_v"], to_np(kn).reshape(shp),
                                to_np(vn).reshape(shp), x["pos_bias_u"], x["pos_bias_v"], to_np(rel))
     check_close(to_np(out), ref, "bf16", "projection -> step")
+
+
+# ------------------------------------------------------------------------- maximum sizes
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
+def test_widest_block_table(fused):
+    """The widest block table the bf16 path takes (512 pages), filled to its last key: the
+    chunk's last row lands in the table's last slot."""
+    bs, mbps, T = 8, 512, 16
+    cfg = syn.StreamingConfig("widest", B=2, H=2, D=64, T=T, C=mbps * bs - T, block_size=bs,
+                              dtype="bf16", seed=71, max_blocks_per_seq=mbps)
+    assert cfg.mbps == mbps
+    x = stream_case(cfg)
+    out, d = _run_step(cfg, x, fused)
+    check_close(to_np(out), oracle_chunk(x), "bf16", f"widest table, fused={fused}")
+    kp = x["k_pool"].copy()
+    vp = x["v_pool"].copy()
+    oracle.paged_append(syn.to_bits(x["k_new"], "bf16"), syn.to_bits(x["v_new"], "bf16"), kp, vp,
+                        x["block_table"], x["cache_seqlens"])
+    assert np.array_equal(host_pool(d["k_pool"], "bf16"), kp)
+    assert np.array_equal(host_pool(d["v_pool"], "bf16"), vp)
+    assert capi.oasr_device_status() == 0
+
+
+@pytest.mark.parametrize("window", [None, (8, 7)], ids=["bidirectional", "chunked"])
+def test_packed_most_segments(window):
+    """The largest segment count the packed calls take (1024), lengths 0..40."""
+    rng = np.random.default_rng(91)
+    lengths = [int(v) for v in rng.integers(0, 41, size=1024)]
+    _, x = _packed_case(lengths, seed=92)
+    if window is None:
+        out = _run_packed(x, "bf16")
+        ref = _oracle_packed(x)
+    else:
+        out = _run_chunked(x, "bf16", *window)
+        ref = _oracle_chunked(x, *window)
+    check_close(to_np(out), ref, "bf16", f"1024 segments, window {window}")
+    assert capi.oasr_device_status() == 0
