@@ -88,9 +88,10 @@ struct ChunkSmem {
 };
 
 // Two CTAs per SM; the position-table kernel with a two-stage ring (short histories on grids
-// of several waves) is built for three, with lighter batches of rel loads.
+// of several waves) is built for four (96 registers, no spills), with lighter batches of rel
+// loads, so that its shared memory alone sets how many share an SM: four up to 56 KB, else three.
 template <int MT, int NS, bool FUSED, bool GT>
-__global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 3 : 2) chunk_attn_bf16_kernel(
+__global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_bf16_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
     const __grid_constant__ CUtensorMap tm_kn, const __grid_constant__ CUtensorMap tm_vn,
@@ -545,7 +546,8 @@ __global__ void __launch_bounds__(128) chunk_attn_f32_kernel(
 
 int g_smem_done[16][64];
 
-// Dynamic shared memory of one CTA that still lets two (three) CTAs share an SM.
+// Dynamic shared memory of one CTA that still lets two (three) CTAs share an SM (four share
+// one up to 56 KB).
 constexpr int kTwoCtaSmem = 112 * 1024;
 constexpr int kThreeCtaSmem = 74 * 1024;
 
@@ -650,8 +652,9 @@ oasr_status dispatch(const void* q, const void* k_new, const void* v_new, void* 
     // rel loads, still faster than the band on 528-key histories), else the per-stage band
     const long long cap = static_cast<long long>(mbps) * block_size;
     // a grid of several waves at two CTAs per SM with a short history: the same kernel with a
-    // two-stage ring, three CTAs per SM (more CTAs resident beats stages in flight there;
-    // measured 18 % faster on the T = 4 sweep, slower on one-wave cohorts)
+    // two-stage ring, three or four CTAs per SM (more CTAs resident beats stages in flight
+    // there: three measured 18 % faster on the T = 4 sweep, four another 16 % on T = 4 and 15 %
+    // on T = 8; slower on one-wave cohorts)
     const int sms = sm_count();
     if (T <= 16 && cap <= 4096 && sms > 0 && static_cast<long long>(B) * H > 2LL * sms &&
         ChunkSmem<1, 2, true>::bytes + 64 * pos_table_stride(static_cast<int>(cap)) <= kThreeCtaSmem)

@@ -162,7 +162,7 @@ EDGE = [
     (2, 2, 16, 528, 8, 0, "bf16"),     # the largest table that fits (544 keys)
     (2, 2, 16, 530, 8, 0, "bf16"),     # one page past it: the per-stage band
     (2, 2, 11, 61, 16, 4, "bf16"),     # odd chunk start: unaligned table reads; longer table
-    (80, 4, 5, 37, 8, 0, "bf16"),      # more than one wave of CTAs: the three-per-SM kernel
+    (80, 4, 5, 37, 8, 0, "bf16"),      # more than one wave of CTAs: the four-per-SM kernel
     (2, 2, 5, 77, 8, 2, "f32"),
     (2, 3, 40, 33, 16, 0, "f32"),
     (1, 1, 1, 0, 8, 0, "f32"),
