@@ -6,8 +6,8 @@
 // a bias and linear_pos does not.
 //
 // A grouped bf16 GEMM on the 5th-generation tensor cores.  Persistent CTAs (one per SM) walk
-// one list of 128 x 128 output tiles: those of the q/k/v problem, then those of the
-// positional one.  Warp 5 feeds a ring of {A tile, W tile} stages (64-wide K steps, TMA,
+// one list of 128 x 128 output tiles (128 x 64 when the wide ones would occupy at most half
+// the SMs): those of the q/k/v problem, then those of the positional one.  Warp 5 feeds a ring of {A tile, W tile} stages (64-wide K steps, TMA,
 // 128-byte swizzle; the row-major inputs are viewed as [rows, K/64, 64]); one thread of warp 4
 // issues tcgen05.mma M128 N128 K16 into one of two TMEM accumulators, so the epilogue of a
 // tile overlaps the products of the next; warps 0-3 (one TMEM lane quadrant each, thread =
