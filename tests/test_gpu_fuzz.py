@@ -158,3 +158,35 @@ def test_random_packed_row(seed):
     torch.cuda.synchronize()
     check_close(to_np(out), ref, dtype, f"seed {seed} {p}")
     assert capi.oasr_device_status() == 0
+
+
+@pytest.mark.parametrize("B,H,T,bs,cmax,seed", [
+    (80, 4, 1, 8, 40, 1),       # 320 CTAs, single-frame chunks
+    (96, 4, 8, 8, 120, 2),      # 384 CTAs, 8-row pages
+    (64, 8, 16, 32, 250, 3),    # 512 CTAs, 32-row pages
+])
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
+def test_multiwave_short_histories(B, H, T, bs, cmax, seed, fused):
+    """Grids of more than two CTAs per SM with short, unequal histories: the two-stage
+    position-table form that three or four CTAs share an SM with."""
+    rng = np.random.default_rng(50_000 + seed)
+    Cs = [int(c) for c in rng.integers(0, cmax + 1, size=B)]
+    x = _stream_inputs(rng, T, bs, H, B, Cs, "bf16", 1, 2)
+    d = {k: dev(x[k], "bf16") for k in ("q", "k_new", "v_new", "pos_bias_u", "pos_bias_v", "rel")}
+    kp, vp = dev_pool(x["k_pool"], "bf16"), dev_pool(x["v_pool"], "bf16")
+    bt = torch.from_numpy(x["block_table"]).cuda()
+    cs = torch.from_numpy(x["cache_seqlens"]).cuda()
+    if fused:
+        out = capi.oasr_chunk_step_paged(d["q"], d["k_new"], d["v_new"], kp, vp, bt, cs,
+                                         d["pos_bias_u"], d["pos_bias_v"], d["rel"])
+    else:
+        capi.oasr_paged_append(d["k_new"], d["v_new"], kp, vp, bt, cs)
+        out = capi.oasr_chunk_relattn_paged(d["q"], kp, vp, bt, cs, d["pos_bias_u"],
+                                            d["pos_bias_v"], d["rel"])
+    torch.cuda.synchronize()
+    got = to_np(out)
+    for b, (ck, cv) in enumerate(x["caches"]):
+        ref = oracle.chunk_relattn(x["q"][b:b + 1], ck, cv, x["k_new"][b:b + 1],
+                                   x["v_new"][b:b + 1], x["pos_bias_u"], x["pos_bias_v"], x["rel"])
+        check_close(got[b:b + 1], ref, "bf16", f"B{B} H{H} T{T} stream {b} (C={Cs[b]})")
+    assert capi.oasr_device_status() == 0
