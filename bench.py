@@ -322,6 +322,65 @@ def run_reference(args, cfg, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_offline(args, name, rank):
+    """Reference arm of the packed row, the Nemotron window and the projections: the oracle
+    on the host cores, each step a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    if name in PROJECTIONS:
+        p = PROJECTIONS[name]
+        H, R = p["H"], p["R"]
+        M, d = p["B"] * p["T"], 64 * H
+        rng = np.random.default_rng(p["seed"])
+        x, pe = rng.standard_normal((M, d)) * syn.SIGMA, rng.standard_normal((R, d)) * syn.SIGMA
+        wq, wp = rng.standard_normal((3 * d, d)) * d ** -0.5, rng.standard_normal((d, d)) * d ** -0.5
+        bq = rng.standard_normal(3 * d) * syn.SIGMA
+
+        def step():
+            oracle.project_qkv_pos(x, wq, bq, pe, wp, H)
+        frames, workload = M, f"{name}_qkv_pos"
+        sample = f"each step: one layer's projections ({M} frames, d {d}, {R} rel rows), float64"
+    else:
+        window = (NEMOTRON_CHUNK, NEMOTRON_LEFT) if name == NEMOTRON else None
+        cfg = syn.PACKED
+        x = syn.packed_inputs(cfg, cfg.seed)
+        cu = x["cu_seqlens"]
+        sq = np.cumsum(np.asarray(x["lengths"], np.float64) ** 2)
+        n = int(min(len(sq), np.searchsorted(sq, 1.5e6) + 1))   # first segments, ~1.5e6 pairs
+        e = int(cu[n])
+        sub = {k: x[k][:e] for k in ("q", "k", "v")}
+
+        def step():
+            if window:
+                oracle.packed_relattn_chunked(sub["q"], sub["k"], sub["v"], cu[:n + 1],
+                                              x["pos_bias_u"], x["pos_bias_v"], x["rel"], *window)
+            else:
+                oracle.packed_relattn(sub["q"], sub["k"], sub["v"], cu[:n + 1], x["pos_bias_u"],
+                                      x["pos_bias_v"], x["rel"])
+        frames = e
+        workload = "nemotron_chunked_offline" if window else "packed_varlen_offline"
+        sample = f"each step: the first {n} of the {cfg.num_seqs} utterances ({e} frames) on the fp64 C oracle"
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = frames * args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": workload},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 # --------------------------------------------------------------------------- GPU arm
 
 
@@ -736,6 +795,10 @@ def run_packed(args, rank, world, local, window=None):
 
 def main():
     args = parse_args()
+    if args.impl == "reference" and (args.config in PROJECTIONS
+                                     or args.config in (syn.PACKED.name, NEMOTRON)):
+        run_reference_offline(args, args.config, int(os.environ.get("RANK", "0")))
+        return
     if args.config in PROJECTIONS:
         rank, world, local = dist_setup()
         run_projection(args, rank, world, local, args.config)

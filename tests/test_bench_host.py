@@ -94,3 +94,24 @@ def test_committed_profiles_name_their_source_and_traffic():
         assert "kernel_source_sha:" in text and "dram_bytes_per_launch:" in text, name
         traffic = float(text.split("dram_bytes_per_launch:")[1].split()[0])
         assert np.isfinite(traffic) and traffic > 0, name
+
+
+@pytest.mark.parametrize("config", ["tiny", "projection_small", "packed_varlen"])
+def test_reference_arm_prints_one_contract_line(config):
+    """`bench.py --impl reference` times the oracle and prints one JSON line with the
+    contract's keys, for a streaming, a projection and a packed workload."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--config", config,
+                          "--steps", "1", "--warmup", "0"], cwd=root, check=True,
+                         capture_output=True, text=True, timeout=600).stdout
+    lines = [l for l in out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in j, key
+    assert j["impl"] == "reference" and j["value"] > 0 and j["cpu_baseline"]["kind"] == "oracle"
