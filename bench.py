@@ -322,11 +322,41 @@ def run_reference(args, cfg, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_reference_offline(args, name, rank):
-    """Reference arm of the packed row, the Nemotron window and the projections: the oracle
-    on the host cores, each step a bounded sample of the same workload."""
-    if rank != 0:
-        return
+def sequential_e2e(stream, h2d_pairs, run, d2h_pairs, steps, warmup, world):
+    """End to end through the public API: every step copies its inputs from pinned host memory
+    (h2d_pairs: (device tensor, pinned host tensor)), runs, and copies its outputs back
+    (d2h_pairs: (pinned host tensor, device tensor)), all on `stream`, inside the timed
+    region.  Returns (ms for all steps, max over ranks; H2D bytes per step; D2H bytes)."""
+    def one():
+        for dst, src in h2d_pairs:
+            dst.copy_(src, non_blocking=True)
+        run()
+        for dst, src in d2h_pairs:
+            dst.copy_(src, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - w0
+    barrier(world)
+    ms = max_over_ranks(max(e0.elapsed_time(e1), 1e3 * wall), world)
+    h2d = sum(t.numel() * t.element_size() for _, t in h2d_pairs)
+    d2h = sum(t.numel() * t.element_size() for t, _ in d2h_pairs)
+    return ms, int(h2d), int(d2h)
+
+
+def offline_oracle_sample(name):
+    """(step, frames, workload, sample): one call of the oracle on a bounded sample of the
+    packed row, the Nemotron window or a projection workload, and what it covers."""
     import oracle
     oracle.build()
     if name in PROJECTIONS:
@@ -362,6 +392,32 @@ def run_reference_offline(args, name, rank):
         frames = e
         workload = "nemotron_chunked_offline" if window else "packed_varlen_offline"
         sample = f"each step: the first {n} of the {cfg.num_seqs} utterances ({e} frames) on the fp64 C oracle"
+    return step, frames, workload, sample
+
+
+def offline_cpu_baseline(name, seconds):
+    """cpu_baseline of an offline workload: the oracle on its bounded sample for ~seconds."""
+    import oracle
+    step, frames, _, sample = offline_oracle_sample(name)
+    step()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        step()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": frames * n / el, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{sample}; {n} steps in {el:.1f} s"}
+
+
+def run_reference_offline(args, name, rank):
+    """Reference arm of the packed row, the Nemotron window and the projections: the oracle
+    on the host cores, each step a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    import oracle
+    step, frames, workload, sample = offline_oracle_sample(name)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -691,6 +747,19 @@ def run_projection(args, rank, world, local, name):
         barrier(world)
     clocks = sampler.stop() if sampler else None
     ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    e2e = None
+    if not args.no_e2e:
+        x_pin = [ins[l][0].cpu().pin_memory() for l in range(layers)]
+        o_pin = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[l]]
+                 for l in range(layers)]
+        e_ms, hb, db = sequential_e2e(
+            stream, [(ins[l][0], x_pin[l]) for l in range(layers)], graph.replay,
+            [(o_pin[l][i], outs[l][i]) for l in range(layers) for i in range(4)],
+            args.steps, max(3, args.warmup), world)
+        e2e = {"value": M * layers * args.steps * world / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": hb, "d2h_bytes_per_step": db,
+               "path": "per step: pinned host x of every layer -> H2D -> graph replay of the "
+                       "oasr_project_qkv_pos calls -> D2H of q, k, v and rel (weights resident)"}
     if rank != 0:
         return
     per_launch_s = ms / 1e3 / (args.steps * layers)
@@ -713,6 +782,10 @@ def run_projection(args, rank, world, local, name):
                      "avg_launch_us": per_launch_s * 1e6, "peak_kind": kind},
         "gpu_launches": args.steps * layers, "clocks": clocks,
     }
+    if e2e:
+        line["e2e"] = e2e
+    if world == 1 and args.cpu_seconds > 0:
+        line["cpu_baseline"] = offline_cpu_baseline(name, args.cpu_seconds)
     print(json.dumps(line), flush=True)
 
 
@@ -763,6 +836,18 @@ def run_packed(args, rank, world, local, window=None):
         barrier(world)
     clocks = sampler.stop() if sampler else None
     ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    e2e = None
+    if not args.no_e2e:
+        pins = {k: d[k].cpu().pin_memory() for k in ("q", "k", "v")}
+        cu_pin = cu.cpu().pin_memory()
+        out_pin = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        e_ms, hb, db = sequential_e2e(
+            stream, [(d[k], pins[k]) for k in ("q", "k", "v")] + [(cu, cu_pin)], call,
+            [(out_pin, out)], args.steps, max(3, args.warmup), world)
+        e2e = {"value": total * args.steps * world / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": hb, "d2h_bytes_per_step": db,
+               "path": "per call: pinned host q, k, v and cu_seqlens -> H2D -> the packed call -> "
+                       "D2H of out (u, v and rel resident)"}
     if rank != 0:
         return
     per_call_s = ms / 1e3 / args.steps
@@ -790,6 +875,11 @@ def run_packed(args, rank, world, local, window=None):
                      "avg_launch_us": per_call_s * 1e6, "peak_kind": kind},
         "gpu_launches": args.steps, "clocks": clocks,
     }
+    if e2e:
+        line["e2e"] = e2e
+    if world == 1 and args.cpu_seconds > 0:
+        line["cpu_baseline"] = offline_cpu_baseline(NEMOTRON if window else syn.PACKED.name,
+                                                    args.cpu_seconds)
     print(json.dumps(line), flush=True)
 
 
