@@ -275,7 +275,10 @@ def window_commit(block_table, cache_seqlens, T: int, block_size: int, window_fr
 
     After the chunk the stream holds n = cache_seqlens[b] + T frames in its first
     P = ceil(n / block_size) pages.  If n exceeds window_frames, the oldest
-    d = ceil((n - window_frames) / block_size) pages are dropped: the first P entries of the
+    d = ceil((n - window_frames) / block_size) pages are dropped, but never more than the
+    floor(n / block_size) full ones: eviction moves whole pages, so a partly written newest
+    page stays even when the window is shorter than a page (the cached length then exceeds
+    the window by less than a page, and never goes negative).  The first P entries of the
     row are rotated left by d, so the dropped blocks become the next pages to be written, and
     the cached length becomes n - d * block_size.  Otherwise the cached length becomes n.
     Entries past the first P are left alone.  Returns new (block_table, cache_seqlens).
@@ -287,7 +290,7 @@ def window_commit(block_table, cache_seqlens, T: int, block_size: int, window_fr
         P = -(-n // block_size)
         d = 0
         if n > window_frames:
-            d = -(-(n - window_frames) // block_size)
+            d = min(-(-(n - window_frames) // block_size), n // block_size)
         row = list(bt[b, :P])
         bt[b, :P] = row[d:] + row[:d]
         cs[b] = n - d * block_size

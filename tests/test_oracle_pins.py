@@ -519,17 +519,42 @@ def test_window_commit_hand_worked():
                                         [41, 42, 40, 43]])
 
 
-@pytest.mark.parametrize("bs,T,window", [(16, 16, 64), (8, 16, 40), (16, 8, 48), (4, 12, 20)])
+def test_window_commit_window_shorter_than_a_page():
+    """Eviction moves whole pages: with a window shorter than a page the partly written
+    newest page stays, so the cached length never goes negative (worked by hand)."""
+    # n = 6 + 4 = 10 frames in pages [0, 1, 2] (page 2 holds frames 8, 9); window 1 would ask
+    # for ceil(9 / 4) = 3 pages, but only the 2 full ones go: row [2, 0, 1, 3], C = 2
+    bt2, cs2 = oracle.window_commit(np.array([[0, 1, 2, 3]], np.int32), np.array([6], np.int32),
+                                    T=4, block_size=4, window_frames=1)
+    np.testing.assert_array_equal(cs2, [2])
+    np.testing.assert_array_equal(bt2, [[2, 0, 1, 3]])
+    # a first chunk of 12 frames on 16-frame pages, window 3: no page is full, nothing moves
+    bt2, cs2 = oracle.window_commit(np.array([[7, 8]], np.int32), np.array([0], np.int32),
+                                    T=12, block_size=16, window_frames=3)
+    np.testing.assert_array_equal(cs2, [12])
+    np.testing.assert_array_equal(bt2, [[7, 8]])
+    # n = 8 on 4-frame pages with window 0: both pages are full and both go
+    bt2, cs2 = oracle.window_commit(np.array([[5, 6, 9]], np.int32), np.array([4], np.int32),
+                                    T=4, block_size=4, window_frames=0)
+    np.testing.assert_array_equal(cs2, [0])
+    np.testing.assert_array_equal(bt2, [[5, 6, 9]])
+
+
+@pytest.mark.parametrize("bs,T,window", [(16, 16, 64), (8, 16, 40), (16, 8, 48), (4, 12, 20),
+                                         (4, 6, 1), (16, 12, 3), (8, 5, 0), (8, 3, 7)])
 def test_window_commit_keeps_the_latest_frames_in_order(bs, T, window):
     """Track frame numbers through the paging for many steps: after every commit the cached
-    frames are exactly the most recent ones, oldest first, and no block is lost."""
+    frames are exactly the most recent ones, oldest first, and no block is lost.  The cached
+    length is at most the window, or the frames of a partly written newest page when the
+    window is shorter than a page, and never negative."""
     B, steps = 3, 12
-    pages = -(-(window + T) // bs) + 1
+    pages = -(-(max(window, bs) + T) // bs) + 1
     bt = np.arange(B * pages, dtype=np.int32).reshape(B, pages)
     cs = np.zeros(B, np.int32)
     slots = {}           # (block, slot) -> frame number
     frame = np.zeros(B, np.int64)
     for _ in range(steps):
+        n = cs + T
         for b in range(B):
             for t in range(T):
                 p = cs[b] + t
@@ -538,7 +563,8 @@ def test_window_commit_keeps_the_latest_frames_in_order(bs, T, window):
         bt2, cs2 = oracle.window_commit(bt, cs, T, bs, window)
         for b in range(B):
             assert sorted(bt2[b]) == sorted(bt[b])
-            assert cs2[b] <= window and cs2[b] >= min(frame[b], window) - bs + 1
+            assert 0 <= cs2[b] <= max(window, n[b] % bs)
+            assert cs2[b] >= min(frame[b], window) - bs + 1
             seen = [slots[(int(bt2[b, p // bs]), p % bs)] for p in range(cs2[b])]
             assert seen == list(range(frame[b] - cs2[b], frame[b]))
         bt, cs = bt2, cs2
