@@ -175,10 +175,13 @@ oasr_status oasr_packed_relattn_chunked(const void* q, const void* k, const void
  *
  * For every stream b, after a chunk of T frames was appended at cache_seqlens[b], the stream
  * holds n = cache_seqlens[b] + T frames in its first P = ceil(n / block_size) pages.  If
- * n > window_frames, the oldest d = ceil((n - window_frames) / block_size) pages are dropped:
- * block_table[b][0 .. P) is rotated left by d, so the dropped blocks become the next pages to
- * be written, and cache_seqlens[b] becomes n - d * block_size; otherwise cache_seqlens[b]
- * becomes n.  Entries past the first P are untouched.  Both arrays are device memory and are
+ * n > window_frames, the oldest d = min(ceil((n - window_frames) / block_size),
+ * floor(n / block_size)) pages are dropped (whole pages only: a partly written newest page
+ * stays, so with a window shorter than a page the cached length may exceed the window by
+ * less than a page and is never negative): block_table[b][0 .. P) is rotated left by d, so
+ * the dropped blocks become the next pages to be written, and cache_seqlens[b] becomes
+ * n - d * block_size; otherwise cache_seqlens[b] becomes n.  Entries past the first P are
+ * untouched.  Both arrays are device memory and are
  * updated in place on `stream`, so a captured step stays replayable.
  *
  * Requirements: B >= 1; 1 <= max_blocks_per_seq <= 512 (else OASR_ERR_UNSUPPORTED);

@@ -8,7 +8,9 @@
 // stream holds n = C + T frames in its first P = ceil(n / block_size) pages; beyond the
 // window the oldest d = ceil((n - window) / block_size) pages are dropped by rotating those
 // P entries left by d (the dropped blocks become the next pages to be written) and the
-// cached length becomes n - d * block_size, else n.  Relative positions make the shift of
+// cached length becomes n - d * block_size, else n.  Eviction moves whole pages, so d never
+// exceeds the floor(n / block_size) full ones: a window shorter than a page keeps the partly
+// written newest page rather than a negative length.  Relative positions make the shift of
 // every remaining frame's page index invisible to the attention.
 //
 // One warp per stream: the lanes gather the row's first P entries into registers, then
@@ -44,7 +46,10 @@ __global__ void __launch_bounds__(128) window_commit_kernel(int32_t* __restrict_
         n = static_cast<long long>(mbps) * bs;
     }
     int d = 0;
-    if (n > window) d = static_cast<int>((n - window + bs - 1) / bs);
+    if (n > window) {
+        const long long want = (n - window + bs - 1) / bs, full = n / bs;
+        d = static_cast<int>(want < full ? want : full);
+    }
     int32_t* row = bt + static_cast<long long>(b) * mbps;
     int32_t vals[kWinMaxPages / 32];
 #pragma unroll

@@ -523,14 +523,17 @@ def test_chunked_full_size_sampled():
 # --------------------------------------------------------- fixed-window ring (eviction)
 
 
-@pytest.mark.parametrize("bs,T,window,mbps", [(16, 16, 64, 12), (8, 16, 40, 20), (4, 12, 20, 40)],
+@pytest.mark.parametrize("bs,T,window,mbps", [(16, 16, 64, 12), (8, 16, 40, 20), (4, 12, 20, 40),
+                                              (4, 6, 1, 40), (16, 12, 3, 12), (8, 5, 0, 20)],
                          ids=str)
 def test_window_commit_matches_oracle(bs, T, window, mbps):
-    rng = np.random.default_rng(bs * 100 + T)
+    """Bit-exact against the oracle's bookkeeping on random states, including windows shorter
+    than a page (where only full pages may go and no cached length is negative)."""
+    rng = np.random.default_rng(bs * 100 + T + 7 * window)
     B = 37
     bt = np.stack([rng.permutation(1000)[:mbps] for _ in range(B)]).astype(np.int32)
     cs = rng.integers(0, mbps * bs - T + 1, size=B).astype(np.int32)
-    cs[:3] = [0, window, window - T]
+    cs[:3] = [0, window, max(window - T, 0)]
     d_bt = torch.from_numpy(bt).cuda()
     d_cs = torch.from_numpy(cs).cuda()
     capi.oasr_window_commit(d_bt, d_cs, T, bs, window)
@@ -538,10 +541,12 @@ def test_window_commit_matches_oracle(bs, T, window, mbps):
     ref_bt, ref_cs = oracle.window_commit(bt, cs, T, bs, window)
     np.testing.assert_array_equal(d_bt.cpu().numpy(), ref_bt)
     np.testing.assert_array_equal(d_cs.cpu().numpy(), ref_cs)
+    assert (ref_cs >= 0).all()
     assert capi.oasr_device_status() == 0
 
 
-@pytest.mark.parametrize("bs,T,window", [(16, 16, 48), (8, 16, 40), (16, 8, 40)], ids=str)
+@pytest.mark.parametrize("bs,T,window", [(16, 16, 48), (8, 16, 40), (16, 8, 40), (16, 12, 3),
+                                         (8, 5, 1)], ids=str)
 def test_window_session_matches_the_sliding_history(bs, T, window):
     """A stream session under a trained window: every step is one fused append + attention
     launch followed by the commit with eviction; each step's output equals the oracle over
@@ -549,11 +554,11 @@ def test_window_session_matches_the_sliding_history(bs, T, window):
     oracle's bookkeeping exactly."""
     B, H, steps = 4, 2, 9
     rng = np.random.default_rng(bs + T + window)
-    mbps = -(-(window + T) // bs) + 1
+    mbps = -(-(max(window, bs) + T) // bs) + 1
     nblk = B * mbps + 5
     bt = rng.permutation(nblk)[: B * mbps].reshape(B, mbps).astype(np.int32)
     cs = np.zeros(B, np.int32)
-    R = window + 2 * T - 1
+    R = max(window, bs) + 2 * T - 1
     u, vb, rel = (syn.normal(rng, shp, "bf16") for shp in ((H, 64), (H, 64), (R, H, 64)))
     d = {"u": dev(u, "bf16"), "vb": dev(vb, "bf16"), "rel": dev(rel, "bf16")}
     kp = dev_pool(syn.canary_pool(nblk, bs, H, 64, "bf16"), "bf16")
@@ -574,7 +579,7 @@ def test_window_session_matches_the_sliding_history(bs, T, window):
         np.testing.assert_array_equal(d_cs.cpu().numpy(), cs)
         hk = np.concatenate([hk, kn], 1)
         hv = np.concatenate([hv, vn], 1)
-    assert int(cs[0]) <= window
+    assert 0 <= int(cs[0]) <= max(window, bs - 1)
     assert capi.oasr_device_status() == 0
 
 
