@@ -48,6 +48,7 @@ METRIC = "encoder frames/s per attention layer and achieved HBM GB/s vs GB300 pe
 UNIT = "frames/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0   # the ~8 TB/s the streaming step's HBM target is stated against
 KERNEL_SOURCES = ["chunk_attn.cu", "attn_core.cuh", "ptx.cuh"]
 PACKED_SOURCES = ["packed_tc.cu", "attn_core.cuh", "ptx.cuh"]
 
@@ -58,7 +59,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="conformer_small",
+    ap.add_argument("--config", default="conformer_large",
                     choices=sorted(syn.STREAMING_CONFIGS) + [syn.PACKED.name, NEMOTRON]
                     + sorted(PROJECTIONS))
     ap.add_argument("--two-call", action="store_true",
@@ -153,18 +154,29 @@ def source_digest(sources=None):
     return h.hexdigest()[:16]
 
 
+TRAFFIC_FILE = os.path.join("profiles", "traffic.json")
+
+
 def profiled_traffic(profile_name, sources=None):
-    """DRAM bytes per launch from the committed ncu summary profiles/<profile_name>.md, if it
-    was taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"{profile_name}.md")
-    if not os.path.exists(path):
-        return None
-    text = open(path).read()
-    m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
-    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not (m_sha and m_tr) or m_sha.group(1) != source_digest(sources):
-        return None
-    return float(m_tr.group(1))
+    """(DRAM bytes per launch, where from) of the ncu capture recorded under `profile_name` in
+    profiles/traffic.json, when that capture was taken on the current kernel source; else
+    (None, why not).  The bytes are dram__bytes_read.sum + dram__bytes_write.sum of one launch
+    of an earlier capture, not of this run."""
+    path = os.path.join(ROOT, TRAFFIC_FILE)
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(profile_name)
+    except (OSError, ValueError):
+        rec = None
+    if not rec:
+        return None, "no ncu capture recorded for this workload"
+    digest = source_digest(sources)
+    if rec.get("kernel_source_sha") != digest:
+        return None, (f"the recorded capture is of kernel source {rec.get('kernel_source_sha')}, "
+                      f"not the current {digest}")
+    return float(rec["dram_bytes_per_launch"]), (
+        f"ncu capture of kernel source {digest} recorded in {TRAFFIC_FILE} (not this run): "
+        f"{rec.get('capture')}")
 
 
 class ClockSampler:
@@ -647,7 +659,8 @@ def run_ours(args, cfg, rank, world, local):
         return
     peak, peak_kind = measured_hbm_peak()
     achieved = touched / (launch_us * 1e-6) / 1e9
-    traffic = None if args.two_call else profiled_traffic(f"chunk_step_{cfg.name}")
+    traffic, traffic_src = ((None, "not captured for the two-call step") if args.two_call
+                            else profiled_traffic(f"chunk_step_{cfg.name}"))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
@@ -665,7 +678,8 @@ def run_ours(args, cfg, rank, world, local):
                    "timing": "CUDA events around graph replays of the step on the launching stream",
                    "soak_s": args.soak_seconds},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
+                     "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_src,
+                     "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
                      "kernel": ("paged_append_kernel + chunk_attn_bf16_kernel" if args.two_call
                                 else "chunk_attn_bf16_kernel (fused append + attention)"),
                      "algorithmic_bytes_per_launch": touched,
@@ -857,6 +871,8 @@ def run_packed(args, rank, world, local, window=None):
         flops = packed_flops(x["lengths"], cfg.H, cfg.D)
     peak, kind = measured_tensor_peak()
     achieved = flops / per_call_s / 1e12
+    traffic, traffic_src = ((None, "no ncu capture recorded for the windowed call") if window
+                            else profiled_traffic("packed_varlen", PACKED_SOURCES))
     line = {
         "metric": METRIC, "value": total * args.steps * world / (ms / 1e3), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -870,7 +886,7 @@ def run_packed(args, rank, world, local, window=None):
                    "l2": f"inputs larger than L2: {packed_bytes(total, x['rel'].shape[0], cfg.H, cfg.D) / 1e6:.0f} MB per call"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
-                     "traffic": None if window else profiled_traffic("packed_varlen", PACKED_SOURCES),
+                     "traffic": traffic, "traffic_source": traffic_src,
                      "kernel": "packed_attn_tc_kernel", "algorithmic_flops_per_launch": flops,
                      "avg_launch_us": per_call_s * 1e6, "peak_kind": kind},
         "gpu_launches": args.steps, "clocks": clocks,
@@ -883,8 +899,37 @@ def run_packed(args, rank, world, local, window=None):
     print(json.dumps(line), flush=True)
 
 
+def torchrun_argv(nproc, argv, port):
+    """The command that runs this benchmark as `nproc` ranks of one node (one per GPU), with
+    the same arguments."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            f"--nproc-per-node={nproc}", "--master-addr", "127.0.0.1", "--master-port", str(port),
+            os.path.join(ROOT, "bench.py")] + list(argv)
+
+
+def free_port():
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def relaunch_ranks(args):
+    """`--gpus N` outside a launcher: run N ranks under torch.distributed.run and return its
+    exit code (None when this process is already a rank, or N is 1)."""
+    if args.gpus <= 1 or "WORLD_SIZE" in os.environ:
+        return None
+    if torch.cuda.is_available() and torch.cuda.device_count() < args.gpus:
+        sys.stderr.write(f"--gpus {args.gpus}: only {torch.cuda.device_count()} GPUs visible\n")
+        return 2
+    return subprocess.run(torchrun_argv(args.gpus, sys.argv[1:], free_port())).returncode
+
+
 def main():
     args = parse_args()
+    rc = relaunch_ranks(args)
+    if rc is not None:
+        sys.exit(rc)
     if args.impl == "reference" and (args.config in PROJECTIONS
                                      or args.config in (syn.PACKED.name, NEMOTRON)):
         run_reference_offline(args, args.config, int(os.environ.get("RANK", "0")))
