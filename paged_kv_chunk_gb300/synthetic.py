@@ -125,6 +125,14 @@ def normal(rng: np.random.Generator, shape, dtype: str, sigma: float = SIGMA) ->
     return round_to(rng.standard_normal(shape, dtype=np.float32) * np.float32(sigma), dtype)
 
 
+def quarters(rng: np.random.Generator, shape, amp: int = 4) -> np.ndarray:
+    """Integers drawn uniformly from [-amp, amp], divided by 4, as float32.  With amp <= 4 the
+    values, their sums with another such tensor and their products by powers of two up to 16
+    are exact in bf16, and dot products of 64 of them are exact in fp32: inputs for which a
+    score carries no rounding in any precision."""
+    return (rng.integers(-amp, amp + 1, size=shape).astype(np.float32) / np.float32(4.0))
+
+
 def block_table(rng: np.random.Generator, B: int, mbps: int, num_blocks: int) -> np.ndarray:
     """Each stream gets mbps distinct pool blocks from one seeded permutation."""
     if B * mbps > num_blocks:
