@@ -71,6 +71,10 @@ def parse_args():
     ap.add_argument("--soak-seconds", type=float, default=1.5,
                     help="untimed replays before the timed region, for the clock record")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--mbps", type=int, default=0,
+                    help="block-table width (max_blocks_per_seq) of a streaming cohort; entries past "
+                         "its pages are -1, as in an engine table sized for unlimited history "
+                         "(0: the pages the history needs)")
     return ap.parse_args()
 
 
@@ -474,7 +478,9 @@ def run_ours(args, cfg, rank, world, local):
     pools = [(dev_normal((nb, bs, H, D)), dev_normal((nb, bs, H, D))) for _ in range(layers)]
     params = [(dev_normal((H, D)), dev_normal((H, D)), dev_normal((cfg.R, H, D)))
               for _ in range(layers)]
-    bt_h = syn.block_table(rng, B, cfg.mbps, nb)
+    mbps = max(args.mbps, cfg.mbps)
+    bt_h = np.full((B, mbps), -1, np.int32)
+    bt_h[:, :cfg.mbps] = syn.block_table(rng, B, cfg.mbps, nb)
     cs_h = syn.cache_lengths(cfg)
     bt = torch.from_numpy(bt_h).to(dev)
     cs = torch.from_numpy(cs_h).to(dev)
@@ -671,6 +677,7 @@ def run_ours(args, cfg, rank, world, local):
                    "cache": (f"U{{0..{cfg.C}}} per stream (mean {cs_h.mean():.1f})" if cfg.hetero
                              else cfg.C),
                    "block_size": bs, "pool_blocks": nb, "rel_rows": cfg.R,
+                   "max_blocks_per_seq": mbps,
                    "layers": layers, "global_batch": B * world, "seq_len": cfg.K,
                    "parallelism": f"dp{world}",
                    "l2": f"inputs larger than L2: {layers} distinct layer pools, "

@@ -96,9 +96,12 @@ oasr_status oasr_paged_append(const void* k_new, const void* v_new, void* k_pool
  * the pool holds for stream b (C_b = cache_seqlens[b]: the cached frames followed by
  * this chunk, which oasr_paged_append must already have written on the same stream)
  * and writes out[b][i][h][:].  Requirements: D = 64; 1 <= T <= 64; block_size a power of
- * two in [8, 256]; R >= max_b C_b + 2T - 1 (a shorter table reads zero rows for the
- * missing distances); C_b + T <= max_blocks_per_seq * block_size (keys past the table
- * are dropped, status bit OASR_ERR_BOUNDS).  scale is normally 1/sqrt(D).
+ * two in [8, 256]; R >= max_b C_b + 2T - 1; C_b + T <= max_blocks_per_seq * block_size.
+ * A stream that breaks either raises the status bit OASR_ERR_BOUNDS and its row is then
+ * unspecified: the bf16 path drops its keys past min(max_blocks_per_seq * block_size,
+ * R - T + 1) (the keys the host can bound, for which it sizes its shared memory, so an
+ * engine-sized block table costs nothing), the f32 path drops keys past the table's pages
+ * and reads zero rows for the distances the rel table lacks.  scale is normally 1/sqrt(D).
  * bf16: bf16 inputs, fp32 accumulation and softmax, bf16 output rounded once.
  * f32: fp32 throughout (no TF32).
  */

@@ -49,6 +49,9 @@ struct ChunkArgs {
     int num_blocks, block_size, mbps, T, H, R;
     int box_rows;            // rows of one K/V TMA box = min(block_size, 64)
     int gt_w;                // position-table variant: row stride of the table (floats)
+    int k_max;               // keys a stream may have: the table's pages and the keys the rel
+                             // table serves (R - T + 1); the position table is sized for them
+    int bt_pages;            // block-table entries a CTA reads: ceil(k_max / block_size)
     float scale_log2;        // scale * log2(e)
 };
 
@@ -156,11 +159,12 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
         }
     }
     int C = __ldg(a.cache_seqlens + b);
-    // The whole block-table row (mbps <= kMaxPages, host check), not just the pages of the
-    // K keys: its loads go out beside the cache length's instead of after it.
+    // The block-table entries of every key a stream may have (bt_pages <= mbps <= kMaxPages,
+    // host check), not just the pages of this stream's K keys: their loads go out beside the
+    // cache length's instead of after it.
     int* s_bt = reinterpret_cast<int*>(sm + SP::off_bt);
     if (!GT || warp == kConsumerWarps) {   // GT: the producer warp alone, so no rel load delays it
-        for (int i = GT ? lane : tid; i < a.mbps; i += GT ? 32 : kThreads)
+        for (int i = GT ? lane : tid; i < a.bt_pages; i += GT ? 32 : kThreads)
             s_bt[i] = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + i);
     }
     // Position-table variant: u, v go out beside the block-table row (the producer warp
@@ -174,8 +178,11 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
     }
     if (C < 0) { C = 0; err |= kErrBounds; }
     int K = C + T;
-    const int cap = a.mbps * a.block_size;
+    // keys past the table's pages (or past the keys the position table was sized for, which
+    // only a rel table shorter than C + 2T - 1 rows allows) are dropped
+    const int cap = a.k_max;
     if (K > cap) { K = cap; err |= kErrBounds; }
+    if (C + 2 * T - 1 > a.R) err |= kErrBounds;   // distances the rel table does not hold
     const int off = a.R - T - C;   // rho = off + j - i
     __syncthreads();
 
@@ -250,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
         // The producer warp only issues copies: no other work shares its warp.
         // without the direct chunk stage, stages from this one on hold chunk rows
         const int first_chunk_stage = (FUSED && !direct) ? C / kStageKeys : n_stages;
+        int n_issued = 0;
         for (int issued = 0; issued < n_stages; ++issued) {
             const int slot = issued % NS;
             bool ok = issued < NS || mbar_wait(bar_empty + 8 * slot, ((issued / NS) - 1) & 1);
@@ -259,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
                 break;
             }
             issue(issued);
+            n_issued = issued + 1;
         }
         if (GT && FUSED && direct) {
             // with every stage out, the chunk's rows (in their own region) go into the pool;
@@ -281,6 +290,11 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
                 err |= kErrTimeout;
             }
         }
+        // Every copy this CTA requested lands before the CTA can end, also when a consumer's
+        // wait ran out and it left early (bounded waits: the last stage of each slot, Q).
+        for (int x = n_issued > NS ? n_issued - NS : 0; x < n_issued; ++x)
+            if (!mbar_wait(bar_full + 8 * (x % NS), (x / NS) & 1)) err |= kErrTimeout;
+        if (!mbar_wait(bar_q, 0)) err |= kErrTimeout;
         if (err) atomicOr(a.status, err);
         return;
     }
@@ -446,6 +460,7 @@ __global__ void __launch_bounds__(128) chunk_attn_f32_kernel(
     int K = C + T;
     const int cap = mbps * block_size;
     if (K > cap) { K = cap; err |= kErrBounds; }
+    if (C + 2 * T - 1 > R) err |= kErrBounds;   // distances the rel table does not hold
     const int off = R - T - C;
 
     if (FUSED) {
@@ -555,6 +570,16 @@ constexpr int kThreeCtaSmem = 74 * 1024;
 // below cap + 32, and a stride of 8 mod 32 keeps the 8-byte reads of a slice conflict-free.
 inline int pos_table_stride(int cap) { return ((cap + 32 + 31) & ~31) + 8; }
 
+// Keys a stream of a call may have, as the host knows them: the table's pages, and the
+// R - T + 1 keys a rel table of R rows serves (R >= C + 2T - 1 is required).
+inline int key_bound(int mbps, int block_size, int R, int T)
+{
+    const long long pages = static_cast<long long>(mbps) * block_size;
+    const long long rel = static_cast<long long>(R) - T + 1;
+    const long long k = pages < rel ? pages : rel;
+    return static_cast<int>(k < T ? T : k);
+}
+
 template <int MT, int NS, bool FUSED, bool GT>
 oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, void* k_pool,
                         void* v_pool, int num_blocks, int block_size, const int32_t* bt,
@@ -584,7 +609,10 @@ oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, voi
     unsigned* status = status_word();
     if (!status) return OASR_ERR_CUDA;
     auto kern = chunk_attn_bf16_kernel<MT, NS, FUSED, GT>;
-    const int gt_w = GT ? pos_table_stride(mbps * block_size) : 0;
+    // the keys the host can bound (the position table is sized for them); a stream with more
+    // (a rel table shorter than the precondition allows) is clamped to them and flagged
+    const int k_max = key_bound(mbps, block_size, R, T);
+    const int gt_w = GT ? pos_table_stride(k_max) : 0;
     const int smem = ChunkSmem<MT, NS, GT>::bytes + 16 * gt_w * 4;
     if (!ensure_smem(kern, smem, g_smem_done[slot])) return OASR_ERR_CUDA;
     ChunkArgs a;
@@ -607,6 +635,8 @@ oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, voi
     a.R = R;
     a.box_rows = box;
     a.gt_w = gt_w;
+    a.k_max = k_max;
+    a.bt_pages = (k_max + block_size - 1) / block_size;
     a.scale_log2 = scale * 1.4426950408889634f;
     return launch_pdl(kern, dim3(static_cast<unsigned>(B) * H), dim3(kThreads), smem, stream, tm_q,
                       tm_k, tm_v, tm_r, tm_kn, tm_vn, a);
@@ -649,8 +679,10 @@ oasr_status dispatch(const void* q, const void* k_new, const void* v_new, void* 
     const int f = FUSED ? 8 : 0;
     // one m-tile: the position table when it fits beside four stages with two CTAs per SM
     // (histories up to 544 keys; a table past 320 columns takes each warp a second batch of
-    // rel loads, still faster than the band on 528-key histories), else the per-stage band
-    const long long cap = static_cast<long long>(mbps) * block_size;
+    // rel loads, still faster than the band on 528-key histories), else the per-stage band.
+    // The table is sized for the keys the host can bound (the table's pages, and the keys the
+    // rel table serves), so an engine-sized block table keeps the faster form.
+    const long long cap = key_bound(mbps, block_size, R, T);
     // a grid of several waves at two CTAs per SM with a short history: the same kernel with a
     // two-stage ring, three or four CTAs per SM (more CTAs resident beats stages in flight
     // there: three measured 18 % faster on the T = 4 sweep, four another 16 % on T = 4 and 15 %

@@ -656,6 +656,46 @@ def test_widest_block_table(fused):
     assert capi.oasr_device_status() == 0
 
 
+@pytest.mark.parametrize("cfg", [syn.SMALL, syn.LARGE], ids=lambda c: c.name)
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
+def test_engine_sized_block_table(cfg, fused):
+    """The engine's table geometry (ASR Engine page, section 6: max_blocks_per_seq sized for
+    unlimited history, 512 pages): the cohort's pages first and every later entry -1.  The
+    kernel sizes its work from the keys it can bound (the rel table's R - T + 1), so the result
+    and the pools are bit-identical to the exact-size table's, and no entry past the pages is
+    read (the status word stays clear)."""
+    x = stream_case(cfg)
+    out_exact, d_exact = _run_step(cfg, x, fused)
+    wide = np.full((cfg.B, 512), -1, np.int32)
+    wide[:, :cfg.mbps] = x["block_table"]
+    xw = dict(x)
+    xw["block_table"] = wide
+    out_wide, d_wide = _run_step(cfg, xw, fused)
+    assert torch.equal(out_exact.view(torch.int16), out_wide.view(torch.int16))
+    assert torch.equal(d_exact["k_pool"].view(torch.int16), d_wide["k_pool"].view(torch.int16))
+    assert torch.equal(d_exact["v_pool"].view(torch.int16), d_wide["v_pool"].view(torch.int16))
+    rng = np.random.default_rng(cfg.seed + 5)
+    rows = sample_rows(rng, cfg.B, cfg.T, cfg.H, 512)
+    ref = oracle_chunk(x, rows=rows)
+    b, i, h = rows[:, 0], rows[:, 1], rows[:, 2]
+    check_close(to_np(out_wide)[b, i, h], ref[b, i, h], "bf16", "engine-sized table")
+    assert capi.oasr_device_status() == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("T", [4, 16, 40])
+def test_short_rel_table_is_flagged(dtype, T):
+    """A rel table shorter than C + 2T - 1 rows breaks the call's precondition: the call stays
+    in bounds and raises the bounds bit of the status word."""
+    cfg = syn.StreamingConfig("short_rel", B=2, H=2, D=64, T=T, C=100, block_size=16, dtype=dtype,
+                              seed=55)
+    x = stream_case(cfg, R=cfg.R - 5)
+    _run_step(cfg, x, fused=True)
+    assert capi.oasr_device_status() & capi.STATUS_BOUNDS_BIT
+    _run_step(cfg, stream_case(cfg), fused=True)
+    assert capi.oasr_device_status() == 0
+
+
 @pytest.mark.parametrize("window", [None, (8, 7)], ids=["bidirectional", "chunked"])
 def test_packed_most_segments(window):
     """The largest segment count the packed calls take (1024), lengths 0..40."""
