@@ -48,6 +48,7 @@ struct ChunkArgs {
     unsigned* status;
     int num_blocks, block_size, mbps, T, H, R;
     int box_rows;            // rows of one K/V TMA box = min(block_size, 64)
+    int bs_shift;            // log2(block_size)
     int gt_w;                // position-table variant: row stride of the table (floats)
     int k_max;               // keys a stream may have: the table's pages and the keys the rel
                              // table serves (R - T + 1); the position table is sized for them
@@ -136,45 +137,65 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
     float* s_vb = reinterpret_cast<float*>(sm + SP::off_vb);
     __shared__ int s_failed;
 
-    if (tid == 0) {
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(bar_full + 8 * i, 1);
-            // one m-tile: all consumer warps read every stage (16-key slices)
-            mbar_init(bar_empty + 8 * i, MT == 1 ? kConsumerWarps : MT);
-        }
-        mbar_init(bar_q, 1);
-        mbar_init(bar_written, 32 * kConsumerWarps);
-        mbar_init(bar_chunk, 1);
-        fence_mbar_init();
-        s_failed = 0;
-        // the Q tile needs neither the cache length nor the block table: it is requested
-        // before either is read
-        mbar_arrive_expect_tx(bar_q, TL::Tp * kRowBytes);
-        tma_load_3d(sb + SP::off_q, &tm_q, bar_q, 0, h, b * T);
-        if (GT && FUSED) {
-            // nor do the chunk's rows (T <= 16: one 16-row box each for K and V)
-            mbar_arrive_expect_tx(bar_chunk, 2 * 16 * kRowBytes);
-            tma_load_3d(sb + SP::off_ck, &tm_kn, bar_chunk, 0, h, b * T);
-            tma_load_3d(sb + SP::off_ck + 16 * kRowBytes, &tm_vn, bar_chunk, 0, h, b * T);
-        }
-    }
-    int C = __ldg(a.cache_seqlens + b);
-    // The block-table entries of every key a stream may have (bt_pages <= mbps <= kMaxPages,
-    // host check), not just the pages of this stream's K keys: their loads go out beside the
-    // cache length's instead of after it.
+    // The producer warp sets up the barriers, requests Q (and the chunk's rows), loads the
+    // block-table row and starts issuing stages without waiting for the consumers: named
+    // barrier 2 (producer arrives, consumers wait) hands them the initialised barriers and the
+    // row in shared memory.
     int* s_bt = reinterpret_cast<int*>(sm + SP::off_bt);
-    if (!GT || warp == kConsumerWarps) {   // GT: the producer warp alone, so no rel load delays it
-        for (int i = GT ? lane : tid; i < a.bt_pages; i += GT ? 32 : kThreads)
-            s_bt[i] = __ldg(a.block_table + static_cast<long long>(b) * a.mbps + i);
-    }
-    // Position-table variant: u, v go out beside the block-table row (the producer warp
-    // alone loads the row, and the table's rel rows are requested only once the row is in:
-    // issued earlier they delay it and the first stages behind them).
-    if (GT && warp < kConsumerWarps) {
+    const bool producer = warp == kConsumerWarps;
+    int C = __ldg(a.cache_seqlens + b);
+    if (producer) {
+        // the block-table entries of every key a stream may have (bt_pages <= mbps <=
+        // kMaxPages, host check), not just the pages of this stream's K keys: their loads go
+        // out beside the cache length's instead of after it (the first 128 held in registers
+        // meanwhile, the rest of a longer row copied after)
+        constexpr int kRowRegs = 4;
+        const int32_t* bt_row = a.block_table + static_cast<long long>(b) * a.mbps;
+        int row[kRowRegs];
+#pragma unroll
+        for (int k = 0; k < kRowRegs; ++k) {
+            const int i = lane + 32 * k;
+            if (i < a.bt_pages) row[k] = __ldg(bt_row + i);
+        }
+        if (lane == 0) {
+            for (int i = 0; i < NS; ++i) {
+                mbar_init(bar_full + 8 * i, 1);
+                // one m-tile: all consumer warps read every stage (16-key slices)
+                mbar_init(bar_empty + 8 * i, MT == 1 ? kConsumerWarps : MT);
+            }
+            mbar_init(bar_q, 1);
+            mbar_init(bar_written, 32 * kConsumerWarps);
+            mbar_init(bar_chunk, 1);
+            fence_mbar_init();
+            s_failed = 0;
+            // the Q tile needs neither the cache length nor the block table: it is requested
+            // before either is read
+            mbar_arrive_expect_tx(bar_q, TL::Tp * kRowBytes);
+            tma_load_3d(sb + SP::off_q, &tm_q, bar_q, 0, h, b * T);
+            if (GT && FUSED) {
+                // nor do the chunk's rows (T <= 16: one 16-row box each for K and V)
+                mbar_arrive_expect_tx(bar_chunk, 2 * 16 * kRowBytes);
+                tma_load_3d(sb + SP::off_ck, &tm_kn, bar_chunk, 0, h, b * T);
+                tma_load_3d(sb + SP::off_ck + 16 * kRowBytes, &tm_vn, bar_chunk, 0, h, b * T);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kRowRegs; ++k) {
+            const int i = lane + 32 * k;
+            if (i < a.bt_pages) s_bt[i] = row[k];
+        }
+        for (int i = lane + 32 * kRowRegs; i < a.bt_pages; i += 32) s_bt[i] = __ldg(bt_row + i);
+        __syncwarp();
+        named_bar_arrive(2, kThreads);
+    } else {
+        // u, v go out beside the block-table row (the position table's rel rows are requested
+        // only once the row is in: issued earlier they delay it and the first stages behind
+        // them)
         if (tid < kHeadDim)
             s_u[tid] = bf16_lo(__ldg(a.pos_bias_u + h * kHeadDim + tid));
         else
             s_vb[tid - kHeadDim] = bf16_lo(__ldg(a.pos_bias_v + h * kHeadDim + tid - kHeadDim));
+        named_bar_sync(2, kThreads);
     }
     if (C < 0) { C = 0; err |= kErrBounds; }
     int K = C + T;
@@ -184,13 +205,13 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
     if (K > cap) { K = cap; err |= kErrBounds; }
     if (C + 2 * T - 1 > a.R) err |= kErrBounds;   // distances the rel table does not hold
     const int off = a.R - T - C;   // rho = off + j - i
-    __syncthreads();
+    const int sh = a.bs_shift;
 
     // Stage plan (every thread derives the same one from the cached table row).
     bool direct = false;
     if (FUSED && C + T <= cap) {
         direct = true;
-        for (int pg = C / a.block_size; pg <= (C + T - 1) / a.block_size; ++pg) {
+        for (int pg = C >> sh; pg <= (C + T - 1) >> sh; ++pg) {
             const int blk = s_bt[pg];
             if (blk < 0 || blk >= a.num_blocks) direct = false;
         }
@@ -210,10 +231,10 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
         return left < kStageKeys ? left : kStageKeys;
     };
 
-    // Stage s into slot s % NS, by the whole producer warp: lane q issues the K and V boxes
-    // of the stage's q-th page (or 16-row piece of the chunk), lane 0 the band box, so a
-    // stage's boxes go out in one instruction rather than one after another.
-    auto issue = [&](int s) {
+    // Stage s into slot s % NS, by the whole producer warp: lane q issues the K box of the
+    // stage's q-th page (or 16-row piece of the chunk) and lane 16 + q its V box, lane 31 the
+    // band box, so a stage's boxes go out in one instruction rather than one after another.
+    auto issue = [&](int s, uint64_t pol) {
         const int slot = s % NS;
         const uint32_t bar = bar_full + 8 * slot;
         const uint32_t base = sb + SP::off_slots + slot * SP::kSlot;
@@ -226,35 +247,33 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
             mbar_arrive_expect_tx(
                 bar, static_cast<uint32_t>((2 * nbox * box + (GT ? 0 : TL::RB)) * kRowBytes));
         __syncwarp();
-        if (lane < nbox) {
-            const uint32_t dk = base + lane * box * kRowBytes;
-            const uint32_t dv = dk + kStageKeys * kRowBytes;
+        const int q = lane & 15;
+        const bool is_v = lane >= 16;
+        if (q < nbox) {
+            const uint32_t dst = base + (q * box + (is_v ? kStageKeys : 0)) * kRowBytes;
             if (chunk) {
-                tma_load_3d(dk, &tm_kn, bar, 0, h, b * T + 16 * lane);
-                tma_load_3d(dv, &tm_vn, bar, 0, h, b * T + 16 * lane);
+                tma_load_3d(dst, is_v ? &tm_vn : &tm_kn, bar, 0, h, b * T + 16 * q);
             } else {
-                const int j = j0 + lane * box;
-                const int lb = j / a.block_size;
+                const int j = j0 + q * box;
+                const int lb = j >> sh;
                 const int blk = s_bt[lb];
                 int row;
                 if (blk < 0 || blk >= a.num_blocks) {
                     err |= kErrBounds;
                     row = -2 * box;   // outside the pool: the box reads zeros
                 } else {
-                    row = blk * a.block_size + (j - lb * a.block_size);
+                    row = (blk << sh) + (j - (lb << sh));
                 }
-                const uint64_t pol = policy_evict_first();
-                tma_load_3d_hint(dk, &tm_k, bar, 0, h, row, pol);
-                tma_load_3d_hint(dv, &tm_v, bar, 0, h, row, pol);
+                tma_load_3d_hint(dst, is_v ? &tm_v : &tm_k, bar, 0, h, row, pol);
             }
         }
-        if (!GT && lane == 0)
+        if (!GT && lane == 31)
             tma_load_3d(base + 2 * kStageKeys * kRowBytes, &tm_r, bar, 0, h, off + j0 - (TL::Tp - 1));
     };
 
-    const bool producer = warp == kConsumerWarps;
     if (producer) {
         // The producer warp only issues copies: no other work shares its warp.
+        const uint64_t pol = policy_evict_first();
         // without the direct chunk stage, stages from this one on hold chunk rows
         const int first_chunk_stage = (FUSED && !direct) ? C / kStageKeys : n_stages;
         int n_issued = 0;
@@ -266,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
                 err |= kErrTimeout;
                 break;
             }
-            issue(issued);
+            issue(issued, pol);
             n_issued = issued + 1;
         }
         if (GT && FUSED && direct) {
@@ -293,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
         // Every copy this CTA requested lands before the CTA can end, also when a consumer's
         // wait ran out and it left early (bounded waits: the last stage of each slot, Q).
         for (int x = n_issued > NS ? n_issued - NS : 0; x < n_issued; ++x)
-            if (!mbar_wait(bar_full + 8 * (x % NS), (x / NS) & 1)) err |= kErrTimeout;
-        if (!mbar_wait(bar_q, 0)) err |= kErrTimeout;
+            if (!mbar_wait_idle(bar_full + 8 * (x % NS), (x / NS) & 1)) err |= kErrTimeout;
+        if (!mbar_wait_idle(bar_q, 0)) err |= kErrTimeout;
         if (err) atomicOr(a.status, err);
         return;
     }
@@ -351,10 +370,6 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
         named_bar_sync(1, 32 * kConsumerWarps);   // the table is complete
         if (!failed) make_q_frags(sb + SP::off_q, s_u, s_vb, mt, lane, qu, qv);
     } else {
-        if (tid < kHeadDim)
-            s_u[tid] = bf16_lo(__ldg(a.pos_bias_u + h * kHeadDim + tid));
-        else
-            s_vb[tid - kHeadDim] = bf16_lo(__ldg(a.pos_bias_v + h * kHeadDim + tid - kHeadDim));
         if constexpr (FUSED) copy_chunk_global();
         named_bar_sync(1, 32 * kConsumerWarps);
         failed = !mbar_wait(bar_q, 0);
@@ -634,6 +649,7 @@ oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, voi
     a.H = H;
     a.R = R;
     a.box_rows = box;
+    a.bs_shift = __builtin_ctz(static_cast<unsigned>(block_size));
     a.gt_w = gt_w;
     a.k_max = k_max;
     a.bt_pages = (k_max + block_size - 1) / block_size;

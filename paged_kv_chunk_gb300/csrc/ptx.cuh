@@ -97,6 +97,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     }
 }
 
+// As mbar_wait, for a thread with nothing else to do meanwhile: it sleeps between polls, so
+// its warp takes no issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity,
+                                               uint64_t limit_ns = kWaitLimitNs)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        __nanosleep(256);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // --------------------------------------------------------------- proxies
 
 // Order this thread's earlier generic-proxy global writes before later async-proxy
