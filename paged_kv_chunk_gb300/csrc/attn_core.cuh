@@ -65,6 +65,10 @@ __device__ __forceinline__ void acc_init(WarpAcc& a)
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ uint16_t bf16_bits(float x)
+{
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // A fragments of bf16(q + u) and bf16(q + v) for the warp's 16 query rows (rows 16*mt..)
@@ -355,7 +359,10 @@ __device__ __forceinline__ void warp_slice16(WarpAcc& acc, const uint32_t (&qu)[
 
 // Position table of one CTA (16 query rows of one head), built once before the key loop:
 // G[i][c] = bf16(q_i + v) . rel[rho0 + c] for c in [0, ncols), rel rows outside [0, R) taken
-// as zero.  It is stored pre-skewed, G[i][c] at gs[i*W + c + i + 1], so that query i and key j
+// as zero, accumulated in fp32 and stored rounded to bf16 (a relative 2^-9 of the position
+// term, the order of the bf16 rounding of P; half the shared memory of fp32, which lets four
+// CTAs share an SM on short histories and five stages fit on long ones).  It is stored
+// pre-skewed, G[i][c] at gs[i*W + c + i + 1], so that query i and key j
 // (c = j + 15 - i) read gs[i*W + j + 16]: one row of a slice's scores is one contiguous run.
 // Warp `warp` of `nw` computes column tiles warp, warp + nw, ...  The head dimension is
 // contracted in a permuted order: lane quad position t4 holds dims [16 t4, 16 t4 + 16) of
@@ -390,7 +397,7 @@ struct PosTable {
 
     // q_tile: the 128-byte-swizzled Q tile; v: the bias v in fp32 (smem).  load(warp) must
     // have been called.
-    __device__ __forceinline__ void build(float* gs, int W, const uint8_t* q_tile, const float* v)
+    __device__ __forceinline__ void build(uint16_t* gs, int W, const uint8_t* q_tile, const float* v)
     {
         const int g4 = lane >> 2, t4 = lane & 3;
         uint32_t qa[4][4];
@@ -422,7 +429,7 @@ struct PosTable {
     }
 
     template <int N>
-    __device__ __forceinline__ void tiles(float* gs, int W, const uint32_t (&qa)[4][4], int nb0)
+    __device__ __forceinline__ void tiles(uint16_t* gs, int W, const uint32_t (&qa)[4][4], int nb0)
     {
         const int g4 = lane >> 2, t4 = lane & 3;
         float c[N][4];
@@ -443,8 +450,8 @@ struct PosTable {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 if (col + e < ncols) {
-                    gs[g4 * W + col + e + g4 + 1] = c[u][e];
-                    gs[(g4 + 8) * W + col + e + g4 + 9] = c[u][2 + e];
+                    gs[g4 * W + col + e + g4 + 1] = bf16_bits(c[u][e]);
+                    gs[(g4 + 8) * W + col + e + g4 + 9] = bf16_bits(c[u][2 + e]);
                 }
             }
         }
@@ -456,29 +463,29 @@ struct PosTable {
 // gq[i*W + jl].  k_s, v_s: the slice's 16 K and V rows (128-byte swizzled); keys
 // [0, kvalid) of the slice exist.
 __device__ __forceinline__ void warp_slice16_gt(WarpAcc& acc, const uint32_t (&qu)[4][4],
-                                                uint32_t k_s, uint32_t v_s, const float* gq,
+                                                uint32_t k_s, uint32_t v_s, const uint16_t* gq,
                                                 int W, bool even, int kvalid, float scale_log2,
                                                 int lane)
 {
     const int g4 = lane >> 2, t4 = lane & 3, mi = lane >> 3;
     float gb[2][4];   // [nt][row g4 cols 2t4, 2t4+1 | row g4+8 cols 2t4, 2t4+1]
     {
-        const float* r0 = gq + g4 * W + 2 * t4;
-        const float* r1 = r0 + 8 * W;
+        const uint16_t* r0 = gq + g4 * W + 2 * t4;
+        const uint16_t* r1 = r0 + 8 * W;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             if (even) {
-                const float2 x = *reinterpret_cast<const float2*>(r0 + 8 * nt);
-                const float2 y = *reinterpret_cast<const float2*>(r1 + 8 * nt);
-                gb[nt][0] = x.x;
-                gb[nt][1] = x.y;
-                gb[nt][2] = y.x;
-                gb[nt][3] = y.y;
+                const uint32_t x = *reinterpret_cast<const uint32_t*>(r0 + 8 * nt);
+                const uint32_t y = *reinterpret_cast<const uint32_t*>(r1 + 8 * nt);
+                gb[nt][0] = bf16_lo(x);
+                gb[nt][1] = bf16_hi(x);
+                gb[nt][2] = bf16_lo(y);
+                gb[nt][3] = bf16_hi(y);
             } else {
-                gb[nt][0] = r0[8 * nt];
-                gb[nt][1] = r0[8 * nt + 1];
-                gb[nt][2] = r1[8 * nt];
-                gb[nt][3] = r1[8 * nt + 1];
+                gb[nt][0] = bf16_lo(r0[8 * nt]);
+                gb[nt][1] = bf16_lo(r0[8 * nt + 1]);
+                gb[nt][2] = bf16_lo(r1[8 * nt]);
+                gb[nt][3] = bf16_lo(r1[8 * nt + 1]);
             }
         }
     }

@@ -13,7 +13,7 @@
 // one box per block-table page for K and for V (the page's rows of this head, 128 B each,
 // 128-byte swizzled), all arriving on one mbarrier.  The position term comes one of two
 // ways.  Position table (GT; T <= 16 and a history that fits): the consumer warps compute
-// the CTA's whole term once, from rel rows read from L2, into a pre-skewed fp32 table in
+// the CTA's whole term once, from rel rows read from L2, into a pre-skewed bf16 table in
 // shared memory while the first pages are in flight, and every 16-key slice reads it back.
 // Band (otherwise): each stage also carries a box of the rel band, and each slice or stage
 // multiplies it and skews the product through shared memory.  The per-slice and per-stage
@@ -49,7 +49,7 @@ struct ChunkArgs {
     int num_blocks, block_size, mbps, T, H, R;
     int box_rows;            // rows of one K/V TMA box = min(block_size, 64)
     int bs_shift;            // log2(block_size)
-    int gt_w;                // position-table variant: row stride of the table (floats)
+    int gt_w;                // position-table variant: row stride of the table (bf16 elements)
     int k_max;               // keys a stream may have: the table's pages and the keys the rel
                              // table serves (R - T + 1); the position table is sized for them
     int bt_pages;            // block-table entries a CTA reads: ceil(k_max / block_size)
@@ -82,7 +82,7 @@ struct ChunkSmem {
     static constexpr int off_bt = off_vb + kHeadDim * 4;    // the stream's block-table row
     static constexpr int off_bar = off_bt + kMaxPages * 4;  // full[NS], empty[NS], q, written, chunk
     static constexpr int off_gt = (off_bar + (2 * NS + 3) * 8 + 15) & ~15;
-    static constexpr int bytes = off_gt + 1024;   // + 16 * gt_w * 4 with GT
+    static constexpr int bytes = off_gt + 1024;   // + 16 * gt_w * 2 with GT
     static constexpr int comb_o = 0;
     static constexpr int comb_m = comb_o + TL::KG * TL::Tp * kOW * 4;
     static constexpr int comb_l = comb_m + TL::KG * TL::Tp * 4;
@@ -92,8 +92,7 @@ struct ChunkSmem {
 };
 
 // Two CTAs per SM; the position-table kernel with a two-stage ring (short histories on grids
-// of several waves) is built for four (96 registers, no spills), with lighter batches of rel
-// loads, so that its shared memory alone sets how many share an SM: four up to 56 KB, else three.
+// of several waves) is built for four (96 registers), with lighter batches of rel loads.
 template <int MT, int NS, bool FUSED, bool GT>
 __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_bf16_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -363,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
         // first pages land
         failed = !mbar_wait(bar_q, 0);
         if (!failed)
-            pt.build(reinterpret_cast<float*>(sm + SP::off_gt), a.gt_w, sm + SP::off_q, s_vb);
+            pt.build(reinterpret_cast<uint16_t*>(sm + SP::off_gt), a.gt_w, sm + SP::off_q, s_vb);
         // fused: the chunk's rows (requested at the start; they must land before the CTA
         // ends even when the stages do not use them)
         if (FUSED && !mbar_wait(bar_chunk, 0)) failed = true;
@@ -378,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
     if (!failed) {
         float* gw = reinterpret_cast<float*>(sm + SP::off_g) + warp * (kGBytes / 4);
         if constexpr (GT) {
-            const float* gs = reinterpret_cast<const float*>(sm + SP::off_gt);
+            const uint16_t* gs = reinterpret_cast<const uint16_t*>(sm + SP::off_gt);
             if (FUSED && direct) {
                 // the chunk, landed long before the first pool stage: its keys are warp 0's
                 // first slice (the producer warp writes its rows into the pool)
@@ -576,14 +575,14 @@ __global__ void __launch_bounds__(128) chunk_attn_f32_kernel(
 
 int g_smem_done[16][64];
 
-// Dynamic shared memory of one CTA that still lets two (three) CTAs share an SM (four share
-// one up to 56 KB).
+// Dynamic shared memory of one CTA that still lets two (four) CTAs share an SM.
 constexpr int kTwoCtaSmem = 112 * 1024;
-constexpr int kThreeCtaSmem = 74 * 1024;
+constexpr int kFourCtaSmem = 56 * 1024;
 
-// Row stride (floats) of the position table for keys up to `cap`: every read and write stays
-// below cap + 32, and a stride of 8 mod 32 keeps the 8-byte reads of a slice conflict-free.
-inline int pos_table_stride(int cap) { return ((cap + 32 + 31) & ~31) + 8; }
+// Row stride (bf16 elements) of the position table for keys up to `cap`: every read and write
+// stays below cap + 32, and a stride of 16 mod 64 elements (8 mod 32 words) keeps the 4-byte
+// reads of a slice conflict-free.
+inline int pos_table_stride(int cap) { return ((cap + 32 + 63) & ~63) + 16; }
 
 // Keys a stream of a call may have, as the host knows them: the table's pages, and the
 // R - T + 1 keys a rel table of R rows serves (R >= C + 2T - 1 is required).
@@ -628,7 +627,7 @@ oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, voi
     // (a rel table shorter than the precondition allows) is clamped to them and flagged
     const int k_max = key_bound(mbps, block_size, R, T);
     const int gt_w = GT ? pos_table_stride(k_max) : 0;
-    const int smem = ChunkSmem<MT, NS, GT>::bytes + 16 * gt_w * 4;
+    const int smem = ChunkSmem<MT, NS, GT>::bytes + 16 * gt_w * 2;
     if (!ensure_smem(kern, smem, g_smem_done[slot])) return OASR_ERR_CUDA;
     ChunkArgs a;
     a.k_new = static_cast<const uint16_t*>(k_new);
@@ -693,27 +692,31 @@ oasr_status dispatch(const void* q, const void* k_new, const void* v_new, void* 
         return launch_status();
     }
     const int f = FUSED ? 8 : 0;
-    // one m-tile: the position table when it fits beside four stages with two CTAs per SM
-    // (histories up to 544 keys; a table past 320 columns takes each warp a second batch of
-    // rel loads, still faster than the band on 528-key histories), else the per-stage band.
-    // The table is sized for the keys the host can bound (the table's pages, and the keys the
-    // rel table serves), so an engine-sized block table keeps the faster form.
+    // One m-tile (T <= 16): the position table when it fits beside the ring, else the
+    // per-stage band.  The table is sized for the keys the host can bound (the table's pages,
+    // and the keys the rel table serves), so an engine-sized block table keeps the table form.
+    // Grids of several waves at two CTAs per SM: four CTAs per SM with a two-stage ring when
+    // their shared memory allows it (short histories: more CTAs resident beat stages in flight,
+    // T = 16 24.3 -> 21.3 us, T = 4 and T = 8 15-18 % each), else two with five stages
+    // (Conformer-large 63.4 -> 62.6 us); one wave: two CTAs with four stages.
     const long long cap = key_bound(mbps, block_size, R, T);
-    // a grid of several waves at two CTAs per SM with a short history: the same kernel with a
-    // two-stage ring, three or four CTAs per SM (more CTAs resident beats stages in flight
-    // there: three measured 18 % faster on the T = 4 sweep, four another 16 % on T = 4 and 15 %
-    // on T = 8; slower on one-wave cohorts)
     const int sms = sm_count();
-    if (T <= 16 && cap <= 4096 && sms > 0 && static_cast<long long>(B) * H > 2LL * sms &&
-        ChunkSmem<1, 2, true>::bytes + 64 * pos_table_stride(static_cast<int>(cap)) <= kThreeCtaSmem)
-        return launch_bf16<1, 2, FUSED, true>(q, k_new, v_new, k_pool, v_pool, num_blocks,
-                                              block_size, bt, mbps, cs, u, vb, rel, R, out, B, T,
-                                              H, scale, stream, f + 4);
-    if (T <= 16 && cap <= 4096 &&
-        ChunkSmem<1, 4, true>::bytes + 64 * pos_table_stride(static_cast<int>(cap)) <= kTwoCtaSmem)
-        return launch_bf16<1, 4, FUSED, true>(q, k_new, v_new, k_pool, v_pool, num_blocks,
-                                              block_size, bt, mbps, cs, u, vb, rel, R, out, B, T,
-                                              H, scale, stream, f + 3);
+    const bool waves = sms > 0 && static_cast<long long>(B) * H > 2LL * sms;
+    if (T <= 16 && cap <= 4096) {
+        const int tb = 32 * pos_table_stride(static_cast<int>(cap));   // 16 rows of bf16
+        if (waves && ChunkSmem<1, 2, true>::bytes + tb <= kFourCtaSmem)
+            return launch_bf16<1, 2, FUSED, true>(q, k_new, v_new, k_pool, v_pool, num_blocks,
+                                                  block_size, bt, mbps, cs, u, vb, rel, R, out, B,
+                                                  T, H, scale, stream, f + 4);
+        if (waves && ChunkSmem<1, 5, true>::bytes + tb <= kTwoCtaSmem)
+            return launch_bf16<1, 5, FUSED, true>(q, k_new, v_new, k_pool, v_pool, num_blocks,
+                                                  block_size, bt, mbps, cs, u, vb, rel, R, out, B,
+                                                  T, H, scale, stream, f + 5);
+        if (ChunkSmem<1, 4, true>::bytes + tb <= kTwoCtaSmem)
+            return launch_bf16<1, 4, FUSED, true>(q, k_new, v_new, k_pool, v_pool, num_blocks,
+                                                  block_size, bt, mbps, cs, u, vb, rel, R, out, B,
+                                                  T, H, scale, stream, f + 3);
+    }
     if (T <= 16)
         return launch_bf16<1, 4, FUSED, false>(q, k_new, v_new, k_pool, v_pool, num_blocks,
                                                block_size, bt, mbps, cs, u, vb, rel, R, out, B, T,

@@ -190,3 +190,77 @@ def test_multiwave_short_histories(B, H, T, bs, cmax, seed, fused):
                                    x["v_new"][b:b + 1], x["pos_bias_u"], x["pos_bias_v"], x["rel"])
         check_close(got[b:b + 1], ref, "bf16", f"B{B} H{H} T{T} stream {b} (C={Cs[b]})")
     assert capi.oasr_device_status() == 0
+
+
+@pytest.mark.parametrize("B,H,T,bs,cmin,cmax,seed", [
+    (40, 8, 16, 16, 300, 530, 4),    # 320 CTAs: the persistent form, one to two items per CTA
+    (128, 8, 16, 32, 400, 512, 5),   # 1024 items over 304 CTAs: three to four items each
+    (64, 8, 1, 8, 250, 520, 6),      # single-frame chunks, 8-row pages
+    (96, 4, 11, 64, 330, 500, 7),    # ragged chunk, 64-row pages
+])
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
+def test_multiwave_long_histories(B, H, T, bs, cmin, cmax, seed, fused):
+    """Grids of several waves with long, unequal histories: the persistent form, whose producer
+    runs one (stream, head) item ahead of its consumers.  Every output row against the oracle,
+    both pools bit for bit against the oracle's append."""
+    rng = np.random.default_rng(60_000 + seed)
+    Cs = [int(c) for c in rng.integers(cmin, cmax + 1, size=B)]
+    x = _stream_inputs(rng, T, bs, H, B, Cs, "bf16", 0, 3)
+    d = {k: dev(x[k], "bf16") for k in ("q", "k_new", "v_new", "pos_bias_u", "pos_bias_v", "rel")}
+    kp, vp = dev_pool(x["k_pool"], "bf16"), dev_pool(x["v_pool"], "bf16")
+    bt = torch.from_numpy(x["block_table"]).cuda()
+    cs = torch.from_numpy(x["cache_seqlens"]).cuda()
+    if fused:
+        out = capi.oasr_chunk_step_paged(d["q"], d["k_new"], d["v_new"], kp, vp, bt, cs,
+                                         d["pos_bias_u"], d["pos_bias_v"], d["rel"])
+    else:
+        capi.oasr_paged_append(d["k_new"], d["v_new"], kp, vp, bt, cs)
+        out = capi.oasr_chunk_relattn_paged(d["q"], kp, vp, bt, cs, d["pos_bias_u"],
+                                            d["pos_bias_v"], d["rel"])
+    torch.cuda.synchronize()
+    got = to_np(out)
+    for b, (ck, cv) in enumerate(x["caches"]):
+        ref = oracle.chunk_relattn(x["q"][b:b + 1], ck, cv, x["k_new"][b:b + 1],
+                                   x["v_new"][b:b + 1], x["pos_bias_u"], x["pos_bias_v"], x["rel"])
+        check_close(got[b:b + 1], ref, "bf16", f"B{B} H{H} T{T} bs{bs} stream {b} (C={Cs[b]})")
+    kp_ref, vp_ref = x["k_pool"].copy(), x["v_pool"].copy()
+    assert oracle.paged_append(syn.to_bits(x["k_new"], "bf16"), syn.to_bits(x["v_new"], "bf16"),
+                               kp_ref, vp_ref, x["block_table"], x["cache_seqlens"]) == 0
+    assert np.array_equal(host_pool(kp, "bf16"), kp_ref)
+    assert np.array_equal(host_pool(vp, "bf16"), vp_ref)
+    assert capi.oasr_device_status() == 0
+
+
+def test_multiwave_invalid_chunk_page():
+    """In a persistent grid, streams whose chunk page names no valid block take the
+    write-fence-read path (their chunk keys on that page read as zeros and are flagged) while
+    the streams around them keep the direct path; every other row is exact."""
+    rng = np.random.default_rng(61_000)
+    B, H, T, bs = 40, 8, 16, 16
+    Cs = [int(c) for c in rng.integers(300, 531, size=B)]
+    x = _stream_inputs(rng, T, bs, H, B, Cs, "bf16", 0, 0)
+    bad = [3, 17, 38]
+    bt = x["block_table"].copy()
+    for b in bad:
+        bt[b, (Cs[b] + T - 1) // bs] = -7      # the page holding the chunk's last row
+    d = {k: dev(x[k], "bf16") for k in ("q", "k_new", "v_new", "pos_bias_u", "pos_bias_v", "rel")}
+    kp, vp = dev_pool(x["k_pool"], "bf16"), dev_pool(x["v_pool"], "bf16")
+    out = capi.oasr_chunk_step_paged(d["q"], d["k_new"], d["v_new"], kp, vp,
+                                     torch.from_numpy(bt).cuda(),
+                                     torch.from_numpy(x["cache_seqlens"]).cuda(),
+                                     d["pos_bias_u"], d["pos_bias_v"], d["rel"])
+    torch.cuda.synchronize()
+    got = to_np(out)
+    assert capi.oasr_device_status() & capi.STATUS_BOUNDS_BIT
+    for b, (ck, cv) in enumerate(x["caches"]):
+        kn, vn = x["k_new"][b:b + 1].copy(), x["v_new"][b:b + 1].copy()
+        if b in bad:
+            # keys on the invalid page read as zero rows
+            page = (Cs[b] + T - 1) // bs
+            for t in range(T):
+                if (Cs[b] + t) // bs == page:
+                    kn[0, t] = 0.0
+                    vn[0, t] = 0.0
+        ref = oracle.chunk_relattn(x["q"][b:b + 1], ck, cv, kn, vn, x["pos_bias_u"],
+                                   x["pos_bias_v"], x["rel"])
+        check_close(got[b:b + 1], ref, "bf16", f"stream {b} (C={Cs[b]}, bad={b in bad})")
