@@ -357,13 +357,13 @@ __device__ __forceinline__ void warp_slice16(WarpAcc& acc, const uint32_t (&qu)[
     softmax_pv16(acc, s, vf, mx0, mx1, kvalid, lane);
 }
 
-// Position table of one CTA (16 query rows of one head), built once before the key loop:
-// G[i][c] = bf16(q_i + v) . rel[rho0 + c] for c in [0, ncols), rel rows outside [0, R) taken
-// as zero, accumulated in fp32 and stored rounded to bf16 (a relative 2^-9 of the position
-// term, the order of the bf16 rounding of P; half the shared memory of fp32, which lets four
-// CTAs share an SM on short histories and five stages fit on long ones).  It is stored
-// pre-skewed, G[i][c] at gs[i*W + c + i + 1], so that query i and key j
-// (c = j + 15 - i) read gs[i*W + j + 16]: one row of a slice's scores is one contiguous run.
+// Position table of one CTA (Tp = 16 MT query rows of one head), built once before the key
+// loop: G[i][c] = bf16(q_i + v) . rel[rho0 + c] for c in [0, ncols), rel rows outside [0, R)
+// taken as zero, accumulated in fp32 and stored rounded to bf16 (a relative 2^-9 of the
+// position term, the order of the bf16 rounding of P; half the shared memory of fp32, which
+// lets four CTAs share an SM on short histories and five stages fit on long ones).  It is
+// stored pre-skewed, G[i][c] at gs[i*W + c + i + 1], so that query i and key j
+// (c = j + Tp - 1 - i) read gs[i*W + j + Tp]: one row of a slice's scores is one contiguous run.
 // Warp `warp` of `nw` computes column tiles warp, warp + nw, ...  The head dimension is
 // contracted in a permuted order: lane quad position t4 holds dims [16 t4, 16 t4 + 16) of
 // both operands, so a lane's B fragments for one rel row are two 16-byte loads (rel is read
@@ -371,7 +371,7 @@ __device__ __forceinline__ void warp_slice16(WarpAcc& acc, const uint32_t (&qu)[
 // The rel rows of the first BATCH tiles are requested by load() (once the caller has the
 // cache length), the rest by build() itself.  BATCH: column tiles of one warp whose rel
 // rows are in flight together (10; 5 for the lighter three-CTAs-per-SM kernel).
-template <int BATCH>
+template <int BATCH, int MT = 1>
 struct PosTable {
     const uint16_t* rel_h;   // rel + h * 64
     long long stride;        // elements between rel rows
@@ -395,15 +395,14 @@ struct PosTable {
         }
     }
 
-    // q_tile: the 128-byte-swizzled Q tile; v: the bias v in fp32 (smem).  load(warp) must
-    // have been called.
-    __device__ __forceinline__ void build(uint16_t* gs, int W, const uint8_t* q_tile, const float* v)
+    // A fragments of bf16(q + v) for m-tile mt (rows 16 mt ..), head dimension permuted
+    __device__ __forceinline__ void make_a(uint32_t (&qa)[4][4], const uint8_t* q_tile,
+                                           const float* v, int mt) const
     {
         const int g4 = lane >> 2, t4 = lane & 3;
-        uint32_t qa[4][4];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            const int row = g4 + 8 * half;
+            const int row = 16 * mt + g4 + 8 * half;
             const uint4 c0 = *reinterpret_cast<const uint4*>(q_tile + swz128(row, 2 * t4));
             const uint4 c1 = *reinterpret_cast<const uint4*>(q_tile + swz128(row, 2 * t4 + 1));
             const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
@@ -415,13 +414,25 @@ struct PosTable {
                     pack_bf16(bf16_lo(w[m]) + v[d], bf16_hi(w[m]) + v[d + 1]);
             }
         }
+    }
+
+    // q_tile: the 128-byte-swizzled Q tile; v: the bias v in fp32 (smem).  load(warp) must
+    // have been called.  Every m-tile's rows of a batch's columns use the batch's rel rows.
+    __device__ __forceinline__ void build(uint16_t* gs, int W, const uint8_t* q_tile, const float* v)
+    {
+        uint32_t qa[MT][4][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) make_a(qa[mt], q_tile, v, mt);
         for (int nb0 = warp;;) {
             // the batch's tiles as independent MMA chains (tiles past the table have zero rel
             // rows and store nothing); a short batch runs the half-size version
-            if (nb0 + (BATCH / 2) * nw < ntiles())
-                tiles<BATCH>(gs, W, qa, nb0);
-            else
-                tiles<BATCH / 2>(gs, W, qa, nb0);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                if (nb0 + (BATCH / 2) * nw < ntiles())
+                    tiles<BATCH>(gs, W, qa[mt], nb0, mt);
+                else
+                    tiles<BATCH / 2>(gs, W, qa[mt], nb0, mt);
+            }
             nb0 += BATCH * nw;
             if (nb0 >= ntiles()) break;
             load(nb0);
@@ -429,7 +440,8 @@ struct PosTable {
     }
 
     template <int N>
-    __device__ __forceinline__ void tiles(uint16_t* gs, int W, const uint32_t (&qa)[4][4], int nb0)
+    __device__ __forceinline__ void tiles(uint16_t* gs, int W, const uint32_t (&qa)[4][4], int nb0,
+                                          int mt)
     {
         const int g4 = lane >> 2, t4 = lane & 3;
         float c[N][4];
@@ -447,11 +459,12 @@ struct PosTable {
 #pragma unroll
         for (int u = 0; u < N; ++u) {
             const int col = 8 * (nb0 + u * nw) + 2 * t4;
+            const int i = 16 * mt + g4;   // query row of c[u][0..1]; c[u][2..3] is row i + 8
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 if (col + e < ncols) {
-                    gs[g4 * W + col + e + g4 + 1] = bf16_bits(c[u][e]);
-                    gs[(g4 + 8) * W + col + e + g4 + 9] = bf16_bits(c[u][2 + e]);
+                    gs[i * W + col + e + i + 1] = bf16_bits(c[u][e]);
+                    gs[(i + 8) * W + col + e + i + 9] = bf16_bits(c[u][2 + e]);
                 }
             }
         }

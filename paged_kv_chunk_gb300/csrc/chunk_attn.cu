@@ -70,14 +70,14 @@ constexpr int kMaxPages = 512;
 template <int MT, int NS, bool GT>
 struct ChunkSmem {
     using TL = Tile<MT>;
-    static_assert(!GT || MT == 1, "the position table serves one m-tile");
+    static_assert(!GT || MT <= 2, "the position table serves one or two m-tiles");
     static constexpr int kBand = GT ? 0 : TL::RB * kRowBytes;
     static constexpr int kSlot = 2 * kStageKeys * kRowBytes + kBand;
     static constexpr int off_slots = 0;
     static constexpr int off_q = NS * kSlot;
     static constexpr int off_ck = off_q + TL::Tp * kRowBytes;   // GT: the chunk's K|V rows
-    static constexpr int off_g = off_ck + (GT ? 2 * 16 * kRowBytes : 0);
-    static constexpr int off_u = off_g + (MT == 1 ? 0 : kConsumerWarps * kGBytes);
+    static constexpr int off_g = off_ck + (GT ? 2 * TL::Tp * kRowBytes : 0);
+    static constexpr int off_u = off_g + ((MT == 1 || GT) ? 0 : kConsumerWarps * kGBytes);
     static constexpr int off_vb = off_u + kHeadDim * 4;
     static constexpr int off_bt = off_vb + kHeadDim * 4;    // the stream's block-table row
     static constexpr int off_bar = off_bt + kMaxPages * 4;  // full[NS], empty[NS], q, written, chunk
@@ -159,8 +159,8 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
         if (lane == 0) {
             for (int i = 0; i < NS; ++i) {
                 mbar_init(bar_full + 8 * i, 1);
-                // one m-tile: all consumer warps read every stage (16-key slices)
-                mbar_init(bar_empty + 8 * i, MT == 1 ? kConsumerWarps : MT);
+                // one m-tile or the position table: all consumer warps read every stage
+                mbar_init(bar_empty + 8 * i, (MT == 1 || GT) ? kConsumerWarps : MT);
             }
             mbar_init(bar_q, 1);
             mbar_init(bar_written, 32 * kConsumerWarps);
@@ -172,10 +172,10 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
             mbar_arrive_expect_tx(bar_q, TL::Tp * kRowBytes);
             tma_load_3d(sb + SP::off_q, &tm_q, bar_q, 0, h, b * T);
             if (GT && FUSED) {
-                // nor do the chunk's rows (T <= 16: one 16-row box each for K and V)
-                mbar_arrive_expect_tx(bar_chunk, 2 * 16 * kRowBytes);
+                // nor do the chunk's rows (T <= Tp: one Tp-row box each for K and V)
+                mbar_arrive_expect_tx(bar_chunk, 2 * TL::Tp * kRowBytes);
                 tma_load_3d(sb + SP::off_ck, &tm_kn, bar_chunk, 0, h, b * T);
-                tma_load_3d(sb + SP::off_ck + 16 * kRowBytes, &tm_vn, bar_chunk, 0, h, b * T);
+                tma_load_3d(sb + SP::off_ck + TL::Tp * kRowBytes, &tm_vn, bar_chunk, 0, h, b * T);
             }
         }
 #pragma unroll
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
                     const int p = C + t;
                     const int lb = p / a.block_size;
                     const uint4 val = *reinterpret_cast<const uint4*>(
-                        sm + SP::off_ck + kv * 16 * kRowBytes + swz128(t, c));
+                        sm + SP::off_ck + kv * TL::Tp * kRowBytes + swz128(t, c));
                     *reinterpret_cast<uint4*>(
                         (kv ? a.v_pool : a.k_pool) +
                         ((static_cast<long long>(s_bt[lb]) * a.block_size + (p - lb * a.block_size)) *
@@ -347,12 +347,12 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
         mbar_arrive(bar_written);
     };
     if constexpr (GT) {
-        PosTable<NS == 2 ? 5 : 10> pt;
+        PosTable<NS == 2 ? 5 : 10, MT> pt;
         pt.rel_h = a.rel + h * kHeadDim;
         pt.stride = static_cast<long long>(a.H) * kHeadDim;
         pt.R = a.R;
-        pt.rho0 = off - 15;
-        pt.ncols = K + 15;
+        pt.rho0 = off - (TL::Tp - 1);
+        pt.ncols = K + TL::Tp - 1;
         pt.warp = warp;
         pt.nw = kConsumerWarps;
         pt.lane = lane;
@@ -378,23 +378,36 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
         float* gw = reinterpret_cast<float*>(sm + SP::off_g) + warp * (kGBytes / 4);
         if constexpr (GT) {
             const uint16_t* gs = reinterpret_cast<const uint16_t*>(sm + SP::off_gt);
+            // warp w: m-tile w % MT (its 16 query rows of the table at gm) and, of every stage,
+            // the MT 16-key slices from key 16 MT (w / MT); query i, key j read table position
+            // j + Tp
+            const int kh = warp / MT;
+            const uint16_t* gm = gs + 16 * mt * a.gt_w;
             if (FUSED && direct) {
-                // the chunk, landed long before the first pool stage: its keys are warp 0's
-                // first slice (the producer warp writes its rows into the pool)
-                if (warp == 0)
-                    warp_slice16_gt(acc, qu, sb + SP::off_ck, sb + SP::off_ck + 16 * kRowBytes,
-                                    gs + C + 16, a.gt_w, ((C + 16) & 1) == 0, T, a.scale_log2, lane);
+                // the chunk, landed long before the first pool stage: its 16-key slice kh (the
+                // producer warp writes its rows into the pool)
+                const int kvc = T - 16 * kh;
+                if (kvc > 0) {
+                    const int x0 = C + 16 * kh + TL::Tp;
+                    warp_slice16_gt(acc, qu, sb + SP::off_ck + 16 * kh * kRowBytes,
+                                    sb + SP::off_ck + (TL::Tp + 16 * kh) * kRowBytes, gm + x0,
+                                    a.gt_w, (x0 & 1) == 0, kvc, a.scale_log2, lane);
+                }
             }
             for (int s = 0; s < n_stages; ++s) {
                 const int slot = s % NS;
                 if (!mbar_wait(bar_full + 8 * slot, (s / NS) & 1)) { failed = true; break; }
                 const uint32_t base = sb + SP::off_slots + slot * SP::kSlot;
-                const int kv = stage_valid(s) - 16 * warp;
-                if (kv > 0) {
-                    const int x0 = stage_j0(s) + 16 * warp + 16;   // table column of the slice
-                    warp_slice16_gt(acc, qu, base + 16 * warp * kRowBytes,
-                                    base + (kStageKeys + 16 * warp) * kRowBytes, gs + x0, a.gt_w,
-                                    (x0 & 1) == 0, kv, a.scale_log2, lane);
+#pragma unroll
+                for (int u = 0; u < MT; ++u) {
+                    const int jl = 16 * (MT * kh + u);   // the slice's first key in the stage
+                    const int kv = stage_valid(s) - jl;
+                    if (kv > 0) {
+                        const int x0 = stage_j0(s) + jl + TL::Tp;   // table position of the slice
+                        warp_slice16_gt(acc, qu, base + jl * kRowBytes,
+                                        base + (kStageKeys + jl) * kRowBytes, gm + x0, a.gt_w,
+                                        (x0 & 1) == 0, kv, a.scale_log2, lane);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
@@ -579,10 +592,16 @@ int g_smem_done[16][64];
 constexpr int kTwoCtaSmem = 112 * 1024;
 constexpr int kFourCtaSmem = 56 * 1024;
 
-// Row stride (bf16 elements) of the position table for keys up to `cap`: every read and write
-// stays below cap + 32, and a stride of 16 mod 64 elements (8 mod 32 words) keeps the 4-byte
-// reads of a slice conflict-free.
-inline int pos_table_stride(int cap) { return ((cap + 32 + 63) & ~63) + 16; }
+// Row stride (bf16 elements) of the position table of Tp query rows for keys up to `cap`:
+// every read and write stays below cap + 2 Tp, and a stride of 16 mod 64 elements (8 mod 32
+// words) keeps the 4-byte reads of a slice conflict-free.
+inline int pos_table_stride(int cap, int Tp = 16) { return ((cap + 2 * Tp + 63) & ~63) + 16; }
+
+// Shared memory of the position table of Tp query rows (bf16).
+inline int pos_table_bytes(long long cap, int Tp)
+{
+    return Tp * pos_table_stride(static_cast<int>(cap), Tp) * 2;
+}
 
 // Keys a stream of a call may have, as the host knows them: the table's pages, and the
 // R - T + 1 keys a rel table of R rows serves (R >= C + 2T - 1 is required).
@@ -612,9 +631,11 @@ oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, voi
     else if (!encode_rows_bf16(&tm_r, rel, R, H, Tile<MT>::RB))
         return OASR_ERR_INVALID_ARG;
     if (FUSED) {
-        // the chunk's rows as TMA sources for the direct chunk stage
-        if (!encode_rows_bf16(&tm_kn, k_new, static_cast<long long>(B) * T, H, 16) ||
-            !encode_rows_bf16(&tm_vn, v_new, static_cast<long long>(B) * T, H, 16))
+        // the chunk's rows as TMA sources for the direct chunk stage (16-row boxes) or the
+        // position-table kernel's chunk region (Tp rows)
+        const int cbox = GT ? Tile<MT>::Tp : 16;
+        if (!encode_rows_bf16(&tm_kn, k_new, static_cast<long long>(B) * T, H, cbox) ||
+            !encode_rows_bf16(&tm_vn, v_new, static_cast<long long>(B) * T, H, cbox))
             return OASR_ERR_INVALID_ARG;
     } else {
         tm_kn = tm_k;
@@ -626,8 +647,8 @@ oasr_status launch_bf16(const void* q, const void* k_new, const void* v_new, voi
     // the keys the host can bound (the position table is sized for them); a stream with more
     // (a rel table shorter than the precondition allows) is clamped to them and flagged
     const int k_max = key_bound(mbps, block_size, R, T);
-    const int gt_w = GT ? pos_table_stride(k_max) : 0;
-    const int smem = ChunkSmem<MT, NS, GT>::bytes + 16 * gt_w * 2;
+    const int gt_w = GT ? pos_table_stride(k_max, Tile<MT>::Tp) : 0;
+    const int smem = ChunkSmem<MT, NS, GT>::bytes + Tile<MT>::Tp * gt_w * 2;
     if (!ensure_smem(kern, smem, g_smem_done[slot])) return OASR_ERR_CUDA;
     ChunkArgs a;
     a.k_new = static_cast<const uint16_t*>(k_new);
@@ -703,7 +724,7 @@ oasr_status dispatch(const void* q, const void* k_new, const void* v_new, void* 
     const int sms = sm_count();
     const bool waves = sms > 0 && static_cast<long long>(B) * H > 2LL * sms;
     if (T <= 16 && cap <= 4096) {
-        const int tb = 32 * pos_table_stride(static_cast<int>(cap));   // 16 rows of bf16
+        const int tb = pos_table_bytes(cap, 16);
         if (waves && ChunkSmem<1, 2, true>::bytes + tb <= kFourCtaSmem)
             return launch_bf16<1, 2, FUSED, true>(q, k_new, v_new, k_pool, v_pool, num_blocks,
                                                   block_size, bt, mbps, cs, u, vb, rel, R, out, B,
@@ -717,6 +738,12 @@ oasr_status dispatch(const void* q, const void* k_new, const void* v_new, void* 
                                                   block_size, bt, mbps, cs, u, vb, rel, R, out, B,
                                                   T, H, scale, stream, f + 3);
     }
+    // T = 17 .. 32: the position table of two m-tiles when it fits beside three stages
+    if (T > 16 && T <= 32 && cap <= 4096 &&
+        ChunkSmem<2, 3, true>::bytes + pos_table_bytes(cap, 32) <= kTwoCtaSmem)
+        return launch_bf16<2, 3, FUSED, true>(q, k_new, v_new, k_pool, v_pool, num_blocks,
+                                              block_size, bt, mbps, cs, u, vb, rel, R, out, B, T,
+                                              H, scale, stream, f + 6);
     if (T <= 16)
         return launch_bf16<1, 4, FUSED, false>(q, k_new, v_new, k_pool, v_pool, num_blocks,
                                                block_size, bt, mbps, cs, u, vb, rel, R, out, B, T,

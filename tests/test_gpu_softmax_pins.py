@@ -335,8 +335,9 @@ def test_one_hot_rel_rows_match_fixture():
 
 
 @pytest.mark.parametrize("T,C,bs", [(1, 0, 16), (1, 300, 16), (1, 530, 16), (16, 0, 16),
-                                    (16, 300, 16), (16, 530, 16), (64, 0, 16), (64, 300, 32),
-                                    (64, 530, 16)], ids=str)
+                                    (16, 300, 16), (16, 530, 16), (32, 0, 16), (32, 500, 16),
+                                    (24, 301, 8), (64, 0, 16), (64, 300, 32), (64, 530, 16)],
+                         ids=str)
 def test_one_hot_rel_rows_streaming(T, C, bs):
     """Every (query, key) pair reads exactly one table row, the one the oracle reads."""
     got_map, ref_map = _probe_streaming(T, C, bs, fused=(T + C) % 2 == 0)
