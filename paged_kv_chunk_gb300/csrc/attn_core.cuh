@@ -475,10 +475,13 @@ struct PosTable {
 // gq points at gs + js + 16 for the slice's first key js, so key jl of query row i uses
 // gq[i*W + jl].  k_s, v_s: the slice's 16 K and V rows (128-byte swizzled); keys
 // [0, kvalid) of the slice exist.
+// release_bar (non-zero): an mbarrier every lane arrives on as soon as its last read of the
+// slice's K and V rows is done (the V fragments are in registers), so the slot can be refilled
+// while the position term, softmax and P.V run.
 __device__ __forceinline__ void warp_slice16_gt(WarpAcc& acc, const uint32_t (&qu)[4][4],
                                                 uint32_t k_s, uint32_t v_s, const uint16_t* gq,
                                                 int W, bool even, int kvalid, float scale_log2,
-                                                int lane)
+                                                int lane, uint32_t release_bar = 0)
 {
     const int g4 = lane >> 2, t4 = lane & 3, mi = lane >> 3;
     float gb[2][4];   // [nt][row g4 cols 2t4, 2t4+1 | row g4+8 cols 2t4, 2t4+1]
@@ -519,6 +522,7 @@ __device__ __forceinline__ void warp_slice16_gt(WarpAcc& acc, const uint32_t (&q
 #pragma unroll
     for (int dp = 0; dp < 4; ++dp)
         ldsm_x4_t(v_s + swz128(vrow, 2 * dp + (mi >> 1)), vf[dp][0], vf[dp][1], vf[dp][2], vf[dp][3]);
+    if (release_bar) mbar_arrive_release(release_bar);
     float mx0 = acc.m[0], mx1 = acc.m[1];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {

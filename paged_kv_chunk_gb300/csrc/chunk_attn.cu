@@ -159,8 +159,10 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
         if (lane == 0) {
             for (int i = 0; i < NS; ++i) {
                 mbar_init(bar_full + 8 * i, 1);
-                // one m-tile or the position table: all consumer warps read every stage
-                mbar_init(bar_empty + 8 * i, (MT == 1 || GT) ? kConsumerWarps : MT);
+                // one m-tile or the position table: all consumer warps read every stage (with
+                // the table and one m-tile every lane arrives, as soon as its reads are done)
+                mbar_init(bar_empty + 8 * i, (GT && MT == 1) ? 32 * kConsumerWarps
+                                             : (MT == 1 || GT) ? kConsumerWarps : MT);
             }
             mbar_init(bar_q, 1);
             mbar_init(bar_written, 32 * kConsumerWarps);
@@ -398,6 +400,10 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
                 const int slot = s % NS;
                 if (!mbar_wait(bar_full + 8 * slot, (s / NS) & 1)) { failed = true; break; }
                 const uint32_t base = sb + SP::off_slots + slot * SP::kSlot;
+                // one m-tile: every lane releases the slot as soon as its slice's K and V rows
+                // are read (before the position term, softmax and P.V), so the producer can
+                // refill it earlier; two m-tiles: lane 0 after both slices
+                const uint32_t rel_bar = MT == 1 ? bar_empty + 8 * slot : 0u;
 #pragma unroll
                 for (int u = 0; u < MT; ++u) {
                     const int jl = 16 * (MT * kh + u);   // the slice's first key in the stage
@@ -406,11 +412,15 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
                         const int x0 = stage_j0(s) + jl + TL::Tp;   // table position of the slice
                         warp_slice16_gt(acc, qu, base + jl * kRowBytes,
                                         base + (kStageKeys + jl) * kRowBytes, gm + x0, a.gt_w,
-                                        (x0 & 1) == 0, kv, a.scale_log2, lane);
+                                        (x0 & 1) == 0, kv, a.scale_log2, lane, rel_bar);
+                    } else if (MT == 1) {
+                        mbar_arrive_release(rel_bar);
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+                if (MT != 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+                }
             }
         } else if constexpr (MT == 1) {
             // every stage: this warp's 16-key slice; its skew scratch overlays its K rows

@@ -71,6 +71,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Arrive on an mbarrier with release semantics: this thread's earlier shared-memory reads (for
+// example the fragment loads of a ring slot) are ordered before the arrival, so a copy that
+// waits on the barrier cannot overwrite what they read.
+__device__ __forceinline__ void mbar_arrive_release(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t done;
