@@ -19,8 +19,9 @@
 //   warps 0-7  softmax.  Warps w and w+4 share TMEM lane quadrant w and the 32 query rows in
 //              it; warp w takes keys 0-63 of each stage, warp w+4 keys 64-127, and the pair
 //              swaps row maxima and sums through shared memory.  Each thread loads its S half
-//              row and, through a shared staging tile, its skewed half row of G; masks keys
-//              past the segment; keeps the running max (O is rescaled in TMEM only when the
+//              row and the G columns its row reaches, releases S and G to the issuer, then
+//              takes its skewed half row of G (rounded to bf16) through a shared staging tile;
+//              masks keys past the segment; keeps the running max (O is rescaled in TMEM only when the
 //              max grows by more than 2^8) and sum; writes its half row of bf16 P to TMEM; at
 //              the end of the tile normalises and stores its half of the O row.
 //   warp 8     MMA issuer (one thread): S and G of stage s+1 as soon as the softmax warps have
@@ -46,9 +47,8 @@ constexpr int kBN = 128;                 // keys per stage
 constexpr int kBand = 256;               // band rows per stage
 constexpr int kTmemCols = 512;
 constexpr int kColS = 0, kColG = 128, kColO = 384, kColP = 448;
-constexpr int kStgW = 68;                // staging row stride (floats): conflict-free both ways
-constexpr int kStgWarpBytes = 32 * kStgW * 4;
-constexpr int kStgOverlay = 5;           // warps whose staging overlays the stage's K and band tiles
+constexpr int kStgWarpBytes = 6400;     // one warp's bf16 staging: 32 rows of 48 words, padded
+constexpr int kStgOverlay = 7;           // warps whose staging overlays the stage's K and band tiles
 constexpr int kUvHeads = 32;             // pos_bias_u / v of up to this many heads live in smem
 
 struct TcSmem {
@@ -499,61 +499,64 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 }
                 const bool live = !MASKED || __any_sync(0xffffffffu, ka < kb && ka < 64 && kb > 0);
                 float sc[64];
+                // position term, skewed: row r needs G[r][127 - r + j].  This warp's rows reach
+                // 95 columns of G for this half (row r, key j of the half: window column
+                // 31 - lane + j), which go through shared memory as bf16 pairs (the stage's K and
+                // band tiles, free once S and G are computed, for the first warps).  Row bases of
+                // 48 * lane + 4 * (lane >> 1) words keep both the 16-byte stores and the
+                // lane-shifted 4-byte loads free of bank conflicts.  Lane reads words w0 .. w0+32
+                // (w0 = (31 - lane) / 2); an even lane's window starts on the odd half of word
+                // w0, so its pairs are realigned with a byte permute.
+                uint32_t* stg = reinterpret_cast<uint32_t*>(
+                                    warp < kStgOverlay ? slot_p + warp * kStgWarpBytes
+                                                       : sm + SP::off_stg + (warp - kStgOverlay) * kStgWarpBytes) +
+                                (48 * lane + 4 * (lane >> 1));
+                const int w0 = (31 - lane) >> 1;
                 if (live) {
-                    uint32_t sr[64], rr[32];
+                    uint32_t gr[96];
                     const uint32_t colg = kColG + static_cast<uint32_t>(96 - 32 * quad + 64 * hf);
+                    OASR_TMEM_LD32(tl + colg, gr);
+                    OASR_TMEM_LD32(tl + colg + 32, (gr + 32));
+                    OASR_TMEM_LD32(tl + colg + 64, (gr + 64));
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int pc = 0; pc < 12; ++pc)
+                        if (4 * pc + 3 >= w0 && 4 * pc <= w0 + 32) {
+                            uint32_t gw[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                gw[e] = pack_bf16(__uint_as_float(gr[8 * pc + 2 * e]),
+                                                  __uint_as_float(gr[8 * pc + 2 * e + 1]));
+                            *reinterpret_cast<uint4*>(stg + 4 * pc) = make_uint4(gw[0], gw[1], gw[2], gw[3]);
+                        }
+                    uint32_t sr[64];
                     OASR_TMEM_LD32(tl + kColS + 64 * hf, sr);
                     OASR_TMEM_LD32(tl + kColS + 64 * hf + 32, (sr + 32));
-                    OASR_TMEM_LD32(tl + colg, rr);
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 64; ++j) sc[j] = __uint_as_float(sr[j]);
-                    // position term, skewed: row r needs G[r][127 - r + j].  Per 32-key chunk a
-                    // warp's rows span 63 columns, staged through shared memory (the stage's K
-                    // and band tiles, free once S and G are computed, for the first warps).
-                    float* stg = reinterpret_cast<float*>(
-                        (warp < kStgOverlay ? slot_p + warp * (32 * kStgW * 4)
-                                            : sm + SP::off_stg + (warp - kStgOverlay) * (32 * kStgW * 4)) +
-                        lane * (kStgW * 4));
-                    // chunk c (keys 32c..32c+31 of this half) reads G columns
-                    // colg + 32c ... colg + 32c + 63, staged as two 32-column blocks
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        // for c = 1, rr still holds block 1 (loaded for chunk 0's upper half);
-                        // the unmasked kernel reloads it rather than keep it live across chunk
-                        // 0's reads (measured faster there, slower in the masked one)
-                        if (c == 1 && !MASKED) {
-                            OASR_TMEM_LD32(tl + colg + 32, rr);
-                            tmem_wait_ld();
-                        }
-                        // only the 16-byte pieces this row reads (columns 31 - lane .. 62 - lane):
-                        // lanes that skip a piece move no data, so about half the store traffic goes
-#pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            if (4 * k + 3 >= 31 - lane)
-                                *reinterpret_cast<uint4*>(stg + 4 * k) =
-                                    make_uint4(rr[4 * k], rr[4 * k + 1], rr[4 * k + 2], rr[4 * k + 3]);
-                        OASR_TMEM_LD32(tl + colg + 32 * c + 32, rr);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            if (32 + 4 * k <= 62 - lane)
-                                *reinterpret_cast<uint4*>(stg + 32 + 4 * k) =
-                                    make_uint4(rr[4 * k], rr[4 * k + 1], rr[4 * k + 2], rr[4 * k + 3]);
-                        __syncwarp();
-#pragma unroll
-                        for (int j = 0; j < 32; j += 2) {   // two scores per packed add
-                            const float2 r2 = __fadd2_rn(make_float2(sc[32 * c + j], sc[32 * c + j + 1]),
-                                                         make_float2(stg[31 - lane + j], stg[32 - lane + j]));
-                            sc[32 * c + j] = r2.x;
-                            sc[32 * c + j + 1] = r2.y;
-                        }
-                        __syncwarp();
-                    }
                 }
+                // S and G are read: the issuer may compute the next stage's into the same
+                // columns while this warp adds the position term and exponentiates
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_sg_free);
+                if (live) {
+                    const uint32_t sel = (lane & 1) ? 0x3210u : 0x5432u;
+                    const uint32_t* rd = stg + w0;
+                    uint32_t wa = rd[0];
+#pragma unroll
+                    for (int m = 0; m < 32; ++m) {
+                        const uint32_t wb = rd[m + 1];
+                        const uint32_t g2 = __byte_perm(wa, wb, sel);
+                        const float2 r2 = __fadd2_rn(make_float2(sc[2 * m], sc[2 * m + 1]),
+                                                     make_float2(__uint_as_float(g2 << 16),
+                                                                 __uint_as_float(g2 & 0xffff0000u)));
+                        sc[2 * m] = r2.x;
+                        sc[2 * m + 1] = r2.y;
+                        wa = wb;
+                    }
+                }
                 // last stage of the item: the next item's Qu/Qv, so that its first S/G can be
                 // issued while this stage's softmax and the epilogue run
                 if (s + 1 == n_st && item + gridDim.x < n_items) {

@@ -49,8 +49,8 @@ SAMPLED = [syn.LARGE] + list(syn.SWEEP)
 # ------------------------------------------------------------------------- append
 
 
-@pytest.mark.parametrize("cfg", [syn.TINY, syn.SMALL, syn.LARGE, syn.SWEEP[0], syn.SWEEP[-1]],
-                         ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [syn.TINY, syn.SMALL, syn.LARGE, syn.WINDOW_RING, syn.HETERO]
+                         + list(syn.SWEEP), ids=lambda c: c.name)
 def test_append_bit_exact(cfg):
     x = stream_case(cfg)
     d = gpu_stream_inputs(x, cfg.dtype)
@@ -117,8 +117,12 @@ def test_chunk_attention_sampled_full_size(cfg):
     assert capi.oasr_device_status() == 0
 
 
-def test_fused_step_writes_the_same_pool():
-    cfg = syn.SMALL
+@pytest.mark.parametrize("cfg", [syn.SMALL, syn.LARGE, syn.HETERO] + list(syn.SWEEP),
+                         ids=lambda c: c.name)
+def test_fused_step_writes_the_same_pool(cfg):
+    """The fused step's append (which may read the chunk into its own stage and write the
+    pool from there) leaves the pools bit-identical to the stand-alone append, at every
+    chunk size the dispatch routes to a different kernel form."""
     x = stream_case(cfg)
     _, d1 = _run_step(cfg, x, fused=True)
     _, d2 = _run_step(cfg, x, fused=False)
