@@ -21,12 +21,15 @@
 //              swaps row maxima and sums through shared memory.  Each thread loads its S half
 //              row and the G columns its row reaches, releases S and G to the issuer, then
 //              takes its skewed half row of G (rounded to bf16) through a shared staging tile;
-//              masks keys past the segment; keeps the running max (O is rescaled in TMEM only when the
-//              max grows by more than 2^8) and sum; writes its half row of bf16 P to TMEM; at
+//              masks keys past the segment; keeps the running max (O is rescaled in TMEM only
+//              when the max grows by more than 2^8) and sum; writes its half row of bf16 P to TMEM; at
 //              the end of the tile normalises and stores its half of the O row.
 //   warp 8     MMA issuer (one thread): S and G of stage s+1 as soon as the softmax warps have
 //              read stage s's, then P.V of stage s.
-//   warp 9     TMA producer: K, band and V tiles into a two-slot ring.
+//   warp 9     TMA producer: q rows, and K, band and V tiles into a two-slot ring.  A slot's
+//              K and band are refilled as soon as the softmax warps are done with that region
+//              (they stage G there), its V once the slot's last P.V has finished; S and G of a
+//              stage wait for K and band alone.
 // Every wait is bounded; a wait that runs out raises the timeout bit and aborts the CTA's
 // remaining work, after which the CTA still drains its copies and tensor-core work and frees
 // its TMEM.
@@ -70,7 +73,7 @@ struct TcSmem {
     static constexpr int off_uv = (off_tile + (kTcMaxSeqs + 1) * 4 + 15) & ~15;   // u | v, bf16
     static constexpr int off_misc = off_uv + 2 * kUvHeads * kRowBytes;   // wsum[16], tmem, abort
     static constexpr int off_bar = (off_misc + 128 + 7) & ~7;
-    static constexpr int n_bars = 2 + 2 + 7 + 4 + 2;
+    static constexpr int n_bars = 2 + 2 + 7 + 4 + 2 + 2 + 2;
     static constexpr int bytes = off_bar + n_bars * 8 + 1024;
     static_assert(bytes <= 232448, "dynamic shared memory of one CTA");
 };
@@ -108,8 +111,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
     int* s_wsum = reinterpret_cast<int*>(sm + SP::off_misc);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + SP::off_misc + 64);
     volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SP::off_misc + 68);
-    const uint32_t bar_full = sb + SP::off_bar;        // [2] TMA stage landed
-    const uint32_t bar_empty = bar_full + 16;          // [2] stage slot free (after P.V)
+    const uint32_t bar_full = sb + SP::off_bar;        // [2] the stage's K and band tiles landed
+    const uint32_t bar_empty = bar_full + 16;          // [2] the slot's V tile free (after P.V)
     const uint32_t bar_sg_full = bar_empty + 16;       // S and G in TMEM
     const uint32_t bar_sg_free = bar_sg_full + 8;      // softmax warps have read S and G
     const uint32_t bar_p_full = bar_sg_free + 8;       // P written to TMEM
@@ -120,6 +123,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
     const uint32_t bar_pair = bar_drain + 8;           // [4] softmax warp pair exchanged a value
     const uint32_t bar_qb_full = bar_pair + 32;        // q rows of the next item landed
     const uint32_t bar_qb_free = bar_qb_full + 8;      // softmax warps have read the q rows
+    const uint32_t bar_kb_empty = bar_qb_free + 8;     // [2] the slot's K and band region free
+    const uint32_t bar_v_full = bar_kb_empty + 16;     // [2] the stage's V tile landed
     const int ns = a.num_seqs;
 
     if (tid == 0) {
@@ -137,6 +142,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
         for (int i = 0; i < 4; ++i) mbar_init(bar_pair + 8 * i, 64);
         mbar_init(bar_qb_full, 1);
         mbar_init(bar_qb_free, kSoftmaxWarps);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_kb_empty + 8 * i, kSoftmaxWarps);
+            mbar_init(bar_v_full + 8 * i, 1);
+        }
         fence_mbar_init();
         *s_abort = 0;
     }
@@ -237,6 +246,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
         }
     };
 
+    // The TMA producer polls with a pause between tries, so that its warp takes few issue
+    // slots from the softmax warps sharing its scheduler.
+    auto prod_wait = [&](uint32_t bar, uint32_t parity, volatile int* abort) {
+        if (mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = global_timer_ns();
+        for (;;) {
+            __nanosleep(128);
+            if (mbar_try_wait(bar, parity)) return true;
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) { *abort = 1; return false; }
+        }
+    };
     // Softmax warps take every wait together: a warp-wide vote keeps the warp converged for
     // the .sync.aligned tensor-memory instructions even if one lane's wait runs out.
     auto warp_wait = [&](uint32_t bar, uint32_t parity) {
@@ -259,30 +280,41 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 decode(item, seg, start, L, i0, h, kl, kh);
                 const int n_st = (kh - kl + kBN - 1) / kBN;
                 // the item's 128 q rows, once the softmax warps have read the previous ones
-                if (itp > 0 && !wait_or_abort(bar_qb_free, (itp - 1) & 1, s_abort)) {
+                if (itp > 0 && !prod_wait(bar_qb_free, (itp - 1) & 1, s_abort)) {
                     ok = false;
                     break;
                 }
                 mbar_arrive_expect_tx(bar_qb_full, kBM * kRowBytes);
                 tma_load_3d(sb + SP::off_qbuf, &tm_q, bar_qb_full, 0, h, start + i0);
                 for (int s = 0; s < n_st; ++s, ++g) {
+                    // K and band as soon as the softmax warps are done with the slot's K and band
+                    // region (its S and G computed, their staging reads finished), V once the
+                    // slot's last P.V has finished
                     const int slot = g & 1;
-                    if (g >= 2 && !wait_or_abort(bar_empty + 8 * slot, ((g >> 1) - 1) & 1, s_abort)) {
+                    const uint32_t ph = ((g >> 1) - 1) & 1;
+                    if (g >= 2 && !prod_wait(bar_kb_empty + 8 * slot, ph, s_abort)) {
                         ok = false;
                         break;
                     }
                     const uint32_t base = sb + SP::off_slot + slot * SP::slot;
                     const uint32_t bar = bar_full + 8 * slot;
-                    mbar_arrive_expect_tx(bar, SP::slot);
+                    mbar_arrive_expect_tx(bar, SP::k_tile + SP::band_tile);
                     const int js = kl + s * kBN;   // first key of the stage
                     tma_load_3d_hint(base, &tm_k, bar, 0, h, start + js, pol);
                     tma_load_3d(base + SP::off_band, &tm_r, bar, 0, h, a.z - i0 + js - (kBM - 1));
-                    tma_load_3d_hint(base + SP::off_v, &tm_v, bar, 0, h, start + js, pol);
+                    if (g >= 2 && !prod_wait(bar_empty + 8 * slot, ph, s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar_v_full + 8 * slot, SP::v_tile);
+                    tma_load_3d_hint(base + SP::off_v, &tm_v, bar_v_full + 8 * slot, 0, h, start + js, pol);
                 }
             }
             // no copy may still be landing when the CTA exits
             for (int u = g - 2; u < g; ++u)
-                if (u >= 0 && !mbar_wait(bar_full + 8 * (u & 1), (u >> 1) & 1)) *s_abort = 1;
+                if (u >= 0 && !(mbar_wait(bar_full + 8 * (u & 1), (u >> 1) & 1) &&
+                                mbar_wait(bar_v_full + 8 * (u & 1), (u >> 1) & 1)))
+                    *s_abort = 1;
             if (itp > 0 && !mbar_wait(bar_qb_full, (itp - 1) & 1)) *s_abort = 1;
         }
     } else if (warp == kMmaWarp) {
@@ -342,7 +374,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     if (next_s + 1 == next_n) { umma_commit(bar_q_free); ++nq; }
                 }
                 // P.V of stage g
-                ok = wait_or_abort(bar_p_full, g & 1, s_abort);
+                ok = wait_or_abort(bar_p_full, g & 1, s_abort) &&
+                     wait_or_abort(bar_v_full + 8 * (g & 1), (g >> 1) & 1, s_abort);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t vbase = sb + SP::off_slot + (g & 1) * SP::slot + SP::off_v;
@@ -557,6 +590,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                         wa = wb;
                     }
                 }
+                // the slot's K and band region (staging included) is no longer read: the producer
+                // may refill it with the stage after next's K and band
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_kb_empty + 8 * (g & 1));
                 // last stage of the item: the next item's Qu/Qv, so that its first S/G can be
                 // issued while this stage's softmax and the epilogue run
                 if (s + 1 == n_st && item + gridDim.x < n_items) {
@@ -646,7 +683,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 const int kstage = kh - (kl + s * kBN);   // keys of this stage that exist
                 const int k16 = (kstage + 15) & ~15;
                 if (kstage < k16 && 32 * quad < k16 && 32 * quad + 32 > kstage) {
-                    if (!warp_wait(bar_full + 8 * (g & 1), (g >> 1) & 1)) { ok = false; break; }
+                    if (!warp_wait(bar_v_full + 8 * (g & 1), (g >> 1) & 1)) { ok = false; break; }
                     if (r >= kstage && r < k16) {
                         uint4* vrow = reinterpret_cast<uint4*>(slot_p + SP::off_v + r * kRowBytes) + 4 * hf;
 #pragma unroll
