@@ -50,7 +50,7 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0   # the ~8 TB/s the streaming step's HBM target is stated against
 KERNEL_SOURCES = ["chunk_attn.cu", "attn_core.cuh", "ptx.cuh"]
-PACKED_SOURCES = ["packed_tc.cu", "attn_core.cuh", "ptx.cuh"]
+PACKED_SOURCES = ["packed_tc.cu", "tcgen05.cuh", "attn_core.cuh", "ptx.cuh"]
 
 
 def parse_args():

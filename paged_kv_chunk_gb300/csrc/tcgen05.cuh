@@ -3,7 +3,8 @@
 // Shared-memory matrix descriptors for 128-byte-swizzled tiles, the kind::f16 instruction
 // descriptor (bf16 A and B, fp32 accumulator), the MMA itself with A in shared memory or in
 // tensor memory, commits to an mbarrier, TMEM loads/stores of 32 lanes x 32 columns, and a
-// bounded mbarrier wait that also gives up when another role of the CTA has aborted.
+// bounded mbarrier wait that sleeps on the barrier and also gives up when another role of the
+// CTA has aborted.
 #pragma once
 
 #include "ptx.cuh"
@@ -85,14 +86,29 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// As mbar_try_wait, but the thread may be suspended until the phase completes or hint_ns
+// nanoseconds pass, so that a waiting warp takes no issue slots meanwhile.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
 // Bounded wait that also gives up as soon as another role has aborted the CTA.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-        for (int k = 0; k < 32; ++k)
-            if (mbar_try_wait(bar, parity)) return true;
+        // suspended until the phase completes, for 20 us at most between the checks below
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*abort) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             *abort = 1;
