@@ -15,21 +15,24 @@
 //   O [128 x 64] += P . V               columns [384,448)  M128 N64, A = P from TMEM, B = V
 //                                                          as an MN-major smem operand
 //   P [128 x 128] bf16                  columns [448,512)
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warps 0-7  softmax.  Warps w and w+4 share TMEM lane quadrant w and the 32 query rows in
 //              it; warp w takes keys 0-63 of each stage, warp w+4 keys 64-127, and the pair
 //              swaps row maxima and sums through shared memory.  Each thread loads its S half
 //              row and the G columns its row reaches, releases S and G to the issuer, then
-//              takes its skewed half row of G (rounded to bf16) through a shared staging tile;
+//              takes its skewed half row of G (rounded to bf16) through its own shared staging
+//              tile;
 //              masks keys past the segment; keeps the running max (O is rescaled in TMEM only
 //              when the max grows by more than 2^8) and sum; writes its half row of bf16 P to TMEM; at
 //              the end of the tile normalises and stores its half of the O row.
 //   warp 8     MMA issuer (one thread): S and G of stage s+1 as soon as the softmax warps have
 //              read stage s's, then P.V of stage s.
-//   warp 9     TMA producer: q rows, and K, band and V tiles into a two-slot ring.  A slot's
-//              K and band are refilled as soon as the softmax warps are done with that region
-//              (they stage G there), its V once the slot's last P.V has finished; S and G of a
-//              stage wait for K and band alone.
+//   warp 9     TMA producer of the q rows and of the K and band tiles of a two-slot ring: a
+//              slot's K and band are refilled as soon as the S and G products that read them
+//              have finished.
+//   warp 10    TMA producer of the ring's V tiles: a slot's V is refilled once its last P.V has
+//              finished.  With V on a thread of its own, the next K and band never wait behind
+//              a V copy; S and G of a stage wait for K and band alone.
 // Every wait is bounded; a wait that runs out raises the timeout bit and aborts the CTA's
 // remaining work, after which the CTA still drains its copies and tensor-core work and frees
 // its TMEM.
@@ -43,16 +46,14 @@ namespace {
 
 constexpr int kTcMaxSeqs = 1024;
 constexpr int kSoftmaxWarps = 8;
-constexpr int kTcThreads = 32 * (kSoftmaxWarps + 2);
-constexpr int kMmaWarp = kSoftmaxWarps, kTmaWarp = kSoftmaxWarps + 1;
+constexpr int kTcThreads = 32 * (kSoftmaxWarps + 3);
+constexpr int kMmaWarp = kSoftmaxWarps, kTmaWarp = kSoftmaxWarps + 1, kVWarp = kSoftmaxWarps + 2;
 constexpr int kBM = 128;                 // queries per tile
 constexpr int kBN = 128;                 // keys per stage
 constexpr int kBand = 256;               // band rows per stage
 constexpr int kTmemCols = 512;
 constexpr int kColS = 0, kColG = 128, kColO = 384, kColP = 448;
-constexpr int kStgWarpBytes = 6400;     // one warp's bf16 staging: 32 rows of 48 words, padded
-constexpr int kStgOverlay = 7;           // warps whose staging overlays the stage's K and band tiles
-constexpr int kUvHeads = 32;             // pos_bias_u / v of up to this many heads live in smem
+constexpr int kStgWarpBytes = 4704;     // one warp's bf16 staging: 32 rows of 9 16-byte chunks
 
 struct TcSmem {
     static constexpr int k_tile = kBN * kRowBytes;               // 16 KB
@@ -61,17 +62,15 @@ struct TcSmem {
     static constexpr int slot = k_tile + band_tile + v_tile;     // 64 KB: K | band | V
     static constexpr int off_band = k_tile;
     static constexpr int off_v = k_tile + band_tile;
-    static_assert(kStgOverlay * kStgWarpBytes <= k_tile + band_tile, "staging overlay");
     static constexpr int off_slot = 0;                           // 2 slots
     static constexpr int off_qu = 2 * slot;                      // 16 KB
     static constexpr int off_qv = off_qu + kBM * kRowBytes;      // 16 KB
     static constexpr int off_qbuf = off_qv + kBM * kRowBytes;    // 16 KB: next item's q rows (TMA)
-    static constexpr int off_stg = off_qbuf + kBM * kRowBytes;   // dedicated staging
-    static constexpr int off_xm = off_stg + (kSoftmaxWarps - kStgOverlay) * kStgWarpBytes;
+    static constexpr int off_stg = off_qbuf + kBM * kRowBytes;   // the softmax warps' staging
+    static constexpr int off_xm = off_stg + kSoftmaxWarps * kStgWarpBytes;
     static constexpr int off_cu = off_xm + 2 * 2 * kBM * 4;      // [exchange parity][half][row]
     static constexpr int off_tile = off_cu + (kTcMaxSeqs + 1) * 4;
-    static constexpr int off_uv = (off_tile + (kTcMaxSeqs + 1) * 4 + 15) & ~15;   // u | v, bf16
-    static constexpr int off_misc = off_uv + 2 * kUvHeads * kRowBytes;   // wsum[16], tmem, abort
+    static constexpr int off_misc = (off_tile + (kTcMaxSeqs + 1) * 4 + 15) & ~15;   // wsum[16], tmem, abort
     static constexpr int off_bar = (off_misc + 128 + 7) & ~7;
     static constexpr int n_bars = 2 + 2 + 7 + 4 + 2 + 2 + 2;
     static constexpr int bytes = off_bar + n_bars * 8 + 1024;
@@ -90,6 +89,16 @@ struct TcArgs {
     uint32_t sign;           // 0x80008000 when the scale is negative (q+u, q+v are negated)
     float scale_log2;        // |scale| * log2(e)
 };
+
+// lo += bf16 low half of pair, hi += bf16 high half, each rounded once in fp32 (a bf16 value
+// widens to fp32 exactly, so this equals widening first and adding in fp32)
+__device__ __forceinline__ void add_bf16x2_f32(float& lo, float& hi, uint32_t pair)
+{
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(pair));
+}
 
 // ------------------------------------------------------------------------ kernel
 
@@ -123,7 +132,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
     const uint32_t bar_pair = bar_drain + 8;           // [4] softmax warp pair exchanged a value
     const uint32_t bar_qb_full = bar_pair + 32;        // q rows of the next item landed
     const uint32_t bar_qb_free = bar_qb_full + 8;      // softmax warps have read the q rows
-    const uint32_t bar_kb_empty = bar_qb_free + 8;     // [2] the slot's K and band region free
+    const uint32_t bar_kb_empty = bar_qb_free + 8;     // [2] the slot's K and band tiles read
     const uint32_t bar_v_full = bar_kb_empty + 16;     // [2] the stage's V tile landed
     const int ns = a.num_seqs;
 
@@ -143,7 +152,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
         mbar_init(bar_qb_full, 1);
         mbar_init(bar_qb_free, kSoftmaxWarps);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_kb_empty + 8 * i, kSoftmaxWarps);
+            mbar_init(bar_kb_empty + 8 * i, 1);
             mbar_init(bar_v_full + 8 * i, 1);
         }
         fence_mbar_init();
@@ -155,15 +164,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                      "r"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
-    // pos_bias_u and pos_bias_v of every head (when they fit), read per item by prep_q
-    const bool uv_smem = a.H <= kUvHeads;
-    uint4* s_uv = reinterpret_cast<uint4*>(sm + SP::off_uv);   // [u | v][head][8 x 16 B]
-    if (uv_smem)
-        for (int i = tid; i < 2 * a.H * 8; i += kTcThreads) {
-            const int which = i >= a.H * 8, rem = i - which * a.H * 8;
-            s_uv[which * kUvHeads * 8 + rem] =
-                __ldg(reinterpret_cast<const uint4*>(which ? a.pos_bias_v : a.pos_bias_u) + rem);
-        }
     // segment starts and the exclusive prefix of per-segment 128-row tile counts
     for (int i = tid; i <= ns; i += kTcThreads) {
         int c = __ldg(a.cu_seqlens + i);
@@ -287,12 +287,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 mbar_arrive_expect_tx(bar_qb_full, kBM * kRowBytes);
                 tma_load_3d(sb + SP::off_qbuf, &tm_q, bar_qb_full, 0, h, start + i0);
                 for (int s = 0; s < n_st; ++s, ++g) {
-                    // K and band as soon as the softmax warps are done with the slot's K and band
-                    // region (its S and G computed, their staging reads finished), V once the
-                    // slot's last P.V has finished
+                    // K and band as soon as the S and G products that read the slot's last ones
+                    // have finished
                     const int slot = g & 1;
-                    const uint32_t ph = ((g >> 1) - 1) & 1;
-                    if (g >= 2 && !prod_wait(bar_kb_empty + 8 * slot, ph, s_abort)) {
+                    if (g >= 2 && !prod_wait(bar_kb_empty + 8 * slot, ((g >> 1) - 1) & 1, s_abort)) {
                         ok = false;
                         break;
                     }
@@ -302,20 +300,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     const int js = kl + s * kBN;   // first key of the stage
                     tma_load_3d_hint(base, &tm_k, bar, 0, h, start + js, pol);
                     tma_load_3d(base + SP::off_band, &tm_r, bar, 0, h, a.z - i0 + js - (kBM - 1));
-                    if (g >= 2 && !prod_wait(bar_empty + 8 * slot, ph, s_abort)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(bar_v_full + 8 * slot, SP::v_tile);
-                    tma_load_3d_hint(base + SP::off_v, &tm_v, bar_v_full + 8 * slot, 0, h, start + js, pol);
                 }
             }
             // no copy may still be landing when the CTA exits
             for (int u = g - 2; u < g; ++u)
-                if (u >= 0 && !(mbar_wait(bar_full + 8 * (u & 1), (u >> 1) & 1) &&
-                                mbar_wait(bar_v_full + 8 * (u & 1), (u >> 1) & 1)))
-                    *s_abort = 1;
+                if (u >= 0 && !mbar_wait(bar_full + 8 * (u & 1), (u >> 1) & 1)) *s_abort = 1;
             if (itp > 0 && !mbar_wait(bar_qb_full, (itp - 1) & 1)) *s_abort = 1;
+        }
+    } else if (warp == kVWarp) {
+        // ---------------------------------------------------------- V producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_last();
+            int g = 0, seg = 0;
+            bool ok = true;
+            for (long long item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+                int start, L, i0, h, kl, kh;
+                decode(item, seg, start, L, i0, h, kl, kh);
+                const int n_st = (kh - kl + kBN - 1) / kBN;
+                for (int s = 0; s < n_st; ++s, ++g) {
+                    const int slot = g & 1;
+                    if (g >= 2 && !prod_wait(bar_empty + 8 * slot, ((g >> 1) - 1) & 1, s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar_v_full + 8 * slot, SP::v_tile);
+                    tma_load_3d_hint(sb + SP::off_slot + slot * SP::slot + SP::off_v, &tm_v,
+                                     bar_v_full + 8 * slot, 0, h, start + kl + s * kBN, pol);
+                }
+            }
+            for (int u = g - 2; u < g; ++u)
+                if (u >= 0 && !mbar_wait(bar_v_full + 8 * (u & 1), (u >> 1) & 1)) *s_abort = 1;
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------- MMA issuer
@@ -323,6 +337,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             constexpr uint32_t id_s = idesc(kBM, kBN, 0), id_g = idesc(kBM, kBand, 0),
                                id_o = idesc(kBM, 64, 1);
             int g = 0, it = 0, sg = 0, nq = 0, npv = 0;
+            int kbn[2] = {0, 0};   // commits to each slot's K-and-band barrier
             auto issue_sg = [&](int slot) {
                 const uint32_t base = sb + SP::off_slot + slot * SP::slot;
                 tc_fence_after();
@@ -334,6 +349,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     umma_ss(tmem + kColG, sdesc(sb + SP::off_qv + 32 * k),
                             sdesc(base + SP::off_band + 32 * k), id_g, k > 0);
                 umma_commit(bar_sg_full);
+                umma_commit(bar_kb_empty + 8 * slot);   // the slot's K and band may be refilled
+                ++kbn[slot];
                 ++sg;
             };
             // One flat walk over the CTA's stages.  The S/G of the next stage, which may be
@@ -410,6 +427,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             if (npv > 0) drained = mbar_wait(bar_pv_done, (npv - 1) & 1) && drained;
             for (int u = npv - 2; u < npv; ++u)
                 if (u >= 0) drained = mbar_wait(bar_empty + 8 * (u & 1), (u >> 1) & 1) && drained;
+            for (int sl = 0; sl < 2; ++sl)
+                if (kbn[sl] > 0) drained = mbar_wait(bar_kb_empty + 8 * sl, (kbn[sl] - 1) & 1) && drained;
             if (!drained) *s_abort = 1;
         }
     } else if (warp < kSoftmaxWarps) {
@@ -439,15 +458,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             if (!warp_wait(bar_qb_full, itq & 1)) return false;
             const uint4* up = reinterpret_cast<const uint4*>(a.pos_bias_u + hq * kHeadDim);
             const uint4* vp = reinterpret_cast<const uint4*>(a.pos_bias_v + hq * kHeadDim);
-            const uint4* sup = s_uv + hq * 8;
-            const uint4* svp = s_uv + (kUvHeads + hq) * 8;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 const int c = 4 * hf + cc;
                 const uint32_t offs = static_cast<uint32_t>(r * kRowBytes + ((c ^ (r & 7)) << 4));
                 const uint4 qc = *reinterpret_cast<const uint4*>(sm + SP::off_qbuf + offs);
-                const uint4 uc = uv_smem ? sup[c] : __ldg(up + c);
-                const uint4 vc = uv_smem ? svp[c] : __ldg(vp + c);
+                const uint4 uc = __ldg(up + c);
+                const uint4 vc = __ldg(vp + c);
                 const uint32_t w[4] = {qc.x, qc.y, qc.z, qc.w};
                 const uint32_t wu[4] = {uc.x, uc.y, uc.z, uc.w};
                 const uint32_t wv[4] = {vc.x, vc.y, vc.z, vc.w};
@@ -534,17 +551,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 float sc[64];
                 // position term, skewed: row r needs G[r][127 - r + j].  This warp's rows reach
                 // 95 columns of G for this half (row r, key j of the half: window column
-                // 31 - lane + j), which go through shared memory as bf16 pairs (the stage's K and
-                // band tiles, free once S and G are computed, for the first warps).  Row bases of
-                // 48 * lane + 4 * (lane >> 1) words keep both the 16-byte stores and the
-                // lane-shifted 4-byte loads free of bank conflicts.  Lane reads words w0 .. w0+32
-                // (w0 = (31 - lane) / 2); an even lane's window starts on the odd half of word
-                // w0, so its pairs are realigned with a byte permute.
-                uint32_t* stg = reinterpret_cast<uint32_t*>(
-                                    warp < kStgOverlay ? slot_p + warp * kStgWarpBytes
-                                                       : sm + SP::off_stg + (warp - kStgOverlay) * kStgWarpBytes) +
-                                (48 * lane + 4 * (lane >> 1));
+                // 31 - lane + j), which go through this warp's shared staging tile as bf16 pairs.
+                // Lane reads words w0 .. w0+32 (w0 = (31 - lane) / 2), so it stores only the
+                // 16-byte chunks q0 .. q0+8 (q0 = w0 / 4) of the window, from a row base of
+                // 4 (9 lane + 2 (lane / 8)) words: the eight lanes of a store phase share q0 and
+                // land in distinct bank quads, and the lane-shifted 4-byte loads hit 32 distinct
+                // banks.  An even lane's window starts on the odd half of word w0, so its pairs
+                // are realigned with a byte permute.
                 const int w0 = (31 - lane) >> 1;
+                const int q0 = w0 >> 2;
+                uint32_t* stg = reinterpret_cast<uint32_t*>(sm + SP::off_stg + warp * kStgWarpBytes) +
+                                4 * (9 * lane + 2 * (lane >> 3));
                 if (live) {
                     uint32_t gr[96];
                     const uint32_t colg = kColG + static_cast<uint32_t>(96 - 32 * quad + 64 * hf);
@@ -554,13 +571,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                     tmem_wait_ld();
 #pragma unroll
                     for (int pc = 0; pc < 12; ++pc)
-                        if (4 * pc + 3 >= w0 && 4 * pc <= w0 + 32) {
+                        if (pc >= q0 && pc <= q0 + 8) {
                             uint32_t gw[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
                                 gw[e] = pack_bf16(__uint_as_float(gr[8 * pc + 2 * e]),
                                                   __uint_as_float(gr[8 * pc + 2 * e + 1]));
-                            *reinterpret_cast<uint4*>(stg + 4 * pc) = make_uint4(gw[0], gw[1], gw[2], gw[3]);
+                            *reinterpret_cast<uint4*>(stg + 4 * (pc - q0)) = make_uint4(gw[0], gw[1], gw[2], gw[3]);
                         }
                     uint32_t sr[64];
                     OASR_TMEM_LD32(tl + kColS + 64 * hf, sr);
@@ -576,24 +593,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 if (lane == 0) mbar_arrive(bar_sg_free);
                 if (live) {
                     const uint32_t sel = (lane & 1) ? 0x3210u : 0x5432u;
-                    const uint32_t* rd = stg + w0;
+                    const uint32_t* rd = stg + (w0 & 3);
                     uint32_t wa = rd[0];
 #pragma unroll
                     for (int m = 0; m < 32; ++m) {
                         const uint32_t wb = rd[m + 1];
-                        const uint32_t g2 = __byte_perm(wa, wb, sel);
-                        const float2 r2 = __fadd2_rn(make_float2(sc[2 * m], sc[2 * m + 1]),
-                                                     make_float2(__uint_as_float(g2 << 16),
-                                                                 __uint_as_float(g2 & 0xffff0000u)));
-                        sc[2 * m] = r2.x;
-                        sc[2 * m + 1] = r2.y;
+                        add_bf16x2_f32(sc[2 * m], sc[2 * m + 1], __byte_perm(wa, wb, sel));
                         wa = wb;
                     }
                 }
-                // the slot's K and band region (staging included) is no longer read: the producer
-                // may refill it with the stage after next's K and band
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_kb_empty + 8 * (g & 1));
                 // last stage of the item: the next item's Qu/Qv, so that its first S/G can be
                 // issued while this stage's softmax and the epilogue run
                 if (s + 1 == n_st && item + gridDim.x < n_items) {
