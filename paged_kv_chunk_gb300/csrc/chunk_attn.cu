@@ -32,6 +32,14 @@
 #include "host_common.h"
 
 namespace oasr {
+
+// The tensor-core kernel for 33 <= T <= 64 (chunk_tc.cu).
+bool chunk_tc_takes(int B, int T, int H, int mbps, int num_blocks, int block_size, int R);
+oasr_status launch_chunk_tc(const void* q, const void* k_pool, const void* v_pool, int num_blocks,
+                            int block_size, const int32_t* bt, int mbps, const int32_t* cs,
+                            const void* u, const void* vb, const void* rel, int R, void* out,
+                            int B, int T, int H, int k_max, float scale, cudaStream_t stream);
+
 namespace {
 
 struct ChunkArgs {
@@ -721,6 +729,19 @@ oasr_status dispatch(const void* q, const void* k_new, const void* v_new, void* 
             static_cast<const float*>(u), static_cast<const float*>(vb),
             static_cast<const float*>(rel), R, static_cast<float*>(out), T, H, scale, status);
         return launch_status();
+    }
+    // 33 <= T <= 64 with an even head count: the tensor-core kernel (two heads of a stream per
+    // 128-row tile); the fused step appends the chunk first, on the same stream
+    if (T > 32 && chunk_tc_takes(B, T, H, mbps, num_blocks, block_size, R)) {
+        if (FUSED) {
+            const oasr_status st = oasr_paged_append(k_new, v_new, k_pool, v_pool, num_blocks,
+                                                     block_size, bt, mbps, cs, B, T, H, D, dt,
+                                                     stream);
+            if (st != OASR_OK) return st;
+        }
+        return launch_chunk_tc(q, k_pool, v_pool, num_blocks, block_size, bt, mbps, cs, u, vb,
+                               rel, R, out, B, T, H, key_bound(mbps, block_size, R, T), scale,
+                               stream);
     }
     const int f = FUSED ? 8 : 0;
     // One m-tile (T <= 16): the position table when it fits beside the ring, else the

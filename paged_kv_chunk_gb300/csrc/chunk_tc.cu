@@ -1,0 +1,764 @@
+// Streaming chunk attention over the block-paged pool on the 5th-generation tensor cores
+// (tcgen05 + TMEM), bf16, for chunks of 33 to 64 frames.  Used by oasr_chunk_relattn_paged
+// and oasr_chunk_step_paged (after the append) for those chunk lengths when H is even.
+//
+// Scheduler page, section 4.3 "Heterogeneous-offset batching": each stream's keys are its
+// cache_seqlens cached frames and the chunk, and the rel-pos term matrix_bd / sqrt(d_k) is
+// added to the content score.  Model Layer page, fixed_attention_window row (one rel table
+// serves the cohort, distances cache + i - j) and Nemotron ASR section (rel_shift order):
+// query i and key j of stream b use rel row rho = (R - T - C_b) - i + j.
+//
+// A chunk of T <= 64 queries fills half of a 128-row tensor-core tile, so one work item is a
+// stream and a pair of its heads (h0 = 2 hp, h0 + 1): TMEM lanes 0-63 hold the chunk's queries
+// for head h0 and lanes 64-127 for head h0 + 1 (rows T..63 of each half are padding).  A
+// tcgen05.mma of M128 K16 costs about the same up to N = 128, so each product spans both heads
+// at N = 128 and each row keeps the half that belongs to its head.  Per stage of 64 keys:
+//   S [128 x 128] = bf16(q+u) . [K_h0 ; K_h1]^T          columns [0, 128)    M128 N128; rows of
+//                   head h0 keep columns 0-63 (its keys), rows of h0 + 1 columns 64-127
+//   G [128 x 128] = A0 . Band_h0^T + A1 . Band_h1^T      columns [128, 256)  M128 N128, block-
+//                   diagonal: A0 = [bf16(q+v) of h0 ; 0], A1 = [0 ; bf16(q+v) of h0+1] (one 8 KB
+//                   zero block shared between them); the band is the 128 rel rows rho_min ..
+//                   rho_min + 127 the stage reaches (rho_min = R - T - C - 63 + 64 s), and row i,
+//                   key j of the stage uses band row 63 - i + j
+//   O [128 x 128] += P . [V_h0 | V_h1]                   columns [256, 384)  M128 N128; rows of
+//                   head h0 keep columns 0-63, rows of h0 + 1 columns 64-127
+//   P [128 x 64] bf16                                    columns [384, 416)
+// Warp roles (352 threads), one persistent CTA per SM walking work items:
+//   warps 0-7  softmax.  Warps w and w+4 share TMEM lane quadrant w (rows 32w .. 32w+31); warp
+//              w takes keys 0-31 of each stage, w+4 keys 32-63, and the pair swaps row maxima
+//              and sums through shared memory.  Each thread reads its S half row and the G
+//              columns its row reaches, releases S and G to the issuer, takes its skewed half
+//              row of G (rounded to bf16) through its own shared staging tile, masks keys past
+//              the stream's history, keeps the running max (O is rescaled in TMEM only when
+//              the max grows by more than 2^8) and sum, and writes its half row of bf16 P to
+//              TMEM; at the end of the item it normalises and stores its half of the O row.
+//   warp 8     MMA issuer (one thread).
+//   warp 9     TMA producer of the q rows and of the stage's K page boxes and rel band.
+//   warp 10    TMA producer of the stage's V page boxes.
+// K and V arrive as one box per block-table page and head (as in the pool: a page's rows of
+// one head, 128 B each, 128-byte swizzled); a block id outside the pool reads as zero rows.
+// Every wait is bounded; a wait that runs out raises the timeout bit and aborts the CTA's
+// remaining work, after which the CTA still drains its copies and tensor-core work and frees
+// its TMEM.
+#include "attn_core.cuh"
+#include "host_common.h"
+#include "ptx.cuh"
+#include "tcgen05.cuh"
+
+namespace oasr {
+namespace {
+
+constexpr int kCtSoftmaxWarps = 8;
+constexpr int kCtThreads = 32 * (kCtSoftmaxWarps + 3);
+constexpr int kCtMmaWarp = 8, kCtKWarp = 9, kCtVWarp = 10;
+constexpr int kCtBN = 64;                 // keys per stage
+constexpr int kCtBand = 128;              // band rows per stage and head
+constexpr int kCtTq = 64;                 // query rows of one head in the tile
+constexpr int kCtTmemCols = 512;
+constexpr int kCtColS = 0, kCtColG = 128, kCtColO = 256, kCtColP = 384;
+constexpr int kCtStg = 2656;              // one softmax warp's bf16 staging: 32 rows of 5 chunks
+constexpr int kCtMaxPages = 512;          // block-table entries a producer caches
+constexpr int kCtMaxItems = 256;          // work items of one CTA whose lengths are cached
+
+struct CtSmem {
+    static constexpr int head_k = kCtBN * kRowBytes;              // 8 KB: 64 keys of one head
+    static constexpr int head_band = kCtBand * kRowBytes;         // 16 KB
+    static constexpr int off_k = 0;                               // K h0 | K h1
+    static constexpr int off_band = 2 * head_k;                   // band h0 | band h1
+    static constexpr int off_v = off_band + 2 * head_band;        // V h0 | V h1
+    static constexpr int slot = off_v + 2 * head_k;               // 64 KB
+    static constexpr int off_slot = 0;                            // 2 slots
+    static constexpr int q_tile = kCtTq * kRowBytes;              // 8 KB: 64 rows of one head
+    // bf16(q+u): one tile [h0 rows | h0+1 rows]; bf16(q+v): [h0 rows | zero | h0+1 rows], A0
+    // starting at 0 and A1 at q_tile
+    static constexpr int off_qu = 2 * slot;
+    static constexpr int off_qv = off_qu + 2 * q_tile;
+    static constexpr int off_qbuf = off_qv + 3 * q_tile;          // next item's q rows (TMA), 2 heads
+    static constexpr int off_stg = off_qbuf + 2 * q_tile;
+    static constexpr int off_xm = off_stg + kCtSoftmaxWarps * kCtStg;   // [parity][half][row]
+    static constexpr int off_btk = off_xm + 2 * 2 * 128 * 4;
+    static constexpr int off_btv = off_btk + kCtMaxPages * 4;
+    static constexpr int off_len = off_btv + kCtMaxPages * 4;     // per item: C, N
+    static constexpr int off_misc = off_len + 2 * kCtMaxItems * 4;   // tmem, abort
+    static constexpr int off_bar = off_misc + 64;
+    static constexpr int n_bars = 2 + 2 + 2 + 2 + 9 + 4;
+    static constexpr int bytes = off_bar + n_bars * 8 + 1024;
+    static_assert(bytes <= 232448, "dynamic shared memory of one CTA");
+    static_assert(slot % 1024 == 0 && off_qu % 1024 == 0 && off_qv % 1024 == 0 &&
+                  off_qbuf % 1024 == 0, "TMA and MMA tiles need 1024-byte alignment");
+};
+
+struct CtArgs {
+    const int32_t* block_table;
+    const int32_t* cache_seqlens;
+    const uint16_t* pos_bias_u;
+    const uint16_t* pos_bias_v;
+    uint16_t* out;
+    unsigned* status;
+    int B, T, H, R, num_blocks, block_size, bs_shift, box_rows, mbps;
+    int k_max;               // keys a stream may have (the table's pages, the rel table's reach)
+    uint32_t sign;           // 0x80008000 when the scale is negative (q+u, q+v are negated)
+    float scale_log2;        // |scale| * log2(e)
+};
+
+// lo += bf16 low half of pair, hi += bf16 high half, each rounded once in fp32 (a bf16 value
+// widens to fp32 exactly, so this equals widening first and adding in fp32)
+__device__ __forceinline__ void ct_add_bf16x2(float& lo, float& hi, uint32_t pair)
+{
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(pair));
+}
+
+__global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r, const CtArgs a)
+{
+    using SP = CtSmem;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte aligned base, derived from the __shared__ array itself so that every access
+    // through it stays a shared-space access
+    uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_addr(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    unsigned err = 0;
+    int* s_len = reinterpret_cast<int*>(sm + SP::off_len);        // [item] C, then N
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + SP::off_misc);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SP::off_misc + 4);
+    const uint32_t bar_full = sb + SP::off_bar;        // [2] the stage's K and band landed
+    const uint32_t bar_vfull = bar_full + 16;          // [2] the stage's V landed
+    const uint32_t bar_kb_empty = bar_vfull + 16;      // [2] the slot's K and band read (S/G done)
+    const uint32_t bar_v_empty = bar_kb_empty + 16;    // [2] the slot's V read (P.V done)
+    const uint32_t bar_sg_full = bar_v_empty + 16;     // S and G in TMEM
+    const uint32_t bar_sg_free = bar_sg_full + 8;      // softmax warps have read S and G
+    const uint32_t bar_p_full = bar_sg_free + 8;       // P written to TMEM
+    const uint32_t bar_pv_done = bar_p_full + 8;       // P.V finished
+    const uint32_t bar_q_ready = bar_pv_done + 8;      // bf16(q+u), bf16(q+v) written
+    const uint32_t bar_q_free = bar_q_ready + 8;       // last S/G MMA of an item finished
+    const uint32_t bar_drain = bar_q_free + 8;         // everything the MMA issuer issued finished
+    const uint32_t bar_qb_full = bar_drain + 8;        // q rows of the next item landed
+    const uint32_t bar_qb_free = bar_qb_full + 8;      // softmax warps have read the q rows
+    const uint32_t bar_pair = bar_qb_free + 8;         // [4] softmax warp pair exchanged a value
+    const int Hp = a.H >> 1;
+    const long long n_items = static_cast<long long>(a.B) * Hp;
+    const int my_items = n_items > blockIdx.x
+                             ? static_cast<int>((n_items - 1 - blockIdx.x) / gridDim.x) + 1
+                             : 0;
+
+    if (warp == kCtKWarp && lane == 0) {
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_r);
+    }
+    if (warp == kCtVWarp && lane == 0) prefetch_tensormap(&tm_v);
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_vfull + 8 * i, 1);
+            mbar_init(bar_kb_empty + 8 * i, 1);
+            mbar_init(bar_v_empty + 8 * i, 1);
+        }
+        mbar_init(bar_sg_full, 1);
+        mbar_init(bar_sg_free, kCtSoftmaxWarps);
+        mbar_init(bar_p_full, kCtSoftmaxWarps);
+        mbar_init(bar_pv_done, 1);
+        mbar_init(bar_q_ready, kCtSoftmaxWarps);
+        mbar_init(bar_q_free, 1);
+        mbar_init(bar_drain, 1);
+        mbar_init(bar_qb_full, 1);
+        mbar_init(bar_qb_free, kCtSoftmaxWarps);
+        for (int i = 0; i < 4; ++i) mbar_init(bar_pair + 8 * i, 64);
+        fence_mbar_init();
+        *s_abort = 0;
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(s_tmem)),
+                     "r"(kCtTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    // the zero block shared by the two block-diagonal A tiles of G
+    for (int i = tid; i < SP::q_tile / 16; i += kCtThreads)
+        reinterpret_cast<uint4*>(sm + SP::off_qv + SP::q_tile)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    // Launched with programmatic stream serialization: everything the previous grid on the
+    // stream wrote (the append of this step's chunk) is visible once this returns.
+    grid_dep_wait();
+    // every item's cache length and key count (keys past what the host can bound are dropped
+    // and flagged, as is a negative cache length)
+    for (int k = tid; k < my_items; k += kCtThreads) {
+        const long long item = blockIdx.x + static_cast<long long>(k) * gridDim.x;
+        const int b = static_cast<int>(item / Hp);
+        int c = __ldg(a.cache_seqlens + b);
+        if (c < 0) { err |= kErrBounds; c = 0; }
+        long long n = static_cast<long long>(c) + a.T;
+        if (n > a.k_max) { err |= kErrBounds; n = a.k_max; }
+        s_len[2 * k] = c;
+        s_len[2 * k + 1] = static_cast<int>(n);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    // The producers poll with a pause between tries, so that their warps take few issue
+    // slots from the softmax warps sharing their schedulers.
+    auto prod_wait = [&](uint32_t bar, uint32_t parity) {
+        if (mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = global_timer_ns();
+        for (;;) {
+            __nanosleep(128);
+            if (mbar_try_wait(bar, parity)) return true;
+            if (*s_abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) { *s_abort = 1; return false; }
+        }
+    };
+    // Softmax warps take every wait together: a warp-wide vote keeps the warp converged for
+    // the .sync.aligned tensor-memory instructions even if one lane's wait runs out.
+    auto warp_wait = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, wait_or_abort(bar, parity, s_abort)) != 0;
+    };
+    auto item_of = [&](int k) { return blockIdx.x + static_cast<long long>(k) * gridDim.x; };
+
+    // One producer warp's page boxes of a stage: box q of the stage (one page of one head)
+    // goes from lane q.  Returns the bytes the stage's boxes bring.
+    auto page_boxes = [&](const CUtensorMap* map, const int* bt_row, int s, int N, int h0,
+                          uint32_t dst0, uint32_t bar, uint64_t pol, bool issue) {
+        const int j0 = s * kCtBN;
+        const int jn = N - j0 < kCtBN ? N - j0 : kCtBN;
+        const int nbox = a.box_rows == kCtBN ? 1 : (jn + a.box_rows - 1) >> a.bs_shift;
+        if (issue && lane < 2 * nbox) {
+            const int idx = lane >> 1, hd = lane & 1;
+            const int key = j0 + idx * a.box_rows;                // first key of the box
+            const int blk = bt_row[key >> a.bs_shift];
+            int row;
+            if (blk >= 0 && blk < a.num_blocks) {
+                row = (blk << a.bs_shift) + (key & (a.block_size - 1));
+            } else {
+                err |= kErrBounds;
+                row = a.num_blocks << a.bs_shift;                 // past the pool: zero rows
+            }
+            tma_load_3d_hint(dst0 + hd * SP::head_k + idx * a.box_rows * kRowBytes, map, bar, 0,
+                             h0 + hd, row, pol);
+        }
+        return 2 * nbox * a.box_rows * kRowBytes;
+    };
+    // the block-table row of stream b, pages [0, ceil(N / block_size)), into a producer's cache
+    auto load_bt = [&](int* bt_row, int b, int N) {
+        const int np = (N + a.block_size - 1) >> a.bs_shift;
+        const int32_t* src = a.block_table + static_cast<long long>(b) * a.mbps;
+        for (int p = lane; p < np; p += 32) bt_row[p] = __ldg(src + p);
+        __syncwarp();
+    };
+
+    if (warp == kCtKWarp) {
+        // ------------------------------------------------ q rows, K and band producer
+        int* bt_row = reinterpret_cast<int*>(sm + SP::off_btk);
+        const uint64_t pol = policy_evict_first();   // every K and V row is read once
+        int g = 0, itp = 0;
+        bool ok = true;
+        for (int k = 0; k < my_items && ok; ++k, ++itp) {
+            const long long item = item_of(k);
+            const int b = static_cast<int>(item / Hp), h0 = 2 * static_cast<int>(item - static_cast<long long>(b) * Hp);
+            const int C = s_len[2 * k], N = s_len[2 * k + 1];
+            const int n_st = (N + kCtBN - 1) / kCtBN;
+            load_bt(bt_row, b, N);
+            // the item's q rows of both heads, once the softmax warps have read the previous ones
+            if (lane == 0) {
+                if (itp > 0 && !prod_wait(bar_qb_free, (itp - 1) & 1)) ok = false;
+                if (ok) {
+                    mbar_arrive_expect_tx(bar_qb_full, 2 * SP::q_tile);
+                    tma_load_3d(sb + SP::off_qbuf, &tm_q, bar_qb_full, 0, h0, b * a.T);
+                    tma_load_3d(sb + SP::off_qbuf + SP::q_tile, &tm_q, bar_qb_full, 0, h0 + 1, b * a.T);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            for (int s = 0; s < n_st && ok; ++s, ++g) {
+                const int slot = g & 1;
+                if (lane == 0 && g >= 2 && !prod_wait(bar_kb_empty + 8 * slot, ((g >> 1) - 1) & 1)) ok = false;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                const uint32_t base = sb + SP::off_slot + slot * SP::slot;
+                const uint32_t bar = bar_full + 8 * slot;
+                const int kbytes = page_boxes(&tm_k, bt_row, s, N, h0, base + SP::off_k, bar, pol, false);
+                if (lane == 0) mbar_arrive_expect_tx(bar, kbytes + 2 * SP::head_band);
+                __syncwarp();
+                page_boxes(&tm_k, bt_row, s, N, h0, base + SP::off_k, bar, pol, true);
+                // the band: rel rows rho_min .. rho_min + 127 of both heads (rows outside the
+                // table read as zeros)
+                if (lane < 2) {
+                    const int rho_min = a.R - a.T - C - (kCtTq - 1) + s * kCtBN;
+                    tma_load_3d(base + SP::off_band + lane * SP::head_band, &tm_r, bar, 0, h0 + lane, rho_min);
+                }
+            }
+        }
+        // no copy may still be landing when the CTA exits
+        if (lane == 0) {
+            for (int u = g - 2; u < g; ++u)
+                if (u >= 0 && !mbar_wait(bar_full + 8 * (u & 1), (u >> 1) & 1)) *s_abort = 1;
+            if (itp > 0 && !mbar_wait(bar_qb_full, (itp - 1) & 1)) *s_abort = 1;
+        }
+    } else if (warp == kCtVWarp) {
+        // ---------------------------------------------------------------- V producer
+        int* bt_row = reinterpret_cast<int*>(sm + SP::off_btv);
+        const uint64_t pol = policy_evict_first();
+        int g = 0;
+        bool ok = true;
+        for (int k = 0; k < my_items && ok; ++k) {
+            const long long item = item_of(k);
+            const int b = static_cast<int>(item / Hp), h0 = 2 * static_cast<int>(item - static_cast<long long>(b) * Hp);
+            const int N = s_len[2 * k + 1];
+            const int n_st = (N + kCtBN - 1) / kCtBN;
+            load_bt(bt_row, b, N);
+            for (int s = 0; s < n_st && ok; ++s, ++g) {
+                const int slot = g & 1;
+                if (lane == 0 && g >= 2 && !prod_wait(bar_v_empty + 8 * slot, ((g >> 1) - 1) & 1)) ok = false;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                const uint32_t dst = sb + SP::off_slot + slot * SP::slot + SP::off_v;
+                const uint32_t bar = bar_vfull + 8 * slot;
+                const int vbytes = page_boxes(&tm_v, bt_row, s, N, h0, dst, bar, pol, false);
+                if (lane == 0) mbar_arrive_expect_tx(bar, vbytes);
+                __syncwarp();
+                page_boxes(&tm_v, bt_row, s, N, h0, dst, bar, pol, true);
+            }
+        }
+        if (lane == 0)
+            for (int u = g - 2; u < g; ++u)
+                if (u >= 0 && !mbar_wait(bar_vfull + 8 * (u & 1), (u >> 1) & 1)) *s_abort = 1;
+    } else if (warp == kCtMmaWarp) {
+        // ------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc(128, 2 * kCtBN, 0), id_g = idesc(128, kCtBand, 0),
+                               id_o = idesc(128, 128, 1);
+            int g = 0, it = 0, sg = 0, nq = 0, npv = 0;
+            int kbn[2] = {0, 0}, vn[2] = {0, 0};
+            auto issue_sg = [&](int slot) {
+                const uint32_t base = sb + SP::off_slot + slot * SP::slot;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    umma_ss(tmem + kCtColS, sdesc(sb + SP::off_qu + 32 * k), sdesc(base + SP::off_k + 32 * k),
+                            id_s, k > 0);
+#pragma unroll
+                for (int hd = 0; hd < 2; ++hd)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        umma_ss(tmem + kCtColG, sdesc(sb + SP::off_qv + hd * SP::q_tile + 32 * k),
+                                sdesc(base + SP::off_band + hd * SP::head_band + 32 * k), id_g,
+                                (hd | k) ? 1 : 0);
+                umma_commit(bar_sg_full);
+                umma_commit(bar_kb_empty + 8 * slot);   // the slot's K and band may be refilled
+                ++kbn[slot];
+                ++sg;
+            };
+            // One flat walk over the CTA's stages: S and G of the next stage (possibly the next
+            // item's first) as soon as this stage's S and G have been read, then P.V of this one.
+            int k_item = 0, n_st = 0, s = 0, n_keys = 0;
+            auto item_stages = [&](int k, int& keys) {
+                keys = s_len[2 * k + 1];
+                return (keys + kCtBN - 1) / kCtBN;
+            };
+            bool ok = my_items > 0;
+            if (ok) {
+                n_st = item_stages(0, n_keys);
+                ok = wait_or_abort(bar_q_ready, 0, s_abort) && wait_or_abort(bar_full, 0, s_abort);
+                if (ok) {
+                    issue_sg(0);
+                    if (n_st == 1) { umma_commit(bar_q_free); ++nq; }
+                }
+            }
+            while (ok) {
+                const bool last = s + 1 == n_st;
+                const int next_k = last ? k_item + 1 : k_item;
+                if (next_k < my_items) {
+                    int next_keys = 0;
+                    const int next_n = last ? item_stages(next_k, next_keys) : n_st;
+                    const int next_s = last ? 0 : s + 1;
+                    ok = (!last || wait_or_abort(bar_q_ready, (it + 1) & 1, s_abort)) &&
+                         wait_or_abort(bar_full + 8 * ((g + 1) & 1), ((g + 1) >> 1) & 1, s_abort) &&
+                         wait_or_abort(bar_sg_free, (sg - 1) & 1, s_abort);
+                    if (!ok) break;
+                    issue_sg((g + 1) & 1);
+                    if (next_s + 1 == next_n) { umma_commit(bar_q_free); ++nq; }
+                }
+                // P.V of stage g, only over the 16-key steps that hold keys of the stream
+                ok = wait_or_abort(bar_p_full, g & 1, s_abort) &&
+                     wait_or_abort(bar_vfull + 8 * (g & 1), (g >> 1) & 1, s_abort);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t vbase = sb + SP::off_slot + (g & 1) * SP::slot + SP::off_v;
+                const int kst = n_keys - s * kCtBN;
+                const int ksteps = kst < kCtBN ? (kst + 15) >> 4 : kCtBN / 16;
+                // B = [V_h0 | V_h1]: MN-major, the second head's 64 columns one tile (8 KB) on
+#pragma unroll
+                for (int k = 0; k < kCtBN / 16; ++k)
+                    if (k < ksteps)
+                        umma_ts(tmem + kCtColO, tmem + kCtColP + 8 * k, sdesc_lbo(vbase + 2048 * k, SP::head_k),
+                                id_o, (s > 0 || k > 0) ? 1 : 0);
+                umma_commit(bar_pv_done);
+                umma_commit(bar_v_empty + 8 * (g & 1));
+                ++vn[g & 1];
+                ++npv;
+                ++g;
+                if (!last) {
+                    ++s;
+                } else {
+                    k_item = next_k;
+                    ++it;
+                    if (k_item >= my_items) break;
+                    n_st = item_stages(k_item, n_keys);
+                    s = 0;
+                }
+            }
+            // drain: every MMA issued has finished and every arrival it owes has landed
+            umma_commit(bar_drain);
+            bool drained = mbar_wait(bar_drain, 0);
+            if (nq > 0) drained = mbar_wait(bar_q_free, (nq - 1) & 1) && drained;
+            if (sg > 0) drained = mbar_wait(bar_sg_full, (sg - 1) & 1) && drained;
+            if (npv > 0) drained = mbar_wait(bar_pv_done, (npv - 1) & 1) && drained;
+            for (int sl = 0; sl < 2; ++sl) {
+                if (kbn[sl] > 0) drained = mbar_wait(bar_kb_empty + 8 * sl, (kbn[sl] - 1) & 1) && drained;
+                if (vn[sl] > 0) drained = mbar_wait(bar_v_empty + 8 * sl, (vn[sl] - 1) & 1) && drained;
+            }
+            if (!drained) *s_abort = 1;
+        }
+    } else if (warp < kCtSoftmaxWarps) {
+        // ----------------------------------------------------------------- softmax
+        const int quad = warp & 3, hf = warp >> 2;
+        const int r = 32 * quad + lane;         // tile row == TMEM lane
+        const int hd = quad >> 1;               // head of the pair
+        const int i = r & (kCtTq - 1);          // query row of the chunk (padding when >= T)
+        const uint32_t tl = tmem + (static_cast<uint32_t>(32 * quad) << 16);
+        float* xm = reinterpret_cast<float*>(sm + SP::off_xm);   // [exchange parity][half][row]
+        const uint32_t pbar = bar_pair + 8 * quad;
+        int nx = 0;
+        auto pair_post = [&](float mine) {
+            xm[(nx & 1) * 256 + hf * 128 + r] = mine;
+            mbar_arrive(pbar);
+        };
+        auto pair_collect = [&](float& theirs) {
+            if (!warp_wait(pbar, nx & 1)) return false;
+            theirs = xm[(nx & 1) * 256 + (1 - hf) * 128 + r];
+            ++nx;
+            return true;
+        };
+        // bf16(q+u) and bf16(q+v) of item number itq (heads h0, h0+1): this thread's half row,
+        // from the q rows the producer staged; padding rows are zero.  The caller has made sure
+        // the MMAs of the previous item no longer read the tiles.
+        auto prep_q = [&](int itq, int h0) {
+            if (!warp_wait(bar_qb_full, itq & 1)) return false;
+            const uint4* up = reinterpret_cast<const uint4*>(a.pos_bias_u + (h0 + hd) * kHeadDim);
+            const uint4* vp = reinterpret_cast<const uint4*>(a.pos_bias_v + (h0 + hd) * kHeadDim);
+            const uint32_t dst_u = hd * SP::q_tile, dst_v = hd ? 2 * SP::q_tile : 0;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int c = 4 * hf + cc;
+                const uint32_t offs = swz128(i, c);
+                uint4 ou4 = make_uint4(0u, 0u, 0u, 0u), ov4 = ou4;
+                if (i < a.T) {
+                    const uint4 qc = *reinterpret_cast<const uint4*>(sm + SP::off_qbuf + hd * SP::q_tile + offs);
+                    const uint4 uc = __ldg(up + c);
+                    const uint4 vc = __ldg(vp + c);
+                    const uint32_t w[4] = {qc.x, qc.y, qc.z, qc.w};
+                    const uint32_t wu[4] = {uc.x, uc.y, uc.z, uc.w};
+                    const uint32_t wv[4] = {vc.x, vc.y, vc.z, vc.w};
+                    uint32_t ou[4], ov[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+                        ou[e] = pack_bf16(lo + __uint_as_float(wu[e] << 16), hi + __uint_as_float(wu[e] & 0xffff0000u));
+                        ov[e] = pack_bf16(lo + __uint_as_float(wv[e] << 16), hi + __uint_as_float(wv[e] & 0xffff0000u));
+                        ou[e] ^= a.sign;   // a negative scale: negate q+u and q+v (exact in bf16)
+                        ov[e] ^= a.sign;
+                    }
+                    ou4 = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+                    ov4 = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+                }
+                *reinterpret_cast<uint4*>(sm + SP::off_qu + dst_u + offs) = ou4;
+                *reinterpret_cast<uint4*>(sm + SP::off_qv + dst_v + offs) = ov4;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_qb_free);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_q_ready);
+            return true;
+        };
+        int g = 0, it = 0, sg = 0;
+        auto heads_of = [&](int k) {
+            const long long item = item_of(k);
+            const int b = static_cast<int>(item / Hp);
+            return 2 * static_cast<int>(item - static_cast<long long>(b) * Hp);
+        };
+        if (my_items > 0 && !prep_q(0, heads_of(0))) *s_abort = 1;
+        // O rows of a finished item: wait for its last P.V, combine the pair's sums, store.
+        // It runs inside the next item's first stage, after that stage's S/G have been read.
+        auto epilogue = [&](int e_b, int e_h0, float e_l) {
+            if (!warp_wait(bar_pv_done, (g - 1) & 1)) return false;
+            float l_other;
+            pair_post(e_l);
+            if (!pair_collect(l_other)) return false;
+            const float l_row = e_l + l_other;
+            tc_fence_after();
+            uint32_t oo[32];
+            OASR_TMEM_LD32(tl + kCtColO + 64 * hd + 32 * hf, oo);
+            tmem_wait_ld();
+            if (i < a.T) {
+                const float inv = 1.f / l_row;
+                uint4* dst = reinterpret_cast<uint4*>(
+                                 a.out + ((static_cast<long long>(e_b) * a.T + i) * a.H + e_h0 + hd) * kHeadDim) + 4 * hf;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    dst[c] = make_uint4(
+                        pack_bf16(__uint_as_float(oo[8 * c]) * inv, __uint_as_float(oo[8 * c + 1]) * inv),
+                        pack_bf16(__uint_as_float(oo[8 * c + 2]) * inv, __uint_as_float(oo[8 * c + 3]) * inv),
+                        pack_bf16(__uint_as_float(oo[8 * c + 4]) * inv, __uint_as_float(oo[8 * c + 5]) * inv),
+                        pack_bf16(__uint_as_float(oo[8 * c + 6]) * inv, __uint_as_float(oo[8 * c + 7]) * inv));
+            }
+            tc_fence_before();
+            return true;
+        };
+        // This warp's bf16 staging of the position term: row `lane` holds the 16-byte chunks
+        // q0 .. q0+4 of its window (q0 = w0 / 4, w0 = (31 - lane) / 2 the first word it reads)
+        // at 4 (5 lane + 2 (lane / 8)) words, so that both the chunk stores (the eight lanes of
+        // a store phase share q0 and land in distinct bank quads) and the lane-shifted 4-byte
+        // loads (32 distinct banks) are free of conflicts.
+        const int w0 = (31 - lane) >> 1;
+        const int q0 = w0 >> 2;
+        uint32_t* stg = reinterpret_cast<uint32_t*>(sm + SP::off_stg + warp * kCtStg) +
+                        4 * (5 * lane + 2 * (lane >> 3));
+        int p_b = 0, p_h0 = 0;
+        float p_l = 0.f;
+        bool have_prev = false, all_ok = true;
+        for (int k = 0; k < my_items && !*s_abort; ++k, ++it) {
+            const long long item = item_of(k);
+            const int b = static_cast<int>(item / Hp), h0 = 2 * static_cast<int>(item - static_cast<long long>(b) * Hp);
+            const int N = s_len[2 * k + 1];
+            const int n_st = (N + kCtBN - 1) / kCtBN;
+            float m_used = -INFINITY, l_sum = 0.f;
+            bool ok = true;
+            for (int s = 0; s < n_st; ++s, ++g) {
+                if (!warp_wait(bar_sg_full, sg & 1)) { ok = false; break; }
+                ++sg;
+                tc_fence_after();
+                // the half holds keys jh .. jh+31 of the stream; keys [0, kb) of it exist
+                const int jh = s * kCtBN + 32 * hf;
+                const int kb = N - jh;
+                float sc[32];
+                {
+                    // position term, skewed: row i needs G[r][63 - i + j] (j the key of the
+                    // stage); this warp's rows reach 63 columns for its half (window column
+                    // 31 - lane + j), which go through the staging tile as bf16 pairs
+                    uint32_t gr[64];
+                    const uint32_t colg = kCtColG + static_cast<uint32_t>(32 * hf + 32 - 32 * (quad & 1));
+                    OASR_TMEM_LD32(tl + colg, gr);
+                    OASR_TMEM_LD32(tl + colg + 32, (gr + 32));
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int pc = 0; pc < 8; ++pc)
+                        if (pc >= q0 && pc <= q0 + 4) {
+                            uint32_t gw[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                gw[e] = pack_bf16(__uint_as_float(gr[8 * pc + 2 * e]),
+                                                  __uint_as_float(gr[8 * pc + 2 * e + 1]));
+                            *reinterpret_cast<uint4*>(stg + 4 * (pc - q0)) = make_uint4(gw[0], gw[1], gw[2], gw[3]);
+                        }
+                    uint32_t sr[32];
+                    OASR_TMEM_LD32(tl + kCtColS + 64 * hd + 32 * hf, sr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) sc[j] = __uint_as_float(sr[j]);
+                }
+                // S and G are read: the issuer may compute the next stage's into the same columns
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_sg_free);
+                {
+                    // an even lane's window starts on the odd half of word w0: its pairs are
+                    // realigned with a byte permute
+                    const uint32_t sel = (lane & 1) ? 0x3210u : 0x5432u;
+                    const uint32_t* rd = stg + (w0 & 3);
+                    uint32_t wa = rd[0];
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
+                        const uint32_t wb = rd[m + 1];
+                        ct_add_bf16x2(sc[2 * m], sc[2 * m + 1], __byte_perm(wa, wb, sel));
+                        wa = wb;
+                    }
+                }
+                // last stage of the item: the next item's A tiles, so that its first S/G can be
+                // issued while this stage's softmax and the epilogue run
+                if (s + 1 == n_st && k + 1 < my_items) {
+                    if (!warp_wait(bar_q_free, it & 1) || !prep_q(it + 1, heads_of(k + 1))) { ok = false; break; }
+                }
+                // the previous item's O, now that this first stage's S/G are read
+                if (s == 0 && have_prev) {
+                    if (!epilogue(p_b, p_h0, p_l)) { ok = false; break; }
+                    have_prev = false;
+                }
+                // mask keys past the stream's history; this half's max (scores unscaled: the
+                // scale, > 0 with its sign folded into q+u and q+v, is applied to the row max
+                // and inside the exponent's FFMA)
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+                if (kb >= 32) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        mx0 = fmax3(mx0, sc[j], sc[j + 1]);
+                        mx1 = fmax3(mx1, sc[j + 2], sc[j + 3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sc[j + e] = j + e < kb ? sc[j + e] : -INFINITY;
+                        mx0 = fmax3(mx0, sc[j], sc[j + 1]);
+                        mx1 = fmax3(mx1, sc[j + 2], sc[j + 3]);
+                    }
+                }
+                float mx = fmaxf(mx0, mx1) * a.scale_log2, mx_other;
+                pair_post(mx);
+                // P.V of the previous stage must be done before P and O are touched
+                if (s > 0 && !warp_wait(bar_pv_done, (g - 1) & 1)) { ok = false; break; }
+                if (!pair_collect(mx_other)) { ok = false; break; }
+                mx = fmaxf(mx, mx_other);
+                const bool rescale = mx > m_used + 8.f;   // keeps every P <= 2^8 between rescales
+                const float m_new = rescale ? mx : m_used;
+                if (s > 0 && __any_sync(0xffffffffu, rescale)) {
+                    const float alpha = ex2_approx(m_used - m_new);
+                    l_sum *= alpha;
+                    tc_fence_after();
+                    uint32_t oo[32];
+                    OASR_TMEM_LD32(tl + kCtColO + 64 * hd + 32 * hf, oo);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) oo[j] = __float_as_uint(__uint_as_float(oo[j]) * alpha);
+                    OASR_TMEM_ST32(tl + kCtColO + 64 * hd + 32 * hf, oo);
+                }
+                m_used = m_new;
+                // every row has seen a key by now (the stage's first key exists), so m_used is finite
+                {
+                    float2 ps = make_float2(0.f, 0.f);
+                    const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+                    const float2 nm2 = make_float2(-m_used, -m_used);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float2 e2 = __ffma2_rn(make_float2(sc[2 * j], sc[2 * j + 1]), sc2, nm2);
+                        const float2 p2 = make_float2(ex2_approx(e2.x), ex2_approx(e2.y));
+                        ps = __fadd2_rn(ps, p2);
+                        pk[j] = pack_bf16(p2.x, p2.y);
+                    }
+                    OASR_TMEM_ST16(tl + kCtColP + 16 * hf, pk);
+                    l_sum += ps.x + ps.y;
+                }
+                // V rows past the history: P.V stops at the 16-key step holding the last key;
+                // that step's rows past it (stale pool rows, possibly non-finite) are zeroed so
+                // that P = 0 there never meets a non-finite value.  Rows 0-63 of the tile are the
+                // stage's keys: warps of quadrants 0 and 1 zero them in head hf's V tile.
+                const int kstage = N - s * kCtBN;
+                const int k16 = (kstage + 15) & ~15;
+                if (kstage < k16 && quad < 2 && 32 * quad < k16 && 32 * quad + 32 > kstage) {
+                    if (!warp_wait(bar_vfull + 8 * (g & 1), (g >> 1) & 1)) { ok = false; break; }
+                    if (r >= kstage && r < k16) {
+                        uint4* vrow = reinterpret_cast<uint4*>(sm + SP::off_slot + (g & 1) * SP::slot + SP::off_v +
+                                                               hf * SP::head_k + r * kRowBytes);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) vrow[c] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_p_full);
+            }
+            if (!ok) { all_ok = false; break; }
+            p_b = b;
+            p_h0 = h0;
+            p_l = l_sum;
+            have_prev = true;
+        }
+        if (all_ok && have_prev && !*s_abort) epilogue(p_b, p_h0, p_l);
+    }
+    grid_dep_trigger();
+    // every role has stopped issuing and the MMA issuer has drained the tensor pipe
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCtTmemCols));
+    }
+    if (tid == 0 && *s_abort) err |= kErrTimeout;
+    if (err) atomicOr(a.status, err);
+}
+
+int g_smem_done_ct[64];
+
+}  // namespace
+
+// Whether the tensor-core kernel takes a bf16 streaming call of this shape: 33 <= T <= 64, an
+// even head count, and coordinates and per-CTA work items within its limits.
+bool chunk_tc_takes(int B, int T, int H, int mbps, int num_blocks, int block_size, int R)
+{
+    if (T < 33 || T > kCtTq || (H & 1) || mbps > kCtMaxPages) return false;
+    if (static_cast<long long>(num_blocks) * block_size + kCtBN >= 0x7fffffffLL ||
+        static_cast<long long>(B) * T + kCtTq >= 0x7fffffffLL ||
+        static_cast<long long>(R) + kCtBand >= 0x7fffffffLL)
+        return false;
+    const int sms = sm_count();
+    if (!sms) return false;
+    const long long n_items = static_cast<long long>(B) * (H / 2);
+    const long long grid = n_items < sms ? n_items : sms;
+    return (n_items + grid - 1) / grid <= kCtMaxItems;
+}
+
+// Host launcher used by the streaming entry points for the shapes chunk_tc_takes accepts
+// (bf16; the caller has validated the arguments).
+oasr_status launch_chunk_tc(const void* q, const void* k_pool, const void* v_pool, int num_blocks,
+                            int block_size, const int32_t* bt, int mbps, const int32_t* cs,
+                            const void* u, const void* vb, const void* rel, int R, void* out,
+                            int B, int T, int H, int k_max, float scale, cudaStream_t stream)
+{
+    if (!chunk_tc_takes(B, T, H, mbps, num_blocks, block_size, R)) return OASR_ERR_UNSUPPORTED;
+    const int sms = sm_count();
+    const long long n_items = static_cast<long long>(B) * (H / 2);
+    const int grid = static_cast<int>(n_items < sms ? n_items : sms);
+    const int box = block_size < kCtBN ? block_size : kCtBN;
+    CUtensorMap tm_q, tm_k, tm_v, tm_r;
+    if (!encode_rows_bf16(&tm_q, q, static_cast<long long>(B) * T, H, kCtTq) ||
+        !encode_rows_bf16(&tm_k, k_pool, static_cast<long long>(num_blocks) * block_size, H, box) ||
+        !encode_rows_bf16(&tm_v, v_pool, static_cast<long long>(num_blocks) * block_size, H, box) ||
+        !encode_rows_bf16(&tm_r, rel, R, H, kCtBand))
+        return OASR_ERR_INVALID_ARG;
+    unsigned* status = status_word();
+    if (!status) return OASR_ERR_CUDA;
+    constexpr int smem = CtSmem::bytes;
+    if (!ensure_smem(chunk_attn_tc_kernel, smem, g_smem_done_ct)) return OASR_ERR_CUDA;
+    CtArgs a;
+    a.block_table = bt;
+    a.cache_seqlens = cs;
+    a.pos_bias_u = static_cast<const uint16_t*>(u);
+    a.pos_bias_v = static_cast<const uint16_t*>(vb);
+    a.out = static_cast<uint16_t*>(out);
+    a.status = status;
+    a.B = B;
+    a.T = T;
+    a.H = H;
+    a.R = R;
+    a.num_blocks = num_blocks;
+    a.block_size = block_size;
+    a.bs_shift = __builtin_ctz(static_cast<unsigned>(block_size));
+    a.box_rows = box;
+    a.mbps = mbps;
+    a.k_max = k_max;
+    a.sign = scale < 0.f ? 0x80008000u : 0u;
+    // > 0 even for a zero scale, so that a masked score (-inf) times it stays -inf
+    a.scale_log2 = fmaxf(fabsf(scale) * 1.4426950408889634f, 1e-30f);
+    return launch_pdl(chunk_attn_tc_kernel, dim3(grid), dim3(kCtThreads), smem, stream, tm_q, tm_k,
+                      tm_v, tm_r, a);
+}
+
+}  // namespace oasr

@@ -19,6 +19,14 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr)
            (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The same with a leading byte offset: for an MN-major operand wider than one 64-element
+// swizzle atom, the distance between its atoms along N.
+__device__ __forceinline__ uint64_t sdesc_lbo(uint32_t addr, uint32_t lbo)
+{
+    return static_cast<uint64_t>((addr >> 4) & 0x3FFF) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M x N, B MN-major if b_mn.
 __host__ __device__ constexpr uint32_t idesc(int M, int N, int b_mn)
 {
