@@ -79,6 +79,23 @@ bool encode_rows_bf16(CUtensorMap* map, const void* base, long long rows, int H,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_head_pairs_bf16(CUtensorMap* map, const void* base, long long rows, int H, int box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || rows < 8 || (rows & 7) || H < 2 || box_rows < 8 || box_rows > 256 || (box_rows & 7) ||
+        !aligned16(base))
+        return false;
+    const cuuint64_t dims[4] = {64, 8, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows / 8)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(H) * 64 * 2, 64 * 2,
+                                   static_cast<cuuint64_t>(H) * 64 * 2 * 8};
+    const cuuint32_t box[4] = {64, 8, 2, static_cast<cuuint32_t>(box_rows / 8)};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 // A wait on a barrier that no thread or copy ever signals: it runs out after limit_ns and
 // takes the path every pipeline wait of the library takes when it runs out.

@@ -13,17 +13,19 @@
 // for head h0 and lanes 64-127 for head h0 + 1 (rows T..63 of each half are padding).  A
 // tcgen05.mma of M128 K16 costs about the same up to N = 128, so each product spans both heads
 // at N = 128 and each row keeps the half that belongs to its head.  Per stage of 64 keys:
-//   S [128 x 128] = bf16(q+u) . [K_h0 ; K_h1]^T          columns [0, 128)    M128 N128; rows of
-//                   head h0 keep columns 0-63 (its keys), rows of h0 + 1 columns 64-127
+//   S [128 x 128] = bf16(q+u) . Kpair^T                  columns [0, 128)    M128 N128; Kpair holds
+//                   the stage's keys of both heads in groups of 8 (column 16 (j / 8) + 8 hd +
+//                   j % 8 is key j of head hd), and each row keeps its own head's columns
 //   G [128 x 128] = A0 . Band_h0^T + A1 . Band_h1^T      columns [128, 256)  M128 N128, block-
 //                   diagonal: A0 = [bf16(q+v) of h0 ; 0], A1 = [0 ; bf16(q+v) of h0+1] (one 8 KB
 //                   zero block shared between them); the band is the 128 rel rows rho_min ..
 //                   rho_min + 127 the stage reaches (rho_min = R - T - C - 63 + 64 s), and row i,
 //                   key j of the stage uses band row 63 - i + j
-//   O [128 x 128] += P . [V_h0 | V_h1]                   columns [256, 384)  M128 N128; rows of
-//                   head h0 keep columns 0-63, rows of h0 + 1 columns 64-127
+//   O [128 x 128] += P . [V_h0 | V_h1]                   columns [256, 384)  M128 N128 (V of both
+//                   heads as one MN-major operand); rows of head h0 keep columns 0-63, rows of
+//                   h0 + 1 columns 64-127
 //   P [128 x 64] bf16                                    columns [384, 416)
-// Warp roles (352 threads), one persistent CTA per SM walking work items:
+// Warp roles (416 threads), one persistent CTA per SM walking work items:
 //   warps 0-7  softmax.  Warps w and w+4 share TMEM lane quadrant w (rows 32w .. 32w+31); warp
 //              w takes keys 0-31 of each stage, w+4 keys 32-63, and the pair swaps row maxima
 //              and sums through shared memory.  Each thread reads its S half row and the G
@@ -32,11 +34,20 @@
 //              the stream's history, keeps the running max (O is rescaled in TMEM only when
 //              the max grows by more than 2^8) and sum, and writes its half row of bf16 P to
 //              TMEM; at the end of the item it normalises and stores its half of the O row.
-//   warp 8     MMA issuer (one thread).
-//   warp 9     TMA producer of the q rows and of the stage's K page boxes and rel band.
+//   warp 8     S/G issuer (one thread).
+//   warp 9     TMA producer of the q rows and of the stage's K page boxes.
 //   warp 10    TMA producer of the stage's V page boxes.
-// K and V arrive as one box per block-table page and head (as in the pool: a page's rows of
-// one head, 128 B each, 128-byte swizzled); a block id outside the pool reads as zero rows.
+//   warp 11    TMA producer of the stage's rel band.
+//   warp 12    P.V issuer (one thread).
+// K and V (read from HBM) run through three-slot rings, a slot's K refilled as soon as the S
+// and G products that read it have finished and its V once its P.V has; the band (rel rows,
+// resident in L2) runs through a two-slot ring, because the softmax warps stage the skewed
+// position term in the band tile of the stage they process (free once G is computed) and
+// release it when their skewed reads are done.
+// K and V arrive as one box per block-table page holding both heads (the pool viewed as
+// {64, key % 8, head, key / 8}, so that each head's 8 consecutive keys form one 128-byte-
+// swizzled 1 KB atom; one box per page instead of one per page and head halves the copies the
+// SM's TMA unit issues); a block id outside the pool reads as zero rows.
 // Every wait is bounded; a wait that runs out raises the timeout bit and aborts the CTA's
 // remaining work, after which the CTA still drains its copies and tensor-core work and frees
 // its TMEM.
@@ -49,8 +60,10 @@ namespace oasr {
 namespace {
 
 constexpr int kCtSoftmaxWarps = 8;
-constexpr int kCtThreads = 32 * (kCtSoftmaxWarps + 3);
-constexpr int kCtMmaWarp = 8, kCtKWarp = 9, kCtVWarp = 10;
+constexpr int kCtThreads = 32 * (kCtSoftmaxWarps + 5);
+constexpr int kCtMmaWarp = 8, kCtKWarp = 9, kCtVWarp = 10, kCtBandWarp = 11, kCtPvWarp = 12;
+constexpr int kKvSlots = 3;               // depth of the K and V rings
+constexpr int kBandSlots = 2;             // depth of the band ring
 constexpr int kCtBN = 64;                 // keys per stage
 constexpr int kCtBand = 128;              // band rows per stage and head
 constexpr int kCtTq = 64;                 // query rows of one head in the tile
@@ -61,31 +74,31 @@ constexpr int kCtMaxPages = 512;          // block-table entries a producer cach
 constexpr int kCtMaxItems = 256;          // work items of one CTA whose lengths are cached
 
 struct CtSmem {
-    static constexpr int head_k = kCtBN * kRowBytes;              // 8 KB: 64 keys of one head
+    static constexpr int kv_tile = 2 * kCtBN * kRowBytes;         // 16 KB: [key / 8][head][key % 8][64]
     static constexpr int head_band = kCtBand * kRowBytes;         // 16 KB
-    static constexpr int off_k = 0;                               // K h0 | K h1
-    static constexpr int off_band = 2 * head_k;                   // band h0 | band h1
-    static constexpr int off_v = off_band + 2 * head_band;        // V h0 | V h1
-    static constexpr int slot = off_v + 2 * head_k;               // 64 KB
-    static constexpr int off_slot = 0;                            // 2 slots
+    static constexpr int band_tile = 2 * head_band;               // band h0 | band h1
+    static constexpr int off_k = 0;                               // kKvSlots K tiles
+    static constexpr int off_v = off_k + kKvSlots * kv_tile;      // kKvSlots V tiles
+    static constexpr int off_band = off_v + kKvSlots * kv_tile;   // kBandSlots band tiles
+    static_assert(kCtSoftmaxWarps * kCtStg <= band_tile, "staging overlays a band tile");
     static constexpr int q_tile = kCtTq * kRowBytes;              // 8 KB: 64 rows of one head
     // bf16(q+u): one tile [h0 rows | h0+1 rows]; bf16(q+v): [h0 rows | zero | h0+1 rows], A0
     // starting at 0 and A1 at q_tile
-    static constexpr int off_qu = 2 * slot;
+    static constexpr int off_qu = off_band + kBandSlots * band_tile;
     static constexpr int off_qv = off_qu + 2 * q_tile;
     static constexpr int off_qbuf = off_qv + 3 * q_tile;          // next item's q rows (TMA), 2 heads
-    static constexpr int off_stg = off_qbuf + 2 * q_tile;
-    static constexpr int off_xm = off_stg + kCtSoftmaxWarps * kCtStg;   // [parity][half][row]
+    static constexpr int off_xm = off_qbuf + 2 * q_tile;          // [parity][half][row]
     static constexpr int off_btk = off_xm + 2 * 2 * 128 * 4;
     static constexpr int off_btv = off_btk + kCtMaxPages * 4;
     static constexpr int off_len = off_btv + kCtMaxPages * 4;     // per item: C, N
     static constexpr int off_misc = off_len + 2 * kCtMaxItems * 4;   // tmem, abort
     static constexpr int off_bar = off_misc + 64;
-    static constexpr int n_bars = 2 + 2 + 2 + 2 + 9 + 4;
+    static constexpr int n_bars = 4 * kKvSlots + 2 * kBandSlots + 10 + 4;
     static constexpr int bytes = off_bar + n_bars * 8 + 1024;
     static_assert(bytes <= 232448, "dynamic shared memory of one CTA");
-    static_assert(slot % 1024 == 0 && off_qu % 1024 == 0 && off_qv % 1024 == 0 &&
-                  off_qbuf % 1024 == 0, "TMA and MMA tiles need 1024-byte alignment");
+    static_assert(kv_tile % 1024 == 0 && off_band % 1024 == 0 && off_qu % 1024 == 0 &&
+                  off_qv % 1024 == 0 && off_qbuf % 1024 == 0,
+                  "TMA and MMA tiles need 1024-byte alignment");
 };
 
 struct CtArgs {
@@ -126,18 +139,21 @@ __global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
     int* s_len = reinterpret_cast<int*>(sm + SP::off_len);        // [item] C, then N
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + SP::off_misc);
     volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SP::off_misc + 4);
-    const uint32_t bar_full = sb + SP::off_bar;        // [2] the stage's K and band landed
-    const uint32_t bar_vfull = bar_full + 16;          // [2] the stage's V landed
-    const uint32_t bar_kb_empty = bar_vfull + 16;      // [2] the slot's K and band read (S/G done)
-    const uint32_t bar_v_empty = bar_kb_empty + 16;    // [2] the slot's V read (P.V done)
-    const uint32_t bar_sg_full = bar_v_empty + 16;     // S and G in TMEM
+    const uint32_t bar_kfull = sb + SP::off_bar;             // [3] the stage's K landed
+    const uint32_t bar_kempty = bar_kfull + 8 * kKvSlots;    // [3] the slot's K read (S/G done)
+    const uint32_t bar_vfull = bar_kempty + 8 * kKvSlots;    // [3] the stage's V landed
+    const uint32_t bar_vempty = bar_vfull + 8 * kKvSlots;    // [3] the slot's V read (P.V done)
+    const uint32_t bar_bfull = bar_vempty + 8 * kKvSlots;    // [2] the stage's band landed
+    const uint32_t bar_bempty = bar_bfull + 8 * kBandSlots;  // [2] the band tile (and staging) free
+    const uint32_t bar_sg_full = bar_bempty + 8 * kBandSlots;  // S and G in TMEM
     const uint32_t bar_sg_free = bar_sg_full + 8;      // softmax warps have read S and G
     const uint32_t bar_p_full = bar_sg_free + 8;       // P written to TMEM
     const uint32_t bar_pv_done = bar_p_full + 8;       // P.V finished
     const uint32_t bar_q_ready = bar_pv_done + 8;      // bf16(q+u), bf16(q+v) written
     const uint32_t bar_q_free = bar_q_ready + 8;       // last S/G MMA of an item finished
-    const uint32_t bar_drain = bar_q_free + 8;         // everything the MMA issuer issued finished
-    const uint32_t bar_qb_full = bar_drain + 8;        // q rows of the next item landed
+    const uint32_t bar_drain = bar_q_free + 8;         // everything the S/G issuer issued finished
+    const uint32_t bar_drain2 = bar_drain + 8;         // everything the P.V issuer issued finished
+    const uint32_t bar_qb_full = bar_drain2 + 8;       // q rows of the next item landed
     const uint32_t bar_qb_free = bar_qb_full + 8;      // softmax warps have read the q rows
     const uint32_t bar_pair = bar_qb_free + 8;         // [4] softmax warp pair exchanged a value
     const int Hp = a.H >> 1;
@@ -149,15 +165,19 @@ __global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
     if (warp == kCtKWarp && lane == 0) {
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_r);
     }
     if (warp == kCtVWarp && lane == 0) prefetch_tensormap(&tm_v);
+    if (warp == kCtBandWarp && lane == 0) prefetch_tensormap(&tm_r);
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_full + 8 * i, 1);
+        for (int i = 0; i < kKvSlots; ++i) {
+            mbar_init(bar_kfull + 8 * i, 1);
+            mbar_init(bar_kempty + 8 * i, 1);
             mbar_init(bar_vfull + 8 * i, 1);
-            mbar_init(bar_kb_empty + 8 * i, 1);
-            mbar_init(bar_v_empty + 8 * i, 1);
+            mbar_init(bar_vempty + 8 * i, 1);
+        }
+        for (int i = 0; i < kBandSlots; ++i) {
+            mbar_init(bar_bfull + 8 * i, 1);
+            mbar_init(bar_bempty + 8 * i, kCtSoftmaxWarps);
         }
         mbar_init(bar_sg_full, 1);
         mbar_init(bar_sg_free, kCtSoftmaxWarps);
@@ -166,6 +186,7 @@ __global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
         mbar_init(bar_q_ready, kCtSoftmaxWarps);
         mbar_init(bar_q_free, 1);
         mbar_init(bar_drain, 1);
+        mbar_init(bar_drain2, 1);
         mbar_init(bar_qb_full, 1);
         mbar_init(bar_qb_free, kCtSoftmaxWarps);
         for (int i = 0; i < 4; ++i) mbar_init(bar_pair + 8 * i, 64);
@@ -202,18 +223,9 @@ __global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    // The producers poll with a pause between tries, so that their warps take few issue
-    // slots from the softmax warps sharing their schedulers.
-    auto prod_wait = [&](uint32_t bar, uint32_t parity) {
-        if (mbar_try_wait(bar, parity)) return true;
-        const uint64_t t0 = global_timer_ns();
-        for (;;) {
-            __nanosleep(128);
-            if (mbar_try_wait(bar, parity)) return true;
-            if (*s_abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) { *s_abort = 1; return false; }
-        }
-    };
+    // The producers wait on the barrier itself (suspended until its phase completes), so that
+    // they react at once and take no issue slots from the softmax warps meanwhile.
+    auto prod_wait = [&](uint32_t bar, uint32_t parity) { return wait_or_abort(bar, parity, s_abort); };
     // Softmax warps take every wait together: a warp-wide vote keeps the warp converged for
     // the .sync.aligned tensor-memory instructions even if one lane's wait runs out.
     auto warp_wait = [&](uint32_t bar, uint32_t parity) {
@@ -221,16 +233,15 @@ __global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
     };
     auto item_of = [&](int k) { return blockIdx.x + static_cast<long long>(k) * gridDim.x; };
 
-    // One producer warp's page boxes of a stage: box q of the stage (one page of one head)
-    // goes from lane q.  Returns the bytes the stage's boxes bring.
+    // One producer warp's page boxes of a stage: box q (one page, both heads) goes from lane q.
+    // Returns the bytes the stage's boxes bring.
     auto page_boxes = [&](const CUtensorMap* map, const int* bt_row, int s, int N, int h0,
                           uint32_t dst0, uint32_t bar, uint64_t pol, bool issue) {
         const int j0 = s * kCtBN;
         const int jn = N - j0 < kCtBN ? N - j0 : kCtBN;
         const int nbox = a.box_rows == kCtBN ? 1 : (jn + a.box_rows - 1) >> a.bs_shift;
-        if (issue && lane < 2 * nbox) {
-            const int idx = lane >> 1, hd = lane & 1;
-            const int key = j0 + idx * a.box_rows;                // first key of the box
+        if (issue && lane < nbox) {
+            const int key = j0 + lane * a.box_rows;               // first key of the box
             const int blk = bt_row[key >> a.bs_shift];
             int row;
             if (blk >= 0 && blk < a.num_blocks) {
@@ -239,10 +250,9 @@ __global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
                 err |= kErrBounds;
                 row = a.num_blocks << a.bs_shift;                 // past the pool: zero rows
             }
-            tma_load_3d_hint(dst0 + hd * SP::head_k + idx * a.box_rows * kRowBytes, map, bar, 0,
-                             h0 + hd, row, pol);
+            tma_load_4d_hint(dst0 + lane * a.box_rows * 2 * kRowBytes, map, bar, 0, 0, h0, row >> 3, pol);
         }
-        return 2 * nbox * a.box_rows * kRowBytes;
+        return nbox * a.box_rows * 2 * kRowBytes;
     };
     // the block-table row of stream b, pages [0, ceil(N / block_size)), into a producer's cache
     auto load_bt = [&](int* bt_row, int b, int N) {
@@ -253,7 +263,7 @@ __global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
     };
 
     if (warp == kCtKWarp) {
-        // ------------------------------------------------ q rows, K and band producer
+        // --------------------------------------------------------- q rows and K producer
         int* bt_row = reinterpret_cast<int*>(sm + SP::off_btk);
         const uint64_t pol = policy_evict_first();   // every K and V row is read once
         int g = 0, itp = 0;
@@ -261,7 +271,7 @@ __global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
         for (int k = 0; k < my_items && ok; ++k, ++itp) {
             const long long item = item_of(k);
             const int b = static_cast<int>(item / Hp), h0 = 2 * static_cast<int>(item - static_cast<long long>(b) * Hp);
-            const int C = s_len[2 * k], N = s_len[2 * k + 1];
+            const int N = s_len[2 * k + 1];
             const int n_st = (N + kCtBN - 1) / kCtBN;
             load_bt(bt_row, b, N);
             // the item's q rows of both heads, once the softmax warps have read the previous ones
@@ -275,28 +285,22 @@ __global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             for (int s = 0; s < n_st && ok; ++s, ++g) {
-                const int slot = g & 1;
-                if (lane == 0 && g >= 2 && !prod_wait(bar_kb_empty + 8 * slot, ((g >> 1) - 1) & 1)) ok = false;
+                const int u = g % kKvSlots, n = g / kKvSlots;
+                if (lane == 0 && n > 0 && !prod_wait(bar_kempty + 8 * u, (n - 1) & 1)) ok = false;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
-                const uint32_t base = sb + SP::off_slot + slot * SP::slot;
-                const uint32_t bar = bar_full + 8 * slot;
-                const int kbytes = page_boxes(&tm_k, bt_row, s, N, h0, base + SP::off_k, bar, pol, false);
-                if (lane == 0) mbar_arrive_expect_tx(bar, kbytes + 2 * SP::head_band);
+                const uint32_t dst = sb + SP::off_k + u * SP::kv_tile;
+                const uint32_t bar = bar_kfull + 8 * u;
+                const int kbytes = page_boxes(&tm_k, bt_row, s, N, h0, dst, bar, pol, false);
+                if (lane == 0) mbar_arrive_expect_tx(bar, kbytes);
                 __syncwarp();
-                page_boxes(&tm_k, bt_row, s, N, h0, base + SP::off_k, bar, pol, true);
-                // the band: rel rows rho_min .. rho_min + 127 of both heads (rows outside the
-                // table read as zeros)
-                if (lane < 2) {
-                    const int rho_min = a.R - a.T - C - (kCtTq - 1) + s * kCtBN;
-                    tma_load_3d(base + SP::off_band + lane * SP::head_band, &tm_r, bar, 0, h0 + lane, rho_min);
-                }
+                page_boxes(&tm_k, bt_row, s, N, h0, dst, bar, pol, true);
             }
         }
         // no copy may still be landing when the CTA exits
         if (lane == 0) {
-            for (int u = g - 2; u < g; ++u)
-                if (u >= 0 && !mbar_wait(bar_full + 8 * (u & 1), (u >> 1) & 1)) *s_abort = 1;
+            for (int x = g - kKvSlots; x < g; ++x)
+                if (x >= 0 && !mbar_wait(bar_kfull + 8 * (x % kKvSlots), (x / kKvSlots) & 1)) *s_abort = 1;
             if (itp > 0 && !mbar_wait(bar_qb_full, (itp - 1) & 1)) *s_abort = 1;
         }
     } else if (warp == kCtVWarp) {
@@ -312,12 +316,12 @@ __global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
             const int n_st = (N + kCtBN - 1) / kCtBN;
             load_bt(bt_row, b, N);
             for (int s = 0; s < n_st && ok; ++s, ++g) {
-                const int slot = g & 1;
-                if (lane == 0 && g >= 2 && !prod_wait(bar_v_empty + 8 * slot, ((g >> 1) - 1) & 1)) ok = false;
+                const int u = g % kKvSlots, n = g / kKvSlots;
+                if (lane == 0 && n > 0 && !prod_wait(bar_vempty + 8 * u, (n - 1) & 1)) ok = false;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
-                const uint32_t dst = sb + SP::off_slot + slot * SP::slot + SP::off_v;
-                const uint32_t bar = bar_vfull + 8 * slot;
+                const uint32_t dst = sb + SP::off_v + u * SP::kv_tile;
+                const uint32_t bar = bar_vfull + 8 * u;
                 const int vbytes = page_boxes(&tm_v, bt_row, s, N, h0, dst, bar, pol, false);
                 if (lane == 0) mbar_arrive_expect_tx(bar, vbytes);
                 __syncwarp();
@@ -325,103 +329,111 @@ __global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
             }
         }
         if (lane == 0)
-            for (int u = g - 2; u < g; ++u)
-                if (u >= 0 && !mbar_wait(bar_vfull + 8 * (u & 1), (u >> 1) & 1)) *s_abort = 1;
-    } else if (warp == kCtMmaWarp) {
-        // ------------------------------------------------------------- MMA issuer
+            for (int x = g - kKvSlots; x < g; ++x)
+                if (x >= 0 && !mbar_wait(bar_vfull + 8 * (x % kKvSlots), (x / kKvSlots) & 1)) *s_abort = 1;
+    } else if (warp == kCtBandWarp) {
+        // ------------------------------------------------------------- band producer
         if (lane == 0) {
-            constexpr uint32_t id_s = idesc(128, 2 * kCtBN, 0), id_g = idesc(128, kCtBand, 0),
-                               id_o = idesc(128, 128, 1);
-            int g = 0, it = 0, sg = 0, nq = 0, npv = 0;
-            int kbn[2] = {0, 0}, vn[2] = {0, 0};
-            auto issue_sg = [&](int slot) {
-                const uint32_t base = sb + SP::off_slot + slot * SP::slot;
-                tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    umma_ss(tmem + kCtColS, sdesc(sb + SP::off_qu + 32 * k), sdesc(base + SP::off_k + 32 * k),
-                            id_s, k > 0);
-#pragma unroll
-                for (int hd = 0; hd < 2; ++hd)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        umma_ss(tmem + kCtColG, sdesc(sb + SP::off_qv + hd * SP::q_tile + 32 * k),
-                                sdesc(base + SP::off_band + hd * SP::head_band + 32 * k), id_g,
-                                (hd | k) ? 1 : 0);
-                umma_commit(bar_sg_full);
-                umma_commit(bar_kb_empty + 8 * slot);   // the slot's K and band may be refilled
-                ++kbn[slot];
-                ++sg;
-            };
-            // One flat walk over the CTA's stages: S and G of the next stage (possibly the next
-            // item's first) as soon as this stage's S and G have been read, then P.V of this one.
-            int k_item = 0, n_st = 0, s = 0, n_keys = 0;
-            auto item_stages = [&](int k, int& keys) {
-                keys = s_len[2 * k + 1];
-                return (keys + kCtBN - 1) / kCtBN;
-            };
-            bool ok = my_items > 0;
-            if (ok) {
-                n_st = item_stages(0, n_keys);
-                ok = wait_or_abort(bar_q_ready, 0, s_abort) && wait_or_abort(bar_full, 0, s_abort);
-                if (ok) {
-                    issue_sg(0);
-                    if (n_st == 1) { umma_commit(bar_q_free); ++nq; }
+            int g = 0;
+            bool ok = true;
+            for (int k = 0; k < my_items && ok; ++k) {
+                const long long item = item_of(k);
+                const int b = static_cast<int>(item / Hp), h0 = 2 * static_cast<int>(item - static_cast<long long>(b) * Hp);
+                const int C = s_len[2 * k], N = s_len[2 * k + 1];
+                const int n_st = (N + kCtBN - 1) / kCtBN;
+                for (int s = 0; s < n_st; ++s, ++g) {
+                    const int slot = g & 1;
+                    if (g >= kBandSlots && !prod_wait(bar_bempty + 8 * slot, ((g >> 1) - 1) & 1)) { ok = false; break; }
+                    // rel rows rho_min .. rho_min + 127 of both heads (rows outside the table
+                    // read as zeros)
+                    const int rho_min = a.R - a.T - C - (kCtTq - 1) + s * kCtBN;
+                    const uint32_t dst = sb + SP::off_band + slot * SP::band_tile;
+                    mbar_arrive_expect_tx(bar_bfull + 8 * slot, SP::band_tile);
+                    tma_load_3d(dst, &tm_r, bar_bfull + 8 * slot, 0, h0, rho_min);
+                    tma_load_3d(dst + SP::head_band, &tm_r, bar_bfull + 8 * slot, 0, h0 + 1, rho_min);
                 }
             }
-            while (ok) {
-                const bool last = s + 1 == n_st;
-                const int next_k = last ? k_item + 1 : k_item;
-                if (next_k < my_items) {
-                    int next_keys = 0;
-                    const int next_n = last ? item_stages(next_k, next_keys) : n_st;
-                    const int next_s = last ? 0 : s + 1;
-                    ok = (!last || wait_or_abort(bar_q_ready, (it + 1) & 1, s_abort)) &&
-                         wait_or_abort(bar_full + 8 * ((g + 1) & 1), ((g + 1) >> 1) & 1, s_abort) &&
-                         wait_or_abort(bar_sg_free, (sg - 1) & 1, s_abort);
+            for (int x = g - kBandSlots; x < g; ++x)
+                if (x >= 0 && !mbar_wait(bar_bfull + 8 * (x & 1), (x >> 1) & 1)) *s_abort = 1;
+        }
+    } else if (warp == kCtMmaWarp) {
+        // ------------------------------------------------------------ S/G issuer
+        // Each tcgen05.mma holds its issuing thread until the tensor pipe takes it, so S/G and
+        // P.V are issued from two threads: while one waits on a barrier the other's products run.
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc(128, 2 * kCtBN, 0), id_g = idesc(128, kCtBand, 0);
+            int x = 0, nq = 0;   // stages issued
+            bool ok = true;
+            for (int k = 0; k < my_items && ok; ++k) {
+                const int n_st = (s_len[2 * k + 1] + kCtBN - 1) / kCtBN;
+                for (int s = 0; s < n_st; ++s, ++x) {
+                    // the item's A tiles (first stage), the stage's K and band, and the previous
+                    // stage's S and G read by the softmax warps
+                    ok = (s > 0 || wait_or_abort(bar_q_ready, k & 1, s_abort)) &&
+                         wait_or_abort(bar_kfull + 8 * (x % kKvSlots), (x / kKvSlots) & 1, s_abort) &&
+                         wait_or_abort(bar_bfull + 8 * (x & 1), (x >> 1) & 1, s_abort) &&
+                         (x == 0 || wait_or_abort(bar_sg_free, (x - 1) & 1, s_abort));
                     if (!ok) break;
-                    issue_sg((g + 1) & 1);
-                    if (next_s + 1 == next_n) { umma_commit(bar_q_free); ++nq; }
-                }
-                // P.V of stage g, only over the 16-key steps that hold keys of the stream
-                ok = wait_or_abort(bar_p_full, g & 1, s_abort) &&
-                     wait_or_abort(bar_vfull + 8 * (g & 1), (g >> 1) & 1, s_abort);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t vbase = sb + SP::off_slot + (g & 1) * SP::slot + SP::off_v;
-                const int kst = n_keys - s * kCtBN;
-                const int ksteps = kst < kCtBN ? (kst + 15) >> 4 : kCtBN / 16;
-                // B = [V_h0 | V_h1]: MN-major, the second head's 64 columns one tile (8 KB) on
+                    const uint32_t kbase = sb + SP::off_k + (x % kKvSlots) * SP::kv_tile;
+                    const uint32_t bbase = sb + SP::off_band + (x & 1) * SP::band_tile;
+                    tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < kCtBN / 16; ++k)
-                    if (k < ksteps)
-                        umma_ts(tmem + kCtColO, tmem + kCtColP + 8 * k, sdesc_lbo(vbase + 2048 * k, SP::head_k),
-                                id_o, (s > 0 || k > 0) ? 1 : 0);
-                umma_commit(bar_pv_done);
-                umma_commit(bar_v_empty + 8 * (g & 1));
-                ++vn[g & 1];
-                ++npv;
-                ++g;
-                if (!last) {
-                    ++s;
-                } else {
-                    k_item = next_k;
-                    ++it;
-                    if (k_item >= my_items) break;
-                    n_st = item_stages(k_item, n_keys);
-                    s = 0;
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_ss(tmem + kCtColS, sdesc(sb + SP::off_qu + 32 * kk), sdesc(kbase + 32 * kk), id_s, kk > 0);
+#pragma unroll
+                    for (int hd = 0; hd < 2; ++hd)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma_ss(tmem + kCtColG, sdesc(sb + SP::off_qv + hd * SP::q_tile + 32 * kk),
+                                    sdesc(bbase + hd * SP::head_band + 32 * kk), id_g, (hd | kk) ? 1 : 0);
+                    umma_commit(bar_sg_full);
+                    umma_commit(bar_kempty + 8 * (x % kKvSlots));   // the slot's K may be refilled
+                    if (s + 1 == n_st) { umma_commit(bar_q_free); ++nq; }   // the A tiles are free
                 }
             }
-            // drain: every MMA issued has finished and every arrival it owes has landed
+            // drain: every product issued here has finished and every arrival it owes has landed
             umma_commit(bar_drain);
             bool drained = mbar_wait(bar_drain, 0);
             if (nq > 0) drained = mbar_wait(bar_q_free, (nq - 1) & 1) && drained;
-            if (sg > 0) drained = mbar_wait(bar_sg_full, (sg - 1) & 1) && drained;
-            if (npv > 0) drained = mbar_wait(bar_pv_done, (npv - 1) & 1) && drained;
-            for (int sl = 0; sl < 2; ++sl) {
-                if (kbn[sl] > 0) drained = mbar_wait(bar_kb_empty + 8 * sl, (kbn[sl] - 1) & 1) && drained;
-                if (vn[sl] > 0) drained = mbar_wait(bar_v_empty + 8 * sl, (vn[sl] - 1) & 1) && drained;
+            if (x > 0) drained = mbar_wait(bar_sg_full, (x - 1) & 1) && drained;
+            for (int y = x - kKvSlots; y < x; ++y)    // the last commits to each K slot
+                if (y >= 0) drained = mbar_wait(bar_kempty + 8 * (y % kKvSlots), (y / kKvSlots) & 1) && drained;
+            if (!drained) *s_abort = 1;
+        }
+    } else if (warp == kCtPvWarp) {
+        // ------------------------------------------------------------ P.V issuer
+        if (lane == 0) {
+            constexpr uint32_t id_o = idesc(128, 128, 1);
+            int g = 0;
+            bool ok = true;
+            for (int k = 0; k < my_items && ok; ++k) {
+                const int n_keys = s_len[2 * k + 1];
+                const int n_st = (n_keys + kCtBN - 1) / kCtBN;
+                for (int s = 0; s < n_st; ++s, ++g) {
+                    ok = wait_or_abort(bar_p_full, g & 1, s_abort) &&
+                         wait_or_abort(bar_vfull + 8 * (g % kKvSlots), (g / kKvSlots) & 1, s_abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t vbase = sb + SP::off_v + (g % kKvSlots) * SP::kv_tile;
+                    // only over the 16-key steps that hold keys of the stream
+                    const int kst = n_keys - s * kCtBN;
+                    const int ksteps = kst < kCtBN ? (kst + 15) >> 4 : kCtBN / 16;
+                    // B = [V_h0 | V_h1], MN-major: a step's 16 keys are two 8-key groups 2 KB apart,
+                    // and within a group head h0 + 1's atom follows h0's (1 KB)
+#pragma unroll
+                    for (int kk = 0; kk < kCtBN / 16; ++kk)
+                        if (kk < ksteps)
+                            umma_ts(tmem + kCtColO, tmem + kCtColP + 8 * kk, sdesc_mn(vbase + 4096 * kk, 1024, 2048),
+                                    id_o, (s > 0 || kk > 0) ? 1 : 0);
+                    umma_commit(bar_pv_done);
+                    umma_commit(bar_vempty + 8 * (g % kKvSlots));
+                }
             }
+            umma_commit(bar_drain2);
+            bool drained = mbar_wait(bar_drain2, 0);
+            if (g > 0) drained = mbar_wait(bar_pv_done, (g - 1) & 1) && drained;
+            for (int y = g - kKvSlots; y < g; ++y)    // and to each V slot
+                if (y >= 0) drained = mbar_wait(bar_vempty + 8 * (y % kKvSlots), (y / kKvSlots) & 1) && drained;
             if (!drained) *s_abort = 1;
         }
     } else if (warp < kCtSoftmaxWarps) {
@@ -527,8 +539,7 @@ __global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
         // loads (32 distinct banks) are free of conflicts.
         const int w0 = (31 - lane) >> 1;
         const int q0 = w0 >> 2;
-        uint32_t* stg = reinterpret_cast<uint32_t*>(sm + SP::off_stg + warp * kCtStg) +
-                        4 * (5 * lane + 2 * (lane >> 3));
+        const int stg_off = warp * kCtStg + 16 * (5 * lane + 2 * (lane >> 3));   // bytes
         int p_b = 0, p_h0 = 0;
         float p_l = 0.f;
         bool have_prev = false, all_ok = true;
@@ -546,6 +557,8 @@ __global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
                 // the half holds keys jh .. jh+31 of the stream; keys [0, kb) of it exist
                 const int jh = s * kCtBN + 32 * hf;
                 const int kb = N - jh;
+                // the staging tile overlays this stage's band tile (G has been computed from it)
+                uint32_t* stg = reinterpret_cast<uint32_t*>(sm + SP::off_band + (g & 1) * SP::band_tile + stg_off);
                 float sc[32];
                 {
                     // position term, skewed: row i needs G[r][63 - i + j] (j the key of the
@@ -566,8 +579,12 @@ __global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
                                                   __uint_as_float(gr[8 * pc + 2 * e + 1]));
                             *reinterpret_cast<uint4*>(stg + 4 * (pc - q0)) = make_uint4(gw[0], gw[1], gw[2], gw[3]);
                         }
+                    // S columns of this half's keys 8 gg + e: 16 (4 hf + gg) + 8 hd + e
                     uint32_t sr[32];
-                    OASR_TMEM_LD32(tl + kCtColS + 64 * hd + 32 * hf, sr);
+                    OASR_TMEM_LD8(tl + kCtColS + 64 * hf + 8 * hd, sr);
+                    OASR_TMEM_LD8(tl + kCtColS + 64 * hf + 16 + 8 * hd, (sr + 8));
+                    OASR_TMEM_LD8(tl + kCtColS + 64 * hf + 32 + 8 * hd, (sr + 16));
+                    OASR_TMEM_LD8(tl + kCtColS + 64 * hf + 48 + 8 * hd, (sr + 24));
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) sc[j] = __uint_as_float(sr[j]);
@@ -589,6 +606,9 @@ __global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
                         wa = wb;
                     }
                 }
+                // the band tile (staging included) is no longer read: its next stage may land
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_bempty + 8 * (g & 1));
                 // last stage of the item: the next item's A tiles, so that its first S/G can be
                 // issued while this stage's softmax and the epilogue run
                 if (s + 1 == n_st && k + 1 < my_items) {
@@ -661,10 +681,10 @@ __global__ void __launch_bounds__(kCtThreads, 1) chunk_attn_tc_kernel(
                 const int kstage = N - s * kCtBN;
                 const int k16 = (kstage + 15) & ~15;
                 if (kstage < k16 && quad < 2 && 32 * quad < k16 && 32 * quad + 32 > kstage) {
-                    if (!warp_wait(bar_vfull + 8 * (g & 1), (g >> 1) & 1)) { ok = false; break; }
+                    if (!warp_wait(bar_vfull + 8 * (g % kKvSlots), (g / kKvSlots) & 1)) { ok = false; break; }
                     if (r >= kstage && r < k16) {
-                        uint4* vrow = reinterpret_cast<uint4*>(sm + SP::off_slot + (g & 1) * SP::slot + SP::off_v +
-                                                               hf * SP::head_k + r * kRowBytes);
+                        uint4* vrow = reinterpret_cast<uint4*>(sm + SP::off_v + (g % kKvSlots) * SP::kv_tile +
+                                                               ((r >> 3) * 2 + hf) * 1024 + (r & 7) * kRowBytes);
 #pragma unroll
                         for (int c = 0; c < 8; ++c) vrow[c] = make_uint4(0u, 0u, 0u, 0u);
                     }
@@ -729,8 +749,8 @@ oasr_status launch_chunk_tc(const void* q, const void* k_pool, const void* v_poo
     const int box = block_size < kCtBN ? block_size : kCtBN;
     CUtensorMap tm_q, tm_k, tm_v, tm_r;
     if (!encode_rows_bf16(&tm_q, q, static_cast<long long>(B) * T, H, kCtTq) ||
-        !encode_rows_bf16(&tm_k, k_pool, static_cast<long long>(num_blocks) * block_size, H, box) ||
-        !encode_rows_bf16(&tm_v, v_pool, static_cast<long long>(num_blocks) * block_size, H, box) ||
+        !encode_head_pairs_bf16(&tm_k, k_pool, static_cast<long long>(num_blocks) * block_size, H, box) ||
+        !encode_head_pairs_bf16(&tm_v, v_pool, static_cast<long long>(num_blocks) * block_size, H, box) ||
         !encode_rows_bf16(&tm_r, rel, R, H, kCtBand))
         return OASR_ERR_INVALID_ARG;
     unsigned* status = status_word();

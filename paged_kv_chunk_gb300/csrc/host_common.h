@@ -21,6 +21,12 @@ int sm_count();
 // one head, 128-byte swizzled.  Returns false if the driver rejects it.
 bool encode_rows_bf16(CUtensorMap* map, const void* base, long long rows, int H, int box_rows);
 
+// Encode a 4-D bf16 tensor map over the rows of [rows, H, 64] (rows a multiple of 8) viewed as
+// {64, row % 8, head, row / 8}, with a box of two adjacent heads and box_rows rows (a multiple
+// of 8), 128-byte swizzled: in shared memory a box is [row / 8][head][row % 8][64], so every
+// 8 rows of one head form one 1 KB swizzle atom.  Returns false if the driver rejects it.
+bool encode_head_pairs_bf16(CUtensorMap* map, const void* base, long long rows, int H, int box_rows);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline oasr_status launch_status()

@@ -246,17 +246,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
         }
     };
 
-    // The TMA producer polls with a pause between tries, so that its warp takes few issue
-    // slots from the softmax warps sharing its scheduler.
+    // The TMA producers wait on the barrier itself (suspended until its phase completes), so
+    // that they react at once and take no issue slots from the softmax warps meanwhile.
     auto prod_wait = [&](uint32_t bar, uint32_t parity, volatile int* abort) {
-        if (mbar_try_wait(bar, parity)) return true;
-        const uint64_t t0 = global_timer_ns();
-        for (;;) {
-            __nanosleep(128);
-            if (mbar_try_wait(bar, parity)) return true;
-            if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) { *abort = 1; return false; }
-        }
+        return wait_or_abort(bar, parity, abort);
     };
     // Softmax warps take every wait together: a warp-wide vote keeps the warp converged for
     // the .sync.aligned tensor-memory instructions even if one lane's wait runs out.

@@ -19,12 +19,12 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr)
            (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// The same with a leading byte offset: for an MN-major operand wider than one 64-element
-// swizzle atom, the distance between its atoms along N.
-__device__ __forceinline__ uint64_t sdesc_lbo(uint32_t addr, uint32_t lbo)
+// The same with both offsets given: for an MN-major operand, lbo is the distance between its
+// 64-element swizzle atoms along N and sbo the distance between its 8-row groups along K.
+__device__ __forceinline__ uint64_t sdesc_mn(uint32_t addr, uint32_t lbo, uint32_t sbo)
 {
     return static_cast<uint64_t>((addr >> 4) & 0x3FFF) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
-           (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M x N, B MN-major if b_mn.
@@ -72,6 +72,12 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
                    "=r"(r[30]), "=r"(r[31])                                                         \
                  : "r"(taddr))
 
+#define OASR_TMEM_LD8(taddr, r)                                                                    \
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"         \
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),          \
+                   "=r"(r[6]), "=r"(r[7])                                                           \
+                 : "r"(taddr))
+
 #define OASR_TMEM_ST32(taddr, r)                                                                   \
     asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"  \
                  "%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,"    \
@@ -107,6 +113,18 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
         : "r"(bar), "r"(parity), "r"(hint_ns)
         : "memory");
     return done != 0;
+}
+
+// 4-D tiled bulk tensor load global -> shared with an L2 hint, completion counted on `bar` in
+// bytes; boxes reaching outside the tensor are filled with zeros.
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int x, int y, int z, int w, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "l"(policy)
+        : "memory");
 }
 
 // Bounded wait that also gives up as soon as another role has aborted the CTA.
