@@ -15,7 +15,7 @@
 //   O [128 x 64] += P . V               columns [384,448)  M128 N64, A = P from TMEM, B = V
 //                                                          as an MN-major smem operand
 //   P [128 x 128] bf16                  columns [448,512)
-// Warp roles (352 threads):
+// Warp roles (384 threads):
 //   warps 0-7  softmax.  Warps w and w+4 share TMEM lane quadrant w and the 32 query rows in
 //              it; warp w takes keys 0-63 of each stage, warp w+4 keys 64-127, and the pair
 //              swaps row maxima and sums through shared memory.  Each thread loads its S half
@@ -25,14 +25,15 @@
 //              masks keys past the segment; keeps the running max (O is rescaled in TMEM only
 //              when the max grows by more than 2^8) and sum; writes its half row of bf16 P to TMEM; at
 //              the end of the tile normalises and stores its half of the O row.
-//   warp 8     MMA issuer (one thread): S and G of stage s+1 as soon as the softmax warps have
-//              read stage s's, then P.V of stage s.
+//   warp 8     S/G issuer (one thread): S and G of stage s+1 as soon as the softmax warps have
+//              read stage s's.
 //   warp 9     TMA producer of the q rows and of the K and band tiles of a two-slot ring: a
 //              slot's K and band are refilled as soon as the S and G products that read them
 //              have finished.
 //   warp 10    TMA producer of the ring's V tiles: a slot's V is refilled once its last P.V has
 //              finished.  With V on a thread of its own, the next K and band never wait behind
 //              a V copy; S and G of a stage wait for K and band alone.
+//   warp 11    P.V issuer (one thread): P.V of stage s once the softmax warps have written P.
 // Every wait is bounded; a wait that runs out raises the timeout bit and aborts the CTA's
 // remaining work, after which the CTA still drains its copies and tensor-core work and frees
 // its TMEM.
@@ -46,8 +47,9 @@ namespace {
 
 constexpr int kTcMaxSeqs = 1024;
 constexpr int kSoftmaxWarps = 8;
-constexpr int kTcThreads = 32 * (kSoftmaxWarps + 3);
-constexpr int kMmaWarp = kSoftmaxWarps, kTmaWarp = kSoftmaxWarps + 1, kVWarp = kSoftmaxWarps + 2;
+constexpr int kTcThreads = 32 * (kSoftmaxWarps + 4);
+constexpr int kMmaWarp = kSoftmaxWarps, kTmaWarp = kSoftmaxWarps + 1, kVWarp = kSoftmaxWarps + 2,
+              kPvWarp = kSoftmaxWarps + 3;
 constexpr int kBM = 128;                 // queries per tile
 constexpr int kBN = 128;                 // keys per stage
 constexpr int kBand = 256;               // band rows per stage
@@ -72,7 +74,7 @@ struct TcSmem {
     static constexpr int off_tile = off_cu + (kTcMaxSeqs + 1) * 4;
     static constexpr int off_misc = (off_tile + (kTcMaxSeqs + 1) * 4 + 15) & ~15;   // wsum[16], tmem, abort
     static constexpr int off_bar = (off_misc + 128 + 7) & ~7;
-    static constexpr int n_bars = 2 + 2 + 7 + 4 + 2 + 2 + 2;
+    static constexpr int n_bars = 2 + 2 + 8 + 4 + 2 + 2 + 2;
     static constexpr int bytes = off_bar + n_bars * 8 + 1024;
     static_assert(bytes <= 232448, "dynamic shared memory of one CTA");
 };
@@ -128,8 +130,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
     const uint32_t bar_pv_done = bar_p_full + 8;       // P.V finished
     const uint32_t bar_q_ready = bar_pv_done + 8;      // bf16(q+u), bf16(q+v) written
     const uint32_t bar_q_free = bar_q_ready + 8;       // last S/G MMA of an item finished
-    const uint32_t bar_drain = bar_q_free + 8;         // everything the MMA issuer issued finished
-    const uint32_t bar_pair = bar_drain + 8;           // [4] softmax warp pair exchanged a value
+    const uint32_t bar_drain = bar_q_free + 8;         // everything the S/G issuer issued finished
+    const uint32_t bar_drain2 = bar_drain + 8;         // everything the P.V issuer issued finished
+    const uint32_t bar_pair = bar_drain2 + 8;          // [4] softmax warp pair exchanged a value
     const uint32_t bar_qb_full = bar_pair + 32;        // q rows of the next item landed
     const uint32_t bar_qb_free = bar_qb_full + 8;      // softmax warps have read the q rows
     const uint32_t bar_kb_empty = bar_qb_free + 8;     // [2] the slot's K and band tiles read
@@ -148,6 +151,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
         mbar_init(bar_q_ready, kSoftmaxWarps);
         mbar_init(bar_q_free, 1);
         mbar_init(bar_drain, 1);
+        mbar_init(bar_drain2, 1);
         for (int i = 0; i < 4; ++i) mbar_init(bar_pair + 8 * i, 64);
         mbar_init(bar_qb_full, 1);
         mbar_init(bar_qb_free, kSoftmaxWarps);
@@ -325,103 +329,86 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 if (u >= 0 && !mbar_wait(bar_v_full + 8 * (u & 1), (u >> 1) & 1)) *s_abort = 1;
         }
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------- MMA issuer
+        // ------------------------------------------------------------ S/G issuer
+        // Each tcgen05.mma holds its issuing thread until the tensor pipe takes it, so S/G and
+        // P.V are issued from two threads: while one waits on a barrier the other's products run.
+        // S and G of a stage (possibly the next item's first) go as soon as the previous stage's
+        // have been read, so they overlap that stage's softmax and, across items, the previous
+        // tile's last stage and epilogue.
         if (lane == 0) {
-            constexpr uint32_t id_s = idesc(kBM, kBN, 0), id_g = idesc(kBM, kBand, 0),
-                               id_o = idesc(kBM, 64, 1);
-            int g = 0, it = 0, sg = 0, nq = 0, npv = 0;
-            int kbn[2] = {0, 0};   // commits to each slot's K-and-band barrier
-            auto issue_sg = [&](int slot) {
-                const uint32_t base = sb + SP::off_slot + slot * SP::slot;
-                tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    umma_ss(tmem + kColS, sdesc(sb + SP::off_qu + 32 * k), sdesc(base + 32 * k), id_s, k > 0);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    umma_ss(tmem + kColG, sdesc(sb + SP::off_qv + 32 * k),
-                            sdesc(base + SP::off_band + 32 * k), id_g, k > 0);
-                umma_commit(bar_sg_full);
-                umma_commit(bar_kb_empty + 8 * slot);   // the slot's K and band may be refilled
-                ++kbn[slot];
-                ++sg;
-            };
-            // One flat walk over the CTA's stages.  The S/G of the next stage, which may be
-            // the next item's first, is issued as soon as this stage's S/G have been read,
-            // so it overlaps this stage's softmax, and across items the next tile's first
-            // products overlap the current tile's last stage and epilogue.
-            long long item = blockIdx.x;
-            int n_st = 0, s = 0, seg = 0, n_keys = 0;
-            auto item_stages = [&](long long itm, int& keys) {
+            constexpr uint32_t id_s = idesc(kBM, kBN, 0), id_g = idesc(kBM, kBand, 0);
+            int x = 0, nq = 0, it = 0, seg = 0;   // x: stages issued
+            int kbn[2] = {0, 0};                  // commits to each slot's K-and-band barrier
+            bool ok = true;
+            for (long long item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
                 int start, L, i0, h, kl, kh;
-                decode(itm, seg, start, L, i0, h, kl, kh);
-                keys = kh - kl;
-                return (kh - kl + kBN - 1) / kBN;
-            };
-            bool ok = item < n_items;
-            if (ok) {
-                n_st = item_stages(item, n_keys);
-                ok = wait_or_abort(bar_q_ready, 0, s_abort) &&
-                     wait_or_abort(bar_full, 0, s_abort);
-                if (ok) {
-                    issue_sg(0);
-                    if (n_st == 1) { umma_commit(bar_q_free); ++nq; }
-                }
-            }
-            while (ok) {
-                // the stage after g: this item's next one, or the next item's first
-                const bool last = s + 1 == n_st;
-                const long long next_item = last ? item + gridDim.x : item;
-                if (next_item < n_items) {
-                    int next_keys = 0;
-                    const int next_n = last ? item_stages(next_item, next_keys) : n_st;
-                    const int next_s = last ? 0 : s + 1;
-                    ok = (!last || wait_or_abort(bar_q_ready, (it + 1) & 1, s_abort)) &&
-                         wait_or_abort(bar_full + 8 * ((g + 1) & 1), ((g + 1) >> 1) & 1, s_abort) &&
-                         wait_or_abort(bar_sg_free, (sg - 1) & 1, s_abort);
+                decode(item, seg, start, L, i0, h, kl, kh);
+                const int n_st = (kh - kl + kBN - 1) / kBN;
+                for (int s = 0; s < n_st; ++s, ++x) {
+                    ok = (s > 0 || wait_or_abort(bar_q_ready, it & 1, s_abort)) &&
+                         wait_or_abort(bar_full + 8 * (x & 1), (x >> 1) & 1, s_abort) &&
+                         (x == 0 || wait_or_abort(bar_sg_free, (x - 1) & 1, s_abort));
                     if (!ok) break;
-                    issue_sg((g + 1) & 1);
-                    if (next_s + 1 == next_n) { umma_commit(bar_q_free); ++nq; }
-                }
-                // P.V of stage g
-                ok = wait_or_abort(bar_p_full, g & 1, s_abort) &&
-                     wait_or_abort(bar_v_full + 8 * (g & 1), (g >> 1) & 1, s_abort);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t vbase = sb + SP::off_slot + (g & 1) * SP::slot + SP::off_v;
-                // only the 16-key steps that hold keys of the segment (a partial last stage
-                // stops early, so V rows past them are never read)
-                const int kst = n_keys - s * kBN;
-                const int ksteps = kst < kBN ? (kst + 15) >> 4 : kBN / 16;
+                    const int slot = x & 1;
+                    const uint32_t base = sb + SP::off_slot + slot * SP::slot;
+                    tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < kBN / 16; ++k)
-                    if (k < ksteps)
-                        umma_ts(tmem + kColO, tmem + kColP + 8 * k, sdesc(vbase + 2048 * k), id_o,
-                                (s > 0 || k > 0) ? 1 : 0);
-                umma_commit(bar_pv_done);
-                umma_commit(bar_empty + 8 * (g & 1));
-                ++npv;
-                ++g;
-                if (!last) {
-                    ++s;
-                } else {
-                    item = next_item;
-                    ++it;
-                    if (item >= n_items) break;
-                    n_st = item_stages(item, n_keys);
-                    s = 0;
+                    for (int k = 0; k < 4; ++k)
+                        umma_ss(tmem + kColS, sdesc(sb + SP::off_qu + 32 * k), sdesc(base + 32 * k), id_s, k > 0);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        umma_ss(tmem + kColG, sdesc(sb + SP::off_qv + 32 * k),
+                                sdesc(base + SP::off_band + 32 * k), id_g, k > 0);
+                    umma_commit(bar_sg_full);
+                    umma_commit(bar_kb_empty + 8 * slot);   // the slot's K and band may be refilled
+                    ++kbn[slot];
+                    if (s + 1 == n_st) { umma_commit(bar_q_free); ++nq; }   // the Qu/Qv tiles are free
                 }
             }
-            // drain: every MMA issued has finished and every arrival it owes has landed
+            // drain: every product issued here has finished and every arrival it owes has landed
             umma_commit(bar_drain);
             bool drained = mbar_wait(bar_drain, 0);
             if (nq > 0) drained = mbar_wait(bar_q_free, (nq - 1) & 1) && drained;
-            if (sg > 0) drained = mbar_wait(bar_sg_full, (sg - 1) & 1) && drained;
-            if (npv > 0) drained = mbar_wait(bar_pv_done, (npv - 1) & 1) && drained;
-            for (int u = npv - 2; u < npv; ++u)
-                if (u >= 0) drained = mbar_wait(bar_empty + 8 * (u & 1), (u >> 1) & 1) && drained;
+            if (x > 0) drained = mbar_wait(bar_sg_full, (x - 1) & 1) && drained;
             for (int sl = 0; sl < 2; ++sl)
                 if (kbn[sl] > 0) drained = mbar_wait(bar_kb_empty + 8 * sl, (kbn[sl] - 1) & 1) && drained;
+            if (!drained) *s_abort = 1;
+        }
+    } else if (warp == kPvWarp) {
+        // ------------------------------------------------------------ P.V issuer
+        if (lane == 0) {
+            constexpr uint32_t id_o = idesc(kBM, 64, 1);
+            int g = 0, seg = 0;
+            bool ok = true;
+            for (long long item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+                int start, L, i0, h, kl, kh;
+                decode(item, seg, start, L, i0, h, kl, kh);
+                const int n_keys = kh - kl;
+                const int n_st = (n_keys + kBN - 1) / kBN;
+                for (int s = 0; s < n_st; ++s, ++g) {
+                    ok = wait_or_abort(bar_p_full, g & 1, s_abort) &&
+                         wait_or_abort(bar_v_full + 8 * (g & 1), (g >> 1) & 1, s_abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t vbase = sb + SP::off_slot + (g & 1) * SP::slot + SP::off_v;
+                    // only the 16-key steps that hold keys of the segment (a partial last stage
+                    // stops early, so V rows past them are never read)
+                    const int kst = n_keys - s * kBN;
+                    const int ksteps = kst < kBN ? (kst + 15) >> 4 : kBN / 16;
+#pragma unroll
+                    for (int k = 0; k < kBN / 16; ++k)
+                        if (k < ksteps)
+                            umma_ts(tmem + kColO, tmem + kColP + 8 * k, sdesc(vbase + 2048 * k), id_o,
+                                    (s > 0 || k > 0) ? 1 : 0);
+                    umma_commit(bar_pv_done);
+                    umma_commit(bar_empty + 8 * (g & 1));
+                }
+            }
+            umma_commit(bar_drain2);
+            bool drained = mbar_wait(bar_drain2, 0);
+            if (g > 0) drained = mbar_wait(bar_pv_done, (g - 1) & 1) && drained;
+            for (int u = g - 2; u < g; ++u)
+                if (u >= 0) drained = mbar_wait(bar_empty + 8 * (u & 1), (u >> 1) & 1) && drained;
             if (!drained) *s_abort = 1;
         }
     } else if (warp < kSoftmaxWarps) {
