@@ -50,6 +50,14 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0   # the ~8 TB/s the streaming step's HBM target is stated against
 KERNEL_SOURCES = ["chunk_attn.cu", "attn_core.cuh", "ptx.cuh"]
+# chunks of 33..64 frames with an even head count run the append, then the tensor-core kernel
+TC_STREAM_SOURCES = ["chunk_tc.cu", "append.cu", "tcgen05.cuh", "attn_core.cuh", "ptx.cuh"]
+
+
+def uses_tc_stream(T, H):
+    """Whether the library runs a streaming step of chunk length T over H heads as the paged
+    append followed by the tcgen05 kernel (the dispatch rule of chunk_attn.cu)."""
+    return 33 <= T <= 64 and H % 2 == 0
 PACKED_SOURCES = ["packed_tc.cu", "tcgen05.cuh", "attn_core.cuh", "ptx.cuh"]
 
 
@@ -665,8 +673,16 @@ def run_ours(args, cfg, rank, world, local):
         return
     peak, peak_kind = measured_hbm_peak()
     achieved = touched / (launch_us * 1e-6) / 1e9
+    tc = uses_tc_stream(T, H)
     traffic, traffic_src = ((None, "not captured for the two-call step") if args.two_call
-                            else profiled_traffic(f"chunk_step_{cfg.name}"))
+                            else profiled_traffic(f"chunk_step_{cfg.name}",
+                                                  TC_STREAM_SOURCES if tc else None))
+    if tc:
+        kernel = "paged_append_kernel + chunk_attn_tc_kernel"
+    elif args.two_call:
+        kernel = "paged_append_kernel + chunk_attn_bf16_kernel"
+    else:
+        kernel = "chunk_attn_bf16_kernel (fused append + attention)"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
@@ -687,12 +703,11 @@ def run_ours(args, cfg, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_src,
                      "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
-                     "kernel": ("paged_append_kernel + chunk_attn_bf16_kernel" if args.two_call
-                                else "chunk_attn_bf16_kernel (fused append + attention)"),
+                     "kernel": kernel,
                      "algorithmic_bytes_per_launch": touched,
                      "avg_launch_us": launch_us, "peak_kind": peak_kind,
                      **({"cold_l2": {**cold, "frac": cold["achieved_gbs"] / peak}} if cold else {})},
-        "gpu_launches": args.steps * (layers * (2 if args.two_call else 1) + (1 if cfg.window else 0)),
+        "gpu_launches": args.steps * (layers * (2 if args.two_call or tc else 1) + (1 if cfg.window else 0)),
         "clocks": clocks,
     }
     if e2e:
