@@ -102,7 +102,9 @@ oasr_status oasr_paged_append(const void* k_new, const void* v_new, void* k_pool
  * R - T + 1) (the keys the host can bound, for which it sizes its shared memory, so an
  * engine-sized block table costs nothing), the f32 path drops keys past the table's pages
  * and reads zero rows for the distances the rel table lacks.  scale is normally 1/sqrt(D).
- * bf16: bf16 inputs, fp32 accumulation and softmax, bf16 output rounded once.
+ * bf16: bf16 inputs, fp32 accumulation and softmax, bf16 output rounded once; chunks of
+ * 33 to 64 frames with an even H run on the 5th-generation tensor cores (two heads of a
+ * stream per 128-row tile), other shapes on the legacy mma.sync path.
  * f32: fp32 throughout (no TF32).
  */
 oasr_status oasr_chunk_relattn_paged(const void* q, const void* k_pool, const void* v_pool,
@@ -118,8 +120,10 @@ oasr_status oasr_chunk_relattn_paged(const void* q, const void* k_pool, const vo
  * one launch.  Each (stream, head) program writes its head's slice of the chunk into
  * the pool and then attends over cache + chunk, so the chunk is never re-read from
  * HBM (when every page the chunk lands in is a valid block, the attention reads the
- * chunk's keys straight from k_new / v_new).  Results equal the two calls in sequence up
- * to floating-point summation order; the pool afterwards is bit-identical.  The same
+ * chunk's keys straight from k_new / v_new).  For bf16 chunks of 33 to 64 frames with an
+ * even H the step is instead the two calls in sequence on `stream` (the append, then the
+ * tensor-core attention over the pool).  Results equal the two calls in sequence up to
+ * floating-point summation order; the pool afterwards is bit-identical.  The same
  * requirements apply.  Block ids of different streams must not alias a block that this
  * step writes.
  */
