@@ -170,6 +170,15 @@ EDGE = [
     (2, 2, 5, 77, 8, 2, "f32"),
     (2, 3, 40, 33, 16, 0, "f32"),
     (1, 1, 1, 0, 8, 0, "f32"),
+    # chunks of 33-64 frames with an even head count: the tcgen05 kernel (a head pair per tile)
+    (2, 2, 33, 0, 16, 0, "bf16"),      # the shortest such chunk, no history: one stage
+    (3, 4, 40, 7, 8, 0, "bf16"),       # odd history, 8-row pages: five boxes per stage
+    (2, 2, 64, 200, 64, 3, "bf16"),    # one page per stage; longer rel table
+    (2, 2, 48, 200, 256, 0, "bf16"),   # pages of 256 rows: 64-row boxes inside a page
+    (1, 2, 64, 1000, 128, 0, "bf16"),  # a long history in 128-row pages
+    (2, 6, 50, 61, 32, 0, "bf16"),     # three head pairs, T not a power of two
+    (3, 2, 63, 1, 16, 0, "bf16"),      # one cached frame: the last stage holds one key
+    (2, 3, 48, 90, 16, 0, "bf16"),     # odd H: the mma.sync kernel for the same chunk
 ]
 
 
@@ -184,8 +193,11 @@ def test_chunk_attention_edge_cases(B, H, T, C, bs, extra, dtype, fused):
     assert capi.oasr_device_status() == 0
 
 
-def test_chunk_scale_argument():
-    cfg = syn.StreamingConfig("scale", B=2, H=2, D=64, T=8, C=24, block_size=16, dtype="bf16",
+@pytest.mark.parametrize("T,scale", [(8, 0.9), (40, 0.9), (40, -0.3), (64, 0.0)], ids=str)
+def test_chunk_scale_argument(T, scale):
+    """The scale argument, including a negative one (its sign is folded into q+u and q+v on
+    the tensor-core path) and zero (uniform weights)."""
+    cfg = syn.StreamingConfig("scale", B=2, H=2, D=64, T=T, C=24, block_size=16, dtype="bf16",
                               seed=5)
     x = stream_case(cfg)
     d = gpu_stream_inputs(x, "bf16")
@@ -193,14 +205,16 @@ def test_chunk_scale_argument():
                            d["cache_seqlens"])
     out = capi.oasr_chunk_relattn_paged(d["q"], d["k_pool"], d["v_pool"], d["block_table"],
                                         d["cache_seqlens"], d["pos_bias_u"], d["pos_bias_v"],
-                                        d["rel"], scale=0.9)
-    check_close(to_np(out), oracle_chunk(x, scale=0.9), "bf16", "scale 0.9")
+                                        d["rel"], scale=scale)
+    check_close(to_np(out), oracle_chunk(x, scale=scale), "bf16", f"scale {scale}")
 
 
-def test_invalid_block_id_is_flagged_and_contained():
+@pytest.mark.parametrize("T", [8, 48])
+def test_invalid_block_id_is_flagged_and_contained(T):
     """A bad block id in one stream's table raises the bounds bit; the other streams'
-    rows are still exact and nothing is read or written outside the pool."""
-    cfg = syn.StreamingConfig("badid", B=3, H=2, D=64, T=8, C=40, block_size=16, dtype="bf16",
+    rows are still exact and nothing is read or written outside the pool (T = 48: the append
+    and the tensor-core kernel)."""
+    cfg = syn.StreamingConfig("badid", B=3, H=2, D=64, T=T, C=40, block_size=16, dtype="bf16",
                               seed=9)
     x = stream_case(cfg)
     bt = x["block_table"].copy()
@@ -219,7 +233,8 @@ def test_invalid_block_id_is_flagged_and_contained():
         check_close(got[b], ref[b], "bf16", f"stream {b}")
 
 
-@pytest.mark.parametrize("C,T,bad_page", [(40, 8, 2), (44, 8, 3), (44, 8, 2), (0, 16, 0)],
+@pytest.mark.parametrize("C,T,bad_page", [(40, 8, 2), (44, 8, 3), (44, 8, 2), (0, 16, 0),
+                                         (40, 40, 3), (32, 48, 4), (0, 64, 1)],
                          ids=lambda v: str(v))
 def test_fused_step_with_an_invalid_chunk_page(C, T, bad_page):
     """A chunk page that names no valid block: the fused step falls back to writing the
@@ -402,14 +417,16 @@ def _hetero_inputs(Cs, T, H, bs, seed, R):
     return x
 
 
-@pytest.mark.parametrize("Cs", [[0, 17, 64, 130, 255, 3], [0, 300, 527, 130, 511, 45]],
-                         ids=["short", "long"])
+@pytest.mark.parametrize("Cs,T", [([0, 17, 64, 130, 255, 3], 16), ([0, 300, 527, 130, 511, 45], 16),
+                                  ([0, 17, 64, 130, 255, 3], 48), ([0, 300, 527, 130, 511, 45], 64)],
+                         ids=["short", "long", "short_T48", "long_T64"])
 @pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
-def test_heterogeneous_cache_lengths_one_launch(fused, Cs):
+def test_heterogeneous_cache_lengths_one_launch(fused, Cs, T):
     """Streams at different offsets in one launch (Scheduler page, section 4.3): each reads
     its own cache_seqlens and indexes the shared table at distance C_b + i - j (the long
-    cohort's position tables take two batches of rel loads)."""
-    T, H, bs = 16, 4, 16
+    cohort's position tables take two batches of rel loads; T = 48 and 64 run on the
+    tensor-core kernel, whose work items then have different stage counts)."""
+    H, bs = 4, 16
     R = max(Cs) + 2 * T - 1 + 4
     x = _hetero_inputs(Cs, T, H, bs, seed=123, R=R)
     cfg = syn.StreamingConfig("het", B=len(Cs), H=H, D=64, T=T, C=max(Cs), block_size=bs,
@@ -641,10 +658,11 @@ def test_projection_feeds_the_step():
 
 
 @pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
-def test_widest_block_table(fused):
+@pytest.mark.parametrize("T", [16, 64])
+def test_widest_block_table(fused, T):
     """The widest block table the bf16 path takes (512 pages), filled to its last key: the
-    chunk's last row lands in the table's last slot."""
-    bs, mbps, T = 8, 512, 16
+    chunk's last row lands in the table's last slot (T = 64: the tensor-core kernel)."""
+    bs, mbps = 8, 512
     cfg = syn.StreamingConfig("widest", B=2, H=2, D=64, T=T, C=mbps * bs - T, block_size=bs,
                               dtype="bf16", seed=71, max_blocks_per_seq=mbps)
     assert cfg.mbps == mbps
