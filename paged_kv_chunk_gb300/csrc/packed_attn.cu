@@ -7,7 +7,8 @@
 // the same segment score ((q_i+u).k_j + (q_i+v).rel[z + j - i]) * scale with
 // z = (R - 1) / 2 (rel_shift order, Model Layer page, Nemotron ASR section).
 //
-// bf16 path: the persistent tcgen05/TMEM kernel of packed_tc.cu.
+// bf16 path: the persistent tcgen05/TMEM kernel of packed_tc.cu; with the chunked-limited
+// window (an even head count, up to 511 segments), the packed mode of chunk_tc.cu.
 // f32 path: a SIMT kernel here (one warp per query row).
 #include "attn_core.cuh"
 #include "host_common.h"
@@ -119,6 +120,11 @@ oasr_status launch_packed_tc(const void* q, const void* k, const void* v, const 
                              int num_seqs, int total, const void* pos_bias_u,
                              const void* pos_bias_v, const void* rel, int R, void* out, int H,
                              float scale, int cs, int left, cudaStream_t stream);
+oasr_status launch_chunk_tc_packed(const void* q, const void* k, const void* v,
+                                   const int32_t* cu_seqlens, int num_seqs, int total,
+                                   const void* pos_bias_u, const void* pos_bias_v, const void* rel,
+                                   int R, void* out, int H, float scale, int cs, int left,
+                                   cudaStream_t stream);
 }  // namespace oasr
 
 namespace oasr {
@@ -151,6 +157,15 @@ oasr_status packed_impl(const void* q, const void* k, const void* v, const int32
             static_cast<const float*>(rel), R, z, static_cast<float*>(out), H, scale, cs, left,
             status);
         return launch_status();
+    }
+    if (cs > 0) {
+        // the chunked-limited window: 64-query blocks of a head pair on the streaming tensor-core
+        // kernel, whose stages cover the window's keys (about two per block); shapes it does not
+        // take go to the packed kernel below
+        const oasr_status st = launch_chunk_tc_packed(q, k, v, cu_seqlens, num_seqs, total,
+                                                      pos_bias_u, pos_bias_v, rel, R, out, H,
+                                                      scale, cs, left, stream);
+        if (st != OASR_ERR_UNSUPPORTED) return st;
     }
     return launch_packed_tc(q, k, v, cu_seqlens, num_seqs, total, pos_bias_u, pos_bias_v, rel, R,
                             out, H, scale, cs, left, stream);

@@ -512,12 +512,16 @@ def test_chunked_full_f32(cs, left):
 
 
 def test_chunked_one_chunk_is_the_bidirectional_call():
-    """A chunk as long as every segment is the plain packed attention, bit for bit."""
+    """A chunk as long as every segment is the plain packed attention: the same window for any
+    chunk at least that long (bit for bit), and the bidirectional result of the oracle."""
     lengths = [300, 1, 129, 64]
     _, x = _packed_case(lengths, seed=8)
     a = _run_chunked(x, "bf16", max(lengths), 0)
-    b = _run_packed(x, "bf16")
-    assert torch.equal(a, b)
+    assert torch.equal(a, _run_chunked(x, "bf16", 7 * max(lengths), 3))
+    ref = _oracle_packed(x)
+    check_close(to_np(a), ref, "bf16", "one chunk")
+    check_close(to_np(_run_packed(x, "bf16")), ref, "bf16", "bidirectional")
+    assert capi.oasr_device_status() == 0
 
 
 def test_chunked_full_size_sampled():
