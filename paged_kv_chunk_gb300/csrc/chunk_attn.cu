@@ -33,6 +33,14 @@
 
 namespace oasr {
 
+// A pipeline wait: the first poll inline, the polling loop with its time limit out of line,
+// so that each wait site costs a few instructions of code.
+__device__ __noinline__ bool ca_wait_slow(uint32_t bar, uint32_t parity) { return mbar_wait(bar, parity); }
+__device__ __forceinline__ bool ca_wait(uint32_t bar, uint32_t parity)
+{
+    return mbar_try_wait(bar, parity) || ca_wait_slow(bar, parity);
+}
+
 // The tensor-core kernel for 33 <= T <= 64 (chunk_tc.cu).
 bool chunk_tc_takes(int B, int T, int H, int mbps, int num_blocks, int block_size, int R);
 oasr_status launch_chunk_tc(const void* q, const void* k_pool, const void* v_pool, int num_blocks,
@@ -288,8 +296,8 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
         int n_issued = 0;
         for (int issued = 0; issued < n_stages; ++issued) {
             const int slot = issued % NS;
-            bool ok = issued < NS || mbar_wait(bar_empty + 8 * slot, ((issued / NS) - 1) & 1);
-            if (ok && issued == first_chunk_stage) ok = mbar_wait(bar_written, 0);
+            bool ok = issued < NS || ca_wait(bar_empty + 8 * slot, ((issued / NS) - 1) & 1);
+            if (ok && issued == first_chunk_stage) ok = ca_wait(bar_written, 0);
             if (!__all_sync(0xffffffffu, ok)) {
                 err |= kErrTimeout;
                 break;
@@ -300,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
         if (GT && FUSED && direct) {
             // with every stage out, the chunk's rows (in their own region) go into the pool;
             // every chunk page is a valid block: that is what selected direct mode
-            if (mbar_wait(bar_chunk, 0)) {
+            if (ca_wait(bar_chunk, 0)) {
                 for (int idx = lane; idx < 2 * T * 8; idx += 32) {
                     const int kv = idx >= T * 8;
                     const int rem = idx - kv * T * 8;
@@ -370,18 +378,18 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
         if (FUSED && !direct) copy_chunk_global();
         // the whole position term of the CTA (its rel rows are in flight or in), while the
         // first pages land
-        failed = !mbar_wait(bar_q, 0);
+        failed = !ca_wait(bar_q, 0);
         if (!failed)
             pt.build(reinterpret_cast<uint16_t*>(sm + SP::off_gt), a.gt_w, sm + SP::off_q, s_vb);
         // fused: the chunk's rows (requested at the start; they must land before the CTA
         // ends even when the stages do not use them)
-        if (FUSED && !mbar_wait(bar_chunk, 0)) failed = true;
+        if (FUSED && !ca_wait(bar_chunk, 0)) failed = true;
         named_bar_sync(1, 32 * kConsumerWarps);   // the table is complete
         if (!failed) make_q_frags(sb + SP::off_q, s_u, s_vb, mt, lane, qu, qv);
     } else {
         if constexpr (FUSED) copy_chunk_global();
         named_bar_sync(1, 32 * kConsumerWarps);
-        failed = !mbar_wait(bar_q, 0);
+        failed = !ca_wait(bar_q, 0);
         if (!failed) make_q_frags(sb + SP::off_q, s_u, s_vb, mt, lane, qu, qv);
     }
     if (!failed) {
@@ -406,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
             }
             for (int s = 0; s < n_stages; ++s) {
                 const int slot = s % NS;
-                if (!mbar_wait(bar_full + 8 * slot, (s / NS) & 1)) { failed = true; break; }
+                if (!ca_wait(bar_full + 8 * slot, (s / NS) & 1)) { failed = true; break; }
                 const uint32_t base = sb + SP::off_slots + slot * SP::kSlot;
                 // one m-tile: every lane releases the slot as soon as its slice's K and V rows
                 // are read (before the position term, softmax and P.V), so the producer can
@@ -434,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
             // every stage: this warp's 16-key slice; its skew scratch overlays its K rows
             for (int s = 0; s < n_stages; ++s) {
                 const int slot = s % NS;
-                if (!mbar_wait(bar_full + 8 * slot, (s / NS) & 1)) { failed = true; break; }
+                if (!ca_wait(bar_full + 8 * slot, (s / NS) & 1)) { failed = true; break; }
                 const uint32_t base = sb + SP::off_slots + slot * SP::kSlot;
                 const int kv = stage_valid(s) - 16 * warp;
                 if (kv > 0) {
@@ -452,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, (GT && NS == 2) ? 4 : 2) chunk_attn_
         } else
         for (int s = kg; s < n_stages; s += TL::KG) {
             const int slot = s % NS;
-            if (!mbar_wait(bar_full + 8 * slot, (s / NS) & 1)) { failed = true; break; }
+            if (!ca_wait(bar_full + 8 * slot, (s / NS) & 1)) { failed = true; break; }
             const uint32_t base = sb + SP::off_slots + slot * SP::kSlot;
             const uint32_t band = base + 2 * kStageKeys * kRowBytes;
             warp_stage(acc, qu, qv, base, base + kStageKeys * kRowBytes, band,

@@ -104,6 +104,29 @@ __device__ __forceinline__ void add_bf16x2_f32(float& lo, float& hi, uint32_t pa
 
 // ------------------------------------------------------------------------ kernel
 
+// A bounded wait: the first poll inline, the rest (sleeping polls, the abort flag, the time
+// limit) out of line, so that the many wait sites cost a few instructions of code each (the
+// kernel's roles run different code at once, and instruction fetch stalls them otherwise).
+__device__ __noinline__ bool pt_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort)
+{
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        // suspended until the phase completes, for 20 us at most between the checks below
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ bool pt_wait(uint32_t bar, uint32_t parity, volatile int* abort)
+{
+    return mbar_try_wait(bar, parity) || pt_wait_slow(bar, parity, abort);
+}
+// The bounded waits of the CTA's final drain, out of line.
+__device__ __noinline__ bool pt_drain_wait(uint32_t bar, uint32_t parity) { return mbar_wait(bar, parity); }
+
 template <bool MASKED>
 __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -253,12 +276,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
     // The TMA producers wait on the barrier itself (suspended until its phase completes), so
     // that they react at once and take no issue slots from the softmax warps meanwhile.
     auto prod_wait = [&](uint32_t bar, uint32_t parity, volatile int* abort) {
-        return wait_or_abort(bar, parity, abort);
+        return pt_wait(bar, parity, abort);
     };
     // Softmax warps take every wait together: a warp-wide vote keeps the warp converged for
     // the .sync.aligned tensor-memory instructions even if one lane's wait runs out.
     auto warp_wait = [&](uint32_t bar, uint32_t parity) {
-        return __all_sync(0xffffffffu, wait_or_abort(bar, parity, s_abort)) != 0;
+        return __all_sync(0xffffffffu, pt_wait(bar, parity, s_abort)) != 0;
     };
 
     if (warp == kTmaWarp) {
@@ -301,8 +324,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             }
             // no copy may still be landing when the CTA exits
             for (int u = g - 2; u < g; ++u)
-                if (u >= 0 && !mbar_wait(bar_full + 8 * (u & 1), (u >> 1) & 1)) *s_abort = 1;
-            if (itp > 0 && !mbar_wait(bar_qb_full, (itp - 1) & 1)) *s_abort = 1;
+                if (u >= 0 && !pt_drain_wait(bar_full + 8 * (u & 1), (u >> 1) & 1)) *s_abort = 1;
+            if (itp > 0 && !pt_drain_wait(bar_qb_full, (itp - 1) & 1)) *s_abort = 1;
         }
     } else if (warp == kVWarp) {
         // ---------------------------------------------------------- V producer
@@ -326,7 +349,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 }
             }
             for (int u = g - 2; u < g; ++u)
-                if (u >= 0 && !mbar_wait(bar_v_full + 8 * (u & 1), (u >> 1) & 1)) *s_abort = 1;
+                if (u >= 0 && !pt_drain_wait(bar_v_full + 8 * (u & 1), (u >> 1) & 1)) *s_abort = 1;
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ S/G issuer
@@ -345,9 +368,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 decode(item, seg, start, L, i0, h, kl, kh);
                 const int n_st = (kh - kl + kBN - 1) / kBN;
                 for (int s = 0; s < n_st; ++s, ++x) {
-                    ok = (s > 0 || wait_or_abort(bar_q_ready, it & 1, s_abort)) &&
-                         wait_or_abort(bar_full + 8 * (x & 1), (x >> 1) & 1, s_abort) &&
-                         (x == 0 || wait_or_abort(bar_sg_free, (x - 1) & 1, s_abort));
+                    ok = (s > 0 || pt_wait(bar_q_ready, it & 1, s_abort)) &&
+                         pt_wait(bar_full + 8 * (x & 1), (x >> 1) & 1, s_abort) &&
+                         (x == 0 || pt_wait(bar_sg_free, (x - 1) & 1, s_abort));
                     if (!ok) break;
                     const int slot = x & 1;
                     const uint32_t base = sb + SP::off_slot + slot * SP::slot;
@@ -367,11 +390,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
             }
             // drain: every product issued here has finished and every arrival it owes has landed
             umma_commit(bar_drain);
-            bool drained = mbar_wait(bar_drain, 0);
-            if (nq > 0) drained = mbar_wait(bar_q_free, (nq - 1) & 1) && drained;
-            if (x > 0) drained = mbar_wait(bar_sg_full, (x - 1) & 1) && drained;
+            bool drained = pt_drain_wait(bar_drain, 0);
+            if (nq > 0) drained = pt_drain_wait(bar_q_free, (nq - 1) & 1) && drained;
+            if (x > 0) drained = pt_drain_wait(bar_sg_full, (x - 1) & 1) && drained;
             for (int sl = 0; sl < 2; ++sl)
-                if (kbn[sl] > 0) drained = mbar_wait(bar_kb_empty + 8 * sl, (kbn[sl] - 1) & 1) && drained;
+                if (kbn[sl] > 0) drained = pt_drain_wait(bar_kb_empty + 8 * sl, (kbn[sl] - 1) & 1) && drained;
             if (!drained) *s_abort = 1;
         }
     } else if (warp == kPvWarp) {
@@ -386,8 +409,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 const int n_keys = kh - kl;
                 const int n_st = (n_keys + kBN - 1) / kBN;
                 for (int s = 0; s < n_st; ++s, ++g) {
-                    ok = wait_or_abort(bar_p_full, g & 1, s_abort) &&
-                         wait_or_abort(bar_v_full + 8 * (g & 1), (g >> 1) & 1, s_abort);
+                    ok = pt_wait(bar_p_full, g & 1, s_abort) &&
+                         pt_wait(bar_v_full + 8 * (g & 1), (g >> 1) & 1, s_abort);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t vbase = sb + SP::off_slot + (g & 1) * SP::slot + SP::off_v;
@@ -405,10 +428,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) packed_attn_tc_kernel(
                 }
             }
             umma_commit(bar_drain2);
-            bool drained = mbar_wait(bar_drain2, 0);
-            if (g > 0) drained = mbar_wait(bar_pv_done, (g - 1) & 1) && drained;
+            bool drained = pt_drain_wait(bar_drain2, 0);
+            if (g > 0) drained = pt_drain_wait(bar_pv_done, (g - 1) & 1) && drained;
             for (int u = g - 2; u < g; ++u)
-                if (u >= 0) drained = mbar_wait(bar_empty + 8 * (u & 1), (u >> 1) & 1) && drained;
+                if (u >= 0) drained = pt_drain_wait(bar_empty + 8 * (u & 1), (u >> 1) & 1) && drained;
             if (!drained) *s_abort = 1;
         }
     } else if (warp < kSoftmaxWarps) {

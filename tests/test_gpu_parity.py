@@ -524,6 +524,36 @@ def test_chunked_one_chunk_is_the_bidirectional_call():
     assert capi.oasr_device_status() == 0
 
 
+@pytest.mark.parametrize("H,scale", [(2, -0.3), (4, 0.0), (6, 0.2), (16, None), (3, None), (1, -0.5)],
+                         ids=str)
+def test_chunked_heads_and_scale(H, scale):
+    """Head counts and scales of the chunked call: even counts run two heads per tensor-core
+    tile (a negative scale's sign folded into q+u and q+v), odd ones the one-head kernel."""
+    _, x = _packed_case([150, 1, 64, 97, 0, 230], seed=31, H=H)
+    d = {k: dev(x[k], "bf16") for k in ("q", "k", "v", "pos_bias_u", "pos_bias_v", "rel")}
+    cu = torch.from_numpy(x["cu_seqlens"]).cuda()
+    out = capi.oasr_packed_relattn_chunked(d["q"], d["k"], d["v"], cu, x["max_seqlen"],
+                                           d["pos_bias_u"], d["pos_bias_v"], d["rel"], 8, 7,
+                                           scale=scale)
+    torch.cuda.synchronize()
+    ref = oracle.packed_relattn_chunked(x["q"], x["k"], x["v"], x["cu_seqlens"], x["pos_bias_u"],
+                                        x["pos_bias_v"], x["rel"], 8, 7, scale=scale)
+    check_close(to_np(out), ref, "bf16", f"chunked H {H} scale {scale}")
+    assert capi.oasr_device_status() == 0
+
+
+@pytest.mark.parametrize("n", [511, 512], ids=str)
+def test_chunked_segment_limit(n):
+    """The most segments the chunked call's head-pair mode takes (511) and one more (the
+    one-head kernel then takes the call), lengths 0..90."""
+    rng = np.random.default_rng(93 + n)
+    lengths = [int(v) for v in rng.integers(0, 91, size=n)]
+    _, x = _packed_case(lengths, seed=94, H=4)
+    out = _run_chunked(x, "bf16", 8, 7)
+    check_close(to_np(out), _oracle_chunked(x, 8, 7), "bf16", f"{n} segments")
+    assert capi.oasr_device_status() == 0
+
+
 def test_chunked_full_size_sampled():
     """The 256-utterance packed row under the Nemotron window: 4096 sampled rows plus
     every row of the shortest and the longest segment."""
