@@ -165,7 +165,9 @@ oasr_status oasr_packed_relattn_varlen(const void* q, const void* k, const void*
  * (sliding_window - 1) / chunk_size.  The work done grows with the segment length, not its
  * square.  Requirements as for oasr_packed_relattn_varlen, plus chunk_size >= 1 and
  * left_chunks >= 0 (else OASR_ERR_INVALID_ARG).  A chunk_size of at least every segment
- * length gives the bidirectional attention.
+ * length gives the bidirectional attention, up to summation order: in bf16 with an even head
+ * count and at most 511 segments the call runs a tensor-core kernel of its own (64 queries
+ * of a segment for a pair of heads per tile), otherwise the one-head packed kernel.
  */
 oasr_status oasr_packed_relattn_chunked(const void* q, const void* k, const void* v,
                                         const int32_t* cu_seqlens, int num_seqs, int max_seqlen,
