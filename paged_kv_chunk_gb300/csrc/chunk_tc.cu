@@ -60,6 +60,8 @@
 // Every wait is bounded; a wait that runs out raises the timeout bit and aborts the CTA's
 // remaining work, after which the CTA still drains its copies and tensor-core work and frees
 // its TMEM.
+#include <mutex>
+
 #include "attn_core.cuh"
 #include "host_common.h"
 #include "ptx.cuh"
@@ -120,8 +122,12 @@ struct CtSmem {
     // prefix of 64-query blocks in the V producer's
     static_assert(kCtMaxSeqs + 1 <= kCtMaxPages, "packed offsets fit a block-table cache");
     static constexpr int off_bar = off_misc + 64;
-    static constexpr int n_bars = 4 * kv_slots + 2 * kBandSlots + 10 + 4 + 3 * 2;
-    static constexpr int bytes = off_bar + n_bars * 8 + 1024;
+    static constexpr int n_bars = 4 * kv_slots + 2 * kBandSlots + 10 + 4 + 3 * 2 + 1;
+    // streaming, an item split over a CTA pair: the partner's row weights for this CTA's head,
+    // and each softmax thread's running max at the end of its last item
+    static constexpr int off_xw = (off_bar + n_bars * 8 + 15) & ~15;
+    static constexpr int off_mlast = off_xw + kCtTq * 4;
+    static constexpr int bytes = off_mlast + (PK ? 0 : 32 * kCtSoftmaxWarps * 4) + 1024;
     static_assert(bytes <= 232448, "dynamic shared memory of one CTA");
     static_assert(kv_tile % 1024 == 0 && off_band % 1024 == 0 && off_qu % 1024 == 0 &&
                   off_qv % 1024 == 0 && off_qbuf % 1024 == 0 && a_set % 1024 == 0,
@@ -142,6 +148,9 @@ struct CtArgs {
     // packed mode
     const int32_t* cu_seqlens;
     int num_seqs, total, z, cs, left;
+    // streaming, launched as CTA pairs: each CTA takes n_full items (c + k grid), and pair p <
+    // n_split also splits item split_base + p by its key stages (0 = no split, no pairs)
+    int n_full, n_split, split_base;
 };
 
 // One work item, as every role sees it: the global rows of its 64 query slots (nq of them real)
@@ -150,6 +159,8 @@ struct CtArgs {
 struct CtItem {
     int q_row0, nq, h0, key0, nkeys, kv_row0, rho_base;
     int b, seg_start, seg_len, i0;   // streaming: b; packed: the segment and first query
+    int s_lo, s_hi;                  // the key stages this CTA runs
+    bool xchg;                       // the other stages run on the pair's other CTA
 };
 
 // lo += bf16 low half of pair, hi += bf16 high half, each rounded once in fp32 (a bf16 value
@@ -184,6 +195,47 @@ __device__ __forceinline__ bool ct_wait(uint32_t bar, uint32_t parity, volatile 
 }
 // The bounded waits of the CTA's final drain, out of line.
 __device__ __noinline__ bool ct_drain_wait(uint32_t bar, uint32_t parity) { return mbar_wait(bar, parity); }
+
+// CTA pairs (a cluster of two): the partner's address of a shared variable, a store and an
+// mbarrier arrival there (release at cluster scope), a bounded wait on this CTA's mbarrier that
+// acquires at cluster scope, and the pair-wide barrier.
+__device__ __forceinline__ uint32_t ct_mapa(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void ct_st_cluster_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void ct_arrive_cluster(uint32_t remote_bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+__device__ __noinline__ bool ct_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort)
+{
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done)
+                     : "r"(bar), "r"(parity)
+                     : "memory");
+        if (done) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ void ct_cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
 // bf16(a + b) of two bf16 pairs, each rounded once: the same value as the fp32 sum rounded to
 // bf16, since fp32 (24 bits) holds more than twice bf16's 8 bits plus two, where rounding twice
@@ -234,6 +286,7 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
     const uint32_t bar_afull = bar_pair + 8 * 4;       // [2]
     const uint32_t bar_aready = bar_afull + 8 * 2;     // [2]
     const uint32_t bar_afree = bar_aready + 8 * 2;     // [2]
+    const uint32_t bar_xchg = bar_afree + 8 * 2;       // the pair's partial of this CTA's head landed
     const int Hp = a.H >> 1;
     __shared__ int s_my_items;
 
@@ -270,6 +323,7 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
             mbar_init(bar_aready + 8 * i, 2);
             mbar_init(bar_afree + 8 * i, 1);
         }
+        mbar_init(bar_xchg, 4 * 32);   // every lane of the partner's four warps of the other head
         fence_mbar_init();
         *s_abort = 0;
     }
@@ -333,13 +387,41 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
     } else {
         n_items = static_cast<long long>(a.B) * Hp;
     }
+    // Streaming on CTA pairs: the items c + k grid (k < n_full), then, for pair p < n_split, item
+    // split_base + p split by key stages (the even CTA the first half, the odd one the rest; an
+    // item of one stage stays whole on the even CTA).
+    __shared__ int s_split_k;   // the split item's place in this CTA's list, or -1
+    const bool pairs = !PK && a.n_split > 0;
+    const long long split_item = a.split_base + static_cast<long long>(blockIdx.x >> 1);
+    auto stages_of = [&](long long item, int& c, int& n) {
+        c = __ldg(a.cache_seqlens + item / Hp);
+        if (c < 0) { err |= kErrBounds; c = 0; }
+        long long nn = static_cast<long long>(c) + a.T;
+        if (nn > a.k_max) { err |= kErrBounds; nn = a.k_max; }
+        n = static_cast<int>(nn);
+        return (n + kCtBN - 1) / kCtBN;
+    };
     if (tid == 0) {
-        long long m = n_items > blockIdx.x ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-        if (m > kCtMaxItems) { err |= kErrBounds; m = kCtMaxItems; }   // the host bounds it
+        long long m;
+        int sk = -1;
+        if (pairs) {
+            m = a.n_full;
+            if ((blockIdx.x >> 1) < a.n_split) {
+                int c, n;
+                if ((blockIdx.x & 1) == 0 || stages_of(split_item, c, n) >= 2) sk = static_cast<int>(m++);
+            }
+        } else {
+            m = n_items > blockIdx.x ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        }
+        if (m > kCtMaxItems) { err |= kErrBounds; m = kCtMaxItems; sk = -1; }   // the host bounds it
         s_my_items = static_cast<int>(m);
+        s_split_k = sk;
     }
     __syncthreads();
+    // the partner's mbarriers are initialised before any arrival from this CTA can reach them
+    if (pairs) ct_cluster_sync();
     const int my_items = s_my_items;
+    const int split_k = s_split_k;
     // every item's keys.  Streaming: the cache length and key count (keys past what the host
     // can bound are dropped and flagged, as is a negative cache length).  Packed: the segment,
     // the first query and the keys the block's queries see (from the first query's window start
@@ -365,13 +447,18 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
             s_len[4 * k + 2] = kl;
             s_len[4 * k + 3] = kh;
         } else {
-            const int b = static_cast<int>(item / Hp);
-            int c = __ldg(a.cache_seqlens + b);
-            if (c < 0) { err |= kErrBounds; c = 0; }
-            long long n = static_cast<long long>(c) + a.T;
-            if (n > a.k_max) { err |= kErrBounds; n = a.k_max; }
+            int c, n;
+            const int n_st = stages_of(k == split_k ? split_item : item, c, n);
+            // the stages [lo, hi) this CTA runs: all of them, or its half of a split item
+            int lo = 0, hi = n_st;
+            if (k == split_k && n_st >= 2) {
+                const int h = (n_st + 1) / 2;
+                if (blockIdx.x & 1) lo = h; else hi = h;
+            }
             s_len[4 * k] = c;
-            s_len[4 * k + 1] = static_cast<int>(n);
+            s_len[4 * k + 1] = n;
+            s_len[4 * k + 2] = lo;
+            s_len[4 * k + 3] = hi;
         }
     }
     tc_fence_before();
@@ -380,7 +467,7 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
     const uint32_t tmem = *s_tmem;
     auto item_info = [&](int k) {
         CtItem it;
-        const long long item = blockIdx.x + static_cast<long long>(k) * gridDim.x;
+        const long long item = (!PK && k == split_k) ? split_item : blockIdx.x + static_cast<long long>(k) * gridDim.x;
         it.h0 = 2 * static_cast<int>(item % Hp);
         if constexpr (PK) {
             const int sg = s_len[4 * k];
@@ -394,6 +481,9 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
             it.kv_row0 = it.seg_start + it.key0;
             it.rho_base = a.z - (it.i0 + kCtTq - 1) + it.key0;
             it.b = 0;
+            it.s_lo = 0;
+            it.s_hi = (it.nkeys + kCtBN - 1) / kCtBN;
+            it.xchg = false;
         } else {
             it.b = static_cast<int>(item / Hp);
             const int C = s_len[4 * k];
@@ -404,6 +494,9 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
             it.kv_row0 = 0;
             it.rho_base = a.R - a.T - C - (kCtTq - 1);
             it.seg_start = it.seg_len = it.i0 = 0;
+            it.s_lo = s_len[4 * k + 2];
+            it.s_hi = s_len[4 * k + 3];
+            it.xchg = k == split_k && (it.nkeys + kCtBN - 1) / kCtBN >= 2;
         }
         return it;
     };
@@ -454,7 +547,6 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
         bool ok = true;
         for (int k = 0; k < my_items && ok; ++k, ++itp) {
             const CtItem it = item_info(k);
-            const int n_st = (it.nkeys + kCtBN - 1) / kCtBN;
             if (!PK) load_bt(bt_row, it.b, it.nkeys);
             // streaming: the item's q rows of both heads, once the softmax warps have read the
             // previous ones (the packed mode's go to the A-tile warp)
@@ -467,7 +559,7 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            for (int s = 0; s < n_st && ok; ++s, ++g) {
+            for (int s = it.s_lo; s < it.s_hi && ok; ++s, ++g) {
                 const int u = g % kKvSlots, n = g / kKvSlots;
                 if (lane == 0 && n > 0 && !prod_wait(bar_kempty + 8 * u, (n - 1) & 1)) ok = false;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -503,9 +595,8 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
         bool ok = true;
         for (int k = 0; k < my_items && ok; ++k) {
             const CtItem it = item_info(k);
-            const int n_st = (it.nkeys + kCtBN - 1) / kCtBN;
             if (!PK) load_bt(bt_row, it.b, it.nkeys);
-            for (int s = 0; s < n_st && ok; ++s, ++g) {
+            for (int s = it.s_lo; s < it.s_hi && ok; ++s, ++g) {
                 const int u = g % kKvSlots, n = g / kKvSlots;
                 if (lane == 0 && n > 0 && !prod_wait(bar_vempty + 8 * u, (n - 1) & 1)) ok = false;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -536,8 +627,7 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
             bool ok = true;
             for (int k = 0; k < my_items && ok; ++k) {
                 const CtItem it = item_info(k);
-                const int n_st = (it.nkeys + kCtBN - 1) / kCtBN;
-                for (int s = 0; s < n_st; ++s, ++g) {
+                for (int s = it.s_lo; s < it.s_hi; ++s, ++g) {
                     const int slot = g & 1;
                     if (g >= kBandSlots && !prod_wait(bar_bempty + 8 * slot, ((g >> 1) - 1) & 1)) { ok = false; break; }
                     // rel rows rho_min .. rho_min + 127 of both heads (rows outside the table
@@ -561,11 +651,11 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
             int x = 0, nq = 0;   // stages issued
             bool ok = true;
             for (int k = 0; k < my_items && ok; ++k) {
-                const int n_st = (item_info(k).nkeys + kCtBN - 1) / kCtBN;
-                for (int s = 0; s < n_st; ++s, ++x) {
+                const CtItem itk = item_info(k);
+                for (int s = itk.s_lo; s < itk.s_hi; ++s, ++x) {
                     // the item's A tiles (first stage), the stage's K and band, and the previous
                     // stage's S and G read by the softmax warps
-                    ok = (s > 0 || (PK ? ct_wait(bar_aready + 8 * (k & 1), (k >> 1) & 1, s_abort)
+                    ok = (s > itk.s_lo || (PK ? ct_wait(bar_aready + 8 * (k & 1), (k >> 1) & 1, s_abort)
                                        : ct_wait(bar_q_ready, k & 1, s_abort))) &&
                          ct_wait(bar_kfull + 8 * (x % kKvSlots), (x / kKvSlots) & 1, s_abort) &&
                          ct_wait(bar_bfull + 8 * (x & 1), (x >> 1) & 1, s_abort) &&
@@ -586,7 +676,7 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
                                     sdesc(bbase + hd * SP::head_band + 32 * kk), id_g, (hd | kk) ? 1 : 0);
                     umma_commit(bar_sg_full);
                     umma_commit(bar_kempty + 8 * (x % kKvSlots));   // the slot's K may be refilled
-                    if (s + 1 == n_st) {   // the A tiles are free
+                    if (s + 1 == itk.s_hi) {   // the A tiles are free
                         umma_commit(PK ? bar_afree + 8 * (k & 1) : bar_q_free);
                         ++nq;
                     }
@@ -613,9 +703,9 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
             int g = 0;
             bool ok = true;
             for (int k = 0; k < my_items && ok; ++k) {
-                const int n_keys = item_info(k).nkeys;
-                const int n_st = (n_keys + kCtBN - 1) / kCtBN;
-                for (int s = 0; s < n_st; ++s, ++g) {
+                const CtItem itk = item_info(k);
+                const int n_keys = itk.nkeys;
+                for (int s = itk.s_lo; s < itk.s_hi; ++s, ++g) {
                     ok = ct_wait(bar_p_full, g & 1, s_abort) &&
                          ct_wait(bar_vfull + 8 * (g % kKvSlots), (g / kKvSlots) & 1, s_abort);
                     if (!ok) break;
@@ -633,7 +723,7 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
                             umma_ts(tmem + kCtColO, tmem + kCtColP + 8 * kk,
                                     PK ? sdesc_mn(vbase + 2048 * kk, SP::kv_tile / 2, 1024)
                                        : sdesc_mn(vbase + 4096 * kk, 1024, 2048),
-                                    id_o, (s > 0 || kk > 0) ? 1 : 0);
+                                    id_o, (s > itk.s_lo || kk > 0) ? 1 : 0);
                     umma_commit(bar_pv_done);
                     umma_commit(bar_vempty + 8 * (g % kKvSlots));
                 }
@@ -764,6 +854,10 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
         }
         // O rows of a finished item: wait for its last P.V, combine the pair's sums, store.
         // It runs inside the next item's first stage, after that stage's S/G have been read.
+        // An item split over the CTA pair: each CTA finishes one head (its rank's), so the warps
+        // of the other head hand their normalised half of the rows to the partner (O through the
+        // output rows the partner then overwrites, the row weight log2(l) + m into its shared
+        // memory), and the warps of this CTA's head wait for the partner's half and merge.
         auto epilogue = [&](int e_row0, int e_nq, int e_h0, float e_l) {
             if (!warp_wait(bar_pv_done, (g - 1) & 1)) return false;
             float l_other;   // posted by the partner when its item ended
@@ -787,6 +881,60 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
             tc_fence_before();
             return true;
         };
+        // The same for the CTA's last item, which may be split over the pair (a split item is
+        // always the last of its CTAs, so only this form carries the exchange).
+        auto epilogue_last = [&](int e_row0, int e_nq, int e_h0, float e_l, float e_m, bool e_x) {
+            if (!warp_wait(bar_pv_done, (g - 1) & 1)) return false;
+            float l_other;   // posted by the partner when its item ended
+            if (!pair_collect(l_other)) return false;
+            tc_fence_after();
+            uint32_t oo[32];
+            OASR_TMEM_LD32(tl + kCtColO + 64 * hd + 32 * hf, oo);
+            tmem_wait_ld();
+            const float l_row = e_l + l_other;
+            uint4* dst = reinterpret_cast<uint4*>(
+                             a.out + ((static_cast<long long>(e_row0) + i) * a.H + e_h0 + hd) * kHeadDim) + 4 * hf;
+            float co = 1.f / l_row, cp = 0.f;   // weights of this CTA's O and of the partner's
+            const uint32_t rank = blockIdx.x & 1;
+            if (e_x && hd == static_cast<int>(rank)) {
+                if (!__all_sync(0xffffffffu, ct_wait_cluster(bar_xchg, 0, s_abort))) return false;
+                if (i < e_nq) {
+                    const float w_own = e_m + __log2f(l_row);
+                    const float w_p = reinterpret_cast<const float*>(sm + SP::off_xw)[i];
+                    const float mw = fmaxf(w_own, w_p);
+                    const float ea = ex2_approx(w_own - mw), eb = ex2_approx(w_p - mw);
+                    const float inv = 1.f / (ea + eb);
+                    co = ea * inv / l_row;
+                    cp = eb * inv;
+                }
+            }
+            if (i < e_nq) {
+                uint32_t w[16];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 part = cp != 0.f ? __ldcg(dst + c) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t pw[4] = {part.x, part.y, part.z, part.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float lo = __uint_as_float(oo[8 * c + 2 * e]) * co;
+                        float hi = __uint_as_float(oo[8 * c + 2 * e + 1]) * co;
+                        if (cp != 0.f) {
+                            lo += __uint_as_float(pw[e] << 16) * cp;
+                            hi += __uint_as_float(pw[e] & 0xffff0000u) * cp;
+                        }
+                        w[4 * c + e] = pack_bf16(lo, hi);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                if (e_x && hd != static_cast<int>(rank) && hf == 0)
+                    ct_st_cluster_f32(ct_mapa(smem_addr(sm + SP::off_xw) + 4 * i, rank ^ 1u), e_m + __log2f(l_row));
+            }
+            // the half of the rows handed over: every lane of these warps signals the partner
+            if (e_x && hd != static_cast<int>(rank)) ct_arrive_cluster(ct_mapa(bar_xchg, rank ^ 1u));
+            tc_fence_before();
+            return true;
+        };
         // This warp's bf16 staging of the position term: row `lane` holds the 16-byte chunks
         // q0 .. q0+4 of its window (q0 = w0 / 4, w0 = (31 - lane) / 2 the first word it reads)
         // at 4 (5 lane + 2 (lane / 8)) words, so that both the chunk stores (the eight lanes of
@@ -801,7 +949,6 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
         for (int k = 0; k < my_items && !*s_abort; ++k, ++it) {
             const CtItem itm = item_info(k);
             const int N = itm.nkeys;
-            const int n_st = (N + kCtBN - 1) / kCtBN;
             // packed: the keys this row sees, in the item's key numbering (none for padding rows)
             int win_lo = 0, win_hi = N;
             if constexpr (PK) {
@@ -819,7 +966,7 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
             }
             float m_used = -INFINITY, l_sum = 0.f;
             bool ok = true;
-            for (int s = 0; s < n_st; ++s, ++g) {
+            for (int s = itm.s_lo; s < itm.s_hi; ++s, ++g) {
                 if (!warp_wait(bar_sg_full, sg & 1)) { ok = false; break; }
                 ++sg;
                 tc_fence_after();
@@ -886,12 +1033,12 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
                 if (lane == 0) mbar_arrive(bar_bempty + 8 * (g & 1));
                 // last stage of the item: the next item's A tiles, so that its first S/G can be
                 // issued while this stage's softmax and the epilogue run
-                if (!PK && s + 1 == n_st && k + 1 < my_items) {
+                if (!PK && s + 1 == itm.s_hi && k + 1 < my_items) {
                     const CtItem nx1 = item_info(k + 1);
                     if (!warp_wait(bar_q_free, it & 1) || !prep_q(it + 1, nx1.h0, nx1.nq)) { ok = false; break; }
                 }
                 // the previous item's O, now that this first stage's S/G are read
-                if (s == 0 && have_prev) {
+                if (s == itm.s_lo && have_prev) {
                     if (!epilogue(p_row0, p_nq, p_h0, p_l)) { ok = false; break; }
                     have_prev = false;
                 }
@@ -917,12 +1064,12 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
                 float mx = fmaxf(mx0, mx1) * a.scale_log2, mx_other;
                 pair_post(mx);
                 // P.V of the previous stage must be done before P and O are touched
-                if (s > 0 && !warp_wait(bar_pv_done, (g - 1) & 1)) { ok = false; break; }
+                if (s > itm.s_lo && !warp_wait(bar_pv_done, (g - 1) & 1)) { ok = false; break; }
                 if (!pair_collect(mx_other)) { ok = false; break; }
                 mx = fmaxf(mx, mx_other);
                 const bool rescale = mx > m_used + 8.f;   // keeps every P <= 2^8 between rescales
                 const float m_new = rescale ? mx : m_used;
-                if (s > 0 && __any_sync(0xffffffffu, rescale)) {
+                if (s > itm.s_lo && __any_sync(0xffffffffu, rescale)) {
                     const float alpha = ex2_approx(m_used - m_new);
                     l_sum *= alpha;
                     tc_fence_after();
@@ -980,9 +1127,17 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
             p_nq = itm.nq;
             p_h0 = itm.h0;
             p_l = l_sum;
+            if (!PK && k + 1 == my_items) reinterpret_cast<float*>(sm + SP::off_mlast)[tid] = m_used;
             have_prev = true;
         }
-        if (all_ok && have_prev && !*s_abort) epilogue(p_row0, p_nq, p_h0, p_l);
+        // the last item's O
+        if (all_ok && have_prev && !*s_abort) {
+            if constexpr (PK)
+                epilogue(p_row0, p_nq, p_h0, p_l);
+            else
+                epilogue_last(p_row0, p_nq, p_h0, p_l, reinterpret_cast<const float*>(sm + SP::off_mlast)[tid],
+                              item_info(my_items - 1).xchg);
+        }
     }
     grid_dep_trigger();
     // every role has stopped issuing and the MMA issuer has drained the tensor pipe
@@ -992,11 +1147,44 @@ __global__ void __launch_bounds__(ct_threads<PK>(), 1) chunk_attn_tc_kernel(
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCtTmemCols));
     }
+    // a CTA of a pair stays until its partner no longer writes into its shared memory
+    if (pairs) ct_cluster_sync();
     if (tid == 0 && *s_abort) err |= kErrTimeout;
     if (err) atomicOr(a.status, err);
 }
 
 int g_smem_done_ct[2][64];
+
+// How many CTA pairs (clusters of two) of the streaming kernel the current device holds at
+// once; 0 if it cannot tell.  Looked up once per device.
+int ct_pair_capacity(int threads, int smem)
+{
+    static std::mutex mu;
+    static int cap[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cap[dev] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(threads);
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, chunk_attn_tc_kernel<false>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        cap[dev] = n > 0 ? n : -1;
+    }
+    return cap[dev] > 0 ? cap[dev] : 0;
+}
 
 }  // namespace
 
@@ -1026,7 +1214,7 @@ oasr_status launch_chunk_tc(const void* q, const void* k_pool, const void* v_poo
     if (!chunk_tc_takes(B, T, H, mbps, num_blocks, block_size, R)) return OASR_ERR_UNSUPPORTED;
     const int sms = sm_count();
     const long long n_items = static_cast<long long>(B) * (H / 2);
-    const int grid = static_cast<int>(n_items < sms ? n_items : sms);
+    int grid = static_cast<int>(n_items < sms ? n_items : sms);
     const int box = block_size < kCtBN ? block_size : kCtBN;
     CUtensorMap tm_q, tm_k, tm_v, tm_r;
     if (!encode_rows_bf16(&tm_q, q, static_cast<long long>(B) * T, H, kCtTq) ||
@@ -1058,8 +1246,37 @@ oasr_status launch_chunk_tc(const void* q, const void* k_pool, const void* v_poo
     a.sign = scale < 0.f ? 0x80008000u : 0u;
     // > 0 even for a zero scale, so that a masked score (-inf) times it stays -inf
     a.scale_log2 = fmaxf(fabsf(scale) * 1.4426950408889634f, 1e-30f);
-    return launch_pdl(chunk_attn_tc_kernel<false>, dim3(grid), dim3(ct_threads<false>()), smem, stream, tm_q,
-                      tm_k, tm_v, tm_r, a);
+    // Items do not divide evenly over the SMs (at most half a wave left over): the leftover
+    // items are split by key stages over CTA pairs, so that no CTA runs a whole extra item.
+    a.n_full = a.n_split = a.split_base = 0;
+    const int pairs = ct_pair_capacity(ct_threads<false>(), smem);
+    if (pairs > 0) {
+        const long long g2 = (2LL * pairs < sms ? 2LL * pairs : sms) & ~1LL;
+        const long long full = g2 > 0 ? n_items / g2 : 0, extra = n_items - full * g2;
+        if (g2 >= 2 && extra > 0 && extra <= g2 / 2 && full + 1 <= kCtMaxItems) {
+            grid = static_cast<int>(full > 0 ? g2 : 2 * extra);
+            a.n_full = static_cast<int>(full);
+            a.n_split = static_cast<int>(extra);
+            a.split_base = static_cast<int>(full * g2);
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(ct_threads<false>());
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.n_split > 0 ? 2 : 1;
+    if (cudaLaunchKernelEx(&cfg, chunk_attn_tc_kernel<false>, tm_q, tm_k, tm_v, tm_r, a) != cudaSuccess)
+        return OASR_ERR_CUDA;
+    return launch_status();
 }
 
 // Host launcher of the packed mode (oasr_packed_relattn_chunked, bf16, chunk_size >= 1): returns

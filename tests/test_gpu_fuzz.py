@@ -132,6 +132,50 @@ def _packed_params(seed):
     return rng, dict(lengths=lengths, H=H, dtype=dtype, window=window, r_extra=r_extra)
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
+@pytest.mark.parametrize("shape", ["whole_and_split", "all_split"])
+def test_tensor_core_items_split_over_pairs(shape, fused):
+    """Chunks of 33-64 frames whose (stream, head pair) items do not divide evenly over the SMs:
+    the leftover items run split by key stages over CTA pairs, each CTA finishing one head of
+    the item.  Cohort sizes taken from the device's SM count reach both forms (whole items plus
+    split ones, every item split); cache lengths of 0 among the split items give items of one
+    stage (kept whole), and a second identical call returns the same bits."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H, T, bs = 4, 40, 16                     # two head pairs per stream
+    n_items = sms + sms // 4 if shape == "whole_and_split" else max(sms // 2 - 4, 4)
+    B = n_items // 2
+    rng = np.random.default_rng(61 if shape == "whole_and_split" else 62)
+    Cs = [int(c) for c in rng.integers(0, 300, size=B)]
+    Cs[-1] = Cs[-3] = 0                      # one-stage items among the last (split) ones
+    Cs[-2] = 299
+    x = _stream_inputs(rng, T, bs, H, B, Cs, "bf16", 1, 0)
+    d = {k: dev(x[k], "bf16") for k in ("q", "k_new", "v_new", "pos_bias_u", "pos_bias_v", "rel")}
+    kp, vp = dev_pool(x["k_pool"], "bf16"), dev_pool(x["v_pool"], "bf16")
+    bt = torch.from_numpy(x["block_table"]).cuda()
+    cs = torch.from_numpy(x["cache_seqlens"]).cuda()
+    outs = []
+    for rep in range(2):
+        if fused:
+            if rep:   # the pool back to its state before the step
+                kp.copy_(dev_pool(x["k_pool"], "bf16"))
+                vp.copy_(dev_pool(x["v_pool"], "bf16"))
+            outs.append(capi.oasr_chunk_step_paged(d["q"], d["k_new"], d["v_new"], kp, vp, bt, cs,
+                                                   d["pos_bias_u"], d["pos_bias_v"], d["rel"]))
+        else:
+            if not rep:
+                capi.oasr_paged_append(d["k_new"], d["v_new"], kp, vp, bt, cs)
+            outs.append(capi.oasr_chunk_relattn_paged(d["q"], kp, vp, bt, cs, d["pos_bias_u"],
+                                                      d["pos_bias_v"], d["rel"]))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    got = to_np(outs[0])
+    for b, (ck, cv) in enumerate(x["caches"]):
+        ref = oracle.chunk_relattn(x["q"][b:b + 1], ck, cv, x["k_new"][b:b + 1],
+                                   x["v_new"][b:b + 1], x["pos_bias_u"], x["pos_bias_v"], x["rel"])
+        check_close(got[b:b + 1], ref, "bf16", f"{shape} B={B}, stream {b} (C={Cs[b]})")
+    assert capi.oasr_device_status() == 0
+
+
 @pytest.mark.parametrize("seed", range(24))
 def test_random_packed_row(seed):
     rng, p = _packed_params(seed)
