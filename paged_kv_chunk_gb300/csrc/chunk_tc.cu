@@ -57,6 +57,12 @@
 // {64, key % 8, head, key / 8}, so that each head's 8 consecutive keys form one 128-byte-
 // swizzled 1 KB atom; one box per page instead of one per page and head halves the copies the
 // SM's TMA unit issues); a block id outside the pool reads as zero rows.
+// Streaming items that leave at most half a wave over the SMs are split: the leftover items
+// run by key stages on the two CTAs of a cluster (the even one the first half of the stages),
+// each CTA finishing one head of the item.  The warps of the other head hand their normalised
+// rows over through that head's output rows (which the partner then overwrites) and their
+// row weights log2(l) + m through the partner's shared memory, signalling an mbarrier there;
+// the partner merges the two halves as two softmax blocks of the same row.
 // Every wait is bounded; a wait that runs out raises the timeout bit and aborts the CTA's
 // remaining work, after which the CTA still drains its copies and tensor-core work and frees
 // its TMEM.
